@@ -1,0 +1,360 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each pin is independent of the oracle's code: a hand-worked example stored
+under tests/golden/, a closed form, a library routine (torch.histc,
+torch bf16 conversion, torch silu, a dense matmul), brute force written here
+in plain Python, or an invariant of the method.  The last group plants
+plausible mistakes in the oracle (on the CPU) and checks that a pin fails.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import mc2_oracle as orc
+from moe_expert_dispatch_histc_gb300.workloads import (
+    WORKLOADS, make_inputs, make_routing, as_f64)
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _small_case(seed, T=16, H=8, I=4, E=4, k=2, W=2, shared=False):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, H))
+    if shared:
+        w1 = np.repeat(rng.standard_normal((1, H, 2 * I)), E, axis=0)
+        w2 = np.repeat(rng.standard_normal((1, I, H)), E, axis=0)
+    else:
+        w1 = rng.standard_normal((E, H, 2 * I))
+        w2 = rng.standard_normal((E, I, H))
+    logits = rng.standard_normal((T, E))
+    sel = np.argsort(-logits, axis=1, kind="stable")[:, :k].astype(np.int32)
+    p = rng.uniform(0.1, 1.0, (T, k))
+    p = p / p.sum(axis=1, keepdims=True)
+    return x, w1, w2, sel, p
+
+
+# ---------------------------------------------------------------- histc
+def test_histc_matches_torch_histc():
+    rng = np.random.default_rng(0)
+    for E in (1, 3, 8, 64):
+        v = rng.integers(-2, E + 2, size=1000)
+        ref = torch.histc(torch.tensor(v, dtype=torch.float64), bins=E, min=0, max=E)
+        assert np.array_equal(orc.histc(v, E, 0, E), ref.numpy().astype(np.int64))
+        f = rng.uniform(-1, E + 1, size=1000)
+        ref = torch.histc(torch.tensor(f), bins=E, min=0, max=E)
+        assert np.array_equal(orc.histc(f, E, 0, E), ref.numpy().astype(np.int64))
+
+
+def test_counts_worked_example():
+    g = _golden("counts_worked_example.json")
+    sel = np.array(g["selected_experts"], dtype=np.int32)
+    E, W = g["E"], g["W"]
+    cnt = orc.rank_counts(sel, E, W)
+    assert cnt.tolist() == g["num_global"]
+    send, recv = orc.send_recv_counts(cnt, W)
+    assert [s.tolist() for s in send] == g["send_counts"]
+    assert [r.tolist() for r in recv] == g["recv_counts"]
+    assert orc.expert_offsets(cnt).tolist() == g["offsets"]
+    rows, idx = orc.permute(np.arange(g["T"]), sel, E)
+    assert idx.tolist() == g["permute_src"]
+    assert rows.tolist() == g["permuted_token"]
+    res = orc.block_forward(np.zeros((4, 2)), np.zeros((E, 2, 2)), np.zeros((E, 1, 2)),
+                            sel, np.full((4, 2), 0.5), E, W)
+    assert res["unpermute_dst"].tolist() == g["unpermute_dst"]
+
+
+def _brute_counts(sel, E, W):
+    T, k = sel.shape
+    Tl = T // W
+    cnt = [[0] * E for _ in range(W)]
+    for t in range(T):
+        for j in range(k):
+            e = int(sel[t, j])
+            if 0 <= e < E:
+                cnt[t // Tl][e] += 1
+    return cnt
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_counts_brute_force_and_invariants(seed):
+    rng = np.random.default_rng(seed)
+    T, k, E, W = 24, 3, 6, 3
+    sel = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    cnt = orc.rank_counts(sel, E, W)
+    assert cnt.tolist() == _brute_counts(sel, E, W)
+    assert cnt.sum() == T * k                              # counts sum to T*k
+    assert all(cnt[r].sum() == (T // W) * k for r in range(W))
+    send, recv = orc.send_recv_counts(cnt, W)
+    El = E // W
+    assert sum(int(r.sum()) for r in recv) == T * k        # everything sent is received
+    for r in range(W):                                     # recv_r[s*El+le] = send_s[r*El+le]
+        for s in range(W):
+            for le in range(El):
+                assert recv[r][s * El + le] == send[s][r * El + le]
+
+
+def test_counts_skip_invalid_ids():
+    sel = np.array([[0, 4], [-1, 1], [3, 3], [2, 5]], dtype=np.int32)
+    cnt = orc.rank_counts(sel, 4, 2)
+    assert cnt.tolist() == _brute_counts(sel, 4, 2)
+    assert cnt.sum() == 5
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_permutation_is_stable_sort_by_expert(seed):
+    rng = np.random.default_rng(seed)
+    T, k, E = 30, 4, 7
+    sel = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    _, idx = orc.permute(np.arange(T), sel, E)
+    flat = sel.reshape(-1).tolist()
+    brute = sorted(range(T * k), key=lambda i: (flat[i], i))   # (expert, t, j)
+    assert idx.tolist() == brute
+    assert sorted(idx.tolist()) == list(range(T * k))
+
+
+def test_permute_then_unpermute_is_identity():
+    rng = np.random.default_rng(3)
+    T, k, E, H = 32, 4, 8, 5
+    x = rng.standard_normal((T, H))
+    sel = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    rows, idx = orc.permute(x, sel, E)
+    back = orc.unpermute(rows, idx, np.full((T, k), 1.0 / k))
+    assert np.array_equal(back, x)                          # 1/k = 2**-2: exact
+    # one-hot probs select one slot: still the identity
+    oh = np.zeros((T, k))
+    oh[np.arange(T), rng.integers(0, k, T)] = 1.0
+    assert np.array_equal(orc.unpermute(rows, idx, oh), x)
+
+
+# ---------------------------------------------------------------- rounding and silu
+def test_round_to_bf16_matches_torch():
+    rng = np.random.default_rng(0)
+    bits = rng.integers(0, 2 ** 32, size=200000, dtype=np.uint64).astype(np.uint32)
+    f = bits.view(np.float32)
+    f = f[np.isfinite(f) & (np.abs(f) >= 2.0 ** -126) & (np.abs(f) < 3e38)]
+    ref = torch.from_numpy(f.copy()).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(orc.round_to_bf16(f.astype(np.float64)), ref)
+    # ties go to even
+    assert orc.round_to_bf16(np.array([1 + 2 ** -8]))[0] == 1.0
+    assert orc.round_to_bf16(np.array([1 + 3 * 2 ** -8]))[0] == 1 + 2 ** -6
+    assert orc.round_to_bf16(np.array([0.0]))[0] == 0.0
+
+
+def test_silu_pins():
+    g = np.linspace(-30, 30, 2001)
+    ref = torch.nn.functional.silu(torch.tensor(g)).numpy()
+    assert np.allclose(orc.silu(g), ref, rtol=1e-14, atol=1e-300)
+    assert orc.silu(np.array([0.0]))[0] == 0.0
+    assert abs(orc.silu(np.array([50.0]))[0] - 50.0) < 1e-15 * 50
+    assert abs(orc.silu(np.array([math.log(3)]))[0] - 0.75 * math.log(3)) < 1e-15
+
+
+def test_swiglu_closed_form():
+    g = _golden("swiglu_closed_form.json")
+    ln3 = math.log(3.0)
+    gate = np.array(g["w1_gate_over_ln3"]) * ln3
+    up = np.array(g["w1_up"])
+    w1 = np.concatenate([gate, up], axis=2)
+    w2 = np.array(g["w2"])
+    sel = np.array(g["selected_experts"], dtype=np.int32)
+    probs = np.array(g["probs"])
+    out = orc.block_forward(np.array(g["x"]), w1, w2, sel, probs, g["E"], g["W"])["out"]
+    assert np.allclose(out, np.array(g["out_over_ln3"]) * ln3, rtol=1e-14, atol=1e-15)
+
+
+# ---------------------------------------------------------------- the block
+def _brute_python(x, w1, w2, sel, probs):
+    """Plain-Python per-token formula: out[t] = sum_j p * swiglu(x w1[e]) w2[e]."""
+    T, H = x.shape
+    I = w2.shape[1]
+    out = [[0.0] * H for _ in range(T)]
+    for t in range(T):
+        for j in range(sel.shape[1]):
+            e = int(sel[t, j])
+            g = [sum(x[t, a] * w1[e, a, n] for a in range(H)) for n in range(2 * I)]
+            h = [g[n] / (1.0 + math.exp(-g[n])) * g[I + n] for n in range(I)]
+            for c in range(H):
+                out[t][c] += probs[t, j] * sum(h[n] * w2[e, n, c] for n in range(I))
+    return np.array(out)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_block_matches_python_brute_force(seed):
+    x, w1, w2, sel, p = _small_case(seed)
+    ref = _brute_python(x, w1, w2, sel, p)
+    got = orc.block_forward(x, w1, w2, sel, p, E=4, W=2)["out"]
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_block_matches_rankwise_alltoallv_flow(seed):
+    x, w1, w2, sel, p = _small_case(seed, T=24, E=6, k=3, W=3)
+    a = orc.block_forward(x, w1, w2, sel, p, E=6, W=3)["out"]
+    b = orc.ep_mc2_forward_emulated(x, w1, w2, sel, p, E=6, W=3)
+    assert np.allclose(a, b, rtol=1e-13, atol=1e-13)
+    for t in range(0, 24, 5):
+        c = orc.brute_force_token(x[t], w1, w2, sel[t], p[t], 6)
+        assert np.allclose(a[t], c, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_shared_weights_reduce_to_dense_swiglu_mlp(seed):
+    x, w1, w2, sel, p = _small_case(seed, T=20, H=16, I=8, E=5, k=3, W=1, shared=True)
+    xt = torch.tensor(x)
+    g = xt @ torch.tensor(w1[0])
+    dense = (torch.nn.functional.silu(g[:, :8]) * g[:, 8:]) @ torch.tensor(w2[0])
+    got = orc.block_forward(x, w1, w2, sel, p, E=5, W=1)["out"]
+    assert np.allclose(got, dense.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_invalid_ids_contribute_nothing():
+    x, w1, w2, sel, p = _small_case(5, T=8, E=4, k=2, W=2)
+    bad = sel.copy()
+    bad[1, 0] = 4
+    bad[6, 1] = -3
+    res = orc.block_forward(x, w1, w2, bad, p, E=4, W=2)
+    assert res["offsets"][-1] == 14
+    assert sorted(res["permute_src"][14:].tolist()) == [2, 13]   # flat t*k+j
+    for t in range(8):
+        ref = orc.brute_force_token(x[t], w1, w2, bad[t], p[t], 4)
+        assert np.allclose(res["out"][t], ref, rtol=1e-13, atol=1e-13)
+
+
+def test_tiny_workload_end_to_end():
+    wl = WORKLOADS["tiny"]
+    d = make_inputs(wl, 0)
+    x, w1, w2 = (as_f64(d[n], wl.act) for n in ("x", "w1", "w2"))
+    res = orc.block_forward(x, w1, w2, d["sel"], d["probs"], wl.E, wl.W, h_dtype="f32")
+    b = orc.ep_mc2_forward_emulated(x, w1, w2, d["sel"], d["probs"], wl.E, wl.W, h_dtype="f32")
+    assert np.allclose(res["out"], b, rtol=1e-12, atol=1e-15)
+    assert res["cnt"].sum() == wl.T * wl.k
+
+
+# ---------------------------------------------------------------- int8 path
+def test_quant_block_integer_parts_by_brute_force():
+    rng = np.random.default_rng(0)
+    T, H, I, E, k, W = 8, 6, 3, 4, 2, 2
+    xq = rng.integers(-127, 128, (T, H)).astype(np.int8)
+    w1q = rng.integers(-127, 128, (E, H, 2 * I)).astype(np.int8)
+    w2q = rng.integers(-127, 128, (E, I, H)).astype(np.int8)
+    xs = rng.uniform(1e-3, 1e-2, T).astype(np.float32)
+    w1s = rng.uniform(1e-3, 1e-2, (E, 2 * I)).astype(np.float32)
+    w2s = rng.uniform(1e-3, 1e-2, (E, H)).astype(np.float32)
+    sel = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    probs = np.full((T, k), 0.5, np.float32)
+    r = orc.quant_block_forward(xq, xs, w1q, w1s, w2q, w2s, sel, probs, E, W)
+    src = r["permute_src"]
+    for p in range(T * k):
+        t, j = divmod(int(src[p]), k)
+        e = int(sel[t, j])
+        for n in range(2 * I):
+            acc = sum(int(xq[t, a]) * int(w1q[e, a, n]) for a in range(H))
+            assert r["acc1"][p, n] == acc
+            assert r["h"].shape == (T * k, I)
+            # dequant formula (x1_scale * x2_scale) * (x1 @ x2), no bias
+            assert math.isclose(
+                (float(xs[t]) * float(w1s[e, n])) * acc,
+                float(xs[t]) * float(w1s[e, n]) * acc, rel_tol=1e-15)
+        for c in range(H):
+            acc2 = sum(int(r["hq"][p, i]) * int(w2q[e, i, c]) for i in range(I))
+            assert r["acc2"][p, c] == acc2
+
+
+def test_quant_worst_case_accumulator_fits_int32():
+    K = 3072
+    xq = np.full((1, K), -127, np.int8)
+    w = np.full((1, K, 2), 127, np.int8)
+    w[0, :, 1] = -127
+    xs = np.ones(1, np.float32)
+    ws = np.ones((1, 2), np.float32)
+    w2 = np.ones((1, 1, 4), np.int8)
+    r = orc.quant_block_forward(xq, xs, w, ws, w2, np.ones((1, 4), np.float32),
+                                np.zeros((1, 1), np.int32), np.ones((1, 1), np.float32), 1, 1)
+    assert r["acc1"][0, 0] == -K * 127 * 127
+    assert abs(int(r["acc1"][0, 0])) < 2 ** 31
+
+
+def test_requant_rows_properties():
+    rng = np.random.default_rng(1)
+    h = rng.standard_normal((50, 37)) * rng.uniform(1e-3, 10, (50, 1))
+    h[3] = 0.0
+    hq, hs = orc.requant_rows(h)
+    assert hq.dtype == np.int8 and np.abs(hq.astype(int)).max() <= 127
+    nz = np.abs(h).max(axis=1) > 0
+    assert np.all(np.abs(hq[nz].astype(int)).max(axis=1) == 127)   # the row max maps to +-127
+    assert np.all(hq[3] == 0) and hs[3] == 1.0
+    err = np.abs(hq.astype(np.float64) * hs[:, None] - h)
+    assert np.all(err <= hs[:, None] * (0.5 + 1e-5))
+
+
+def test_tolerance_rule():
+    ref = np.array([1.0, -2.0, 4.0])
+    assert orc.bf16_tolerance_ok(ref + 1e-4, ref)[0]
+    assert not orc.bf16_tolerance_ok(ref + np.array([0, 0, 0.05]), ref)[0]     # max rule
+    assert not orc.bf16_tolerance_ok(ref * 1.003, ref)[0]                      # mean rule
+
+
+# ---------------------------------------------------------------- planted mistakes
+def _mut_swap_gate_up(gu):
+    I = gu.shape[1] // 2
+    return orc.silu(gu[:, I:]) * gu[:, :I]
+
+
+def _mut_sign(g):
+    g = np.asarray(g, dtype=np.float64)
+    return g / (1.0 + np.exp(g))
+
+
+@pytest.mark.parametrize("mutation", ["swap_gate_up", "silu_sign", "transposed_recv",
+                                      "unstable_permute", "drop_prob", "off_by_one_rank"])
+def test_planted_mistakes_are_caught(monkeypatch, mutation):
+    """Each plausible mistake, planted in the oracle, makes some pin fail."""
+    if mutation == "swap_gate_up":
+        monkeypatch.setattr(orc, "swiglu", _mut_swap_gate_up)
+    elif mutation == "silu_sign":
+        monkeypatch.setattr(orc, "silu", _mut_sign)
+    elif mutation == "transposed_recv":
+        def bad(num_global, W):
+            El = num_global.shape[1] // W
+            send = [num_global[r].copy() for r in range(W)]
+            recv = [num_global[:, r * El:(r + 1) * El].T.reshape(-1).copy() for r in range(W)]
+            return send, recv
+        monkeypatch.setattr(orc, "send_recv_counts", bad)
+    elif mutation == "unstable_permute":
+        real = orc.permute
+
+        def bad(hidden, sel, E=None):
+            rows, idx = real(hidden, sel, E)
+            return rows[::-1], idx[::-1]
+        monkeypatch.setattr(orc, "permute", bad)
+    elif mutation == "drop_prob":
+        real_un = orc.unpermute
+        monkeypatch.setattr(orc, "unpermute",
+                            lambda y, i, p, valid_rows=None: real_un(y, i, np.ones_like(p), valid_rows))
+    elif mutation == "off_by_one_rank":
+        def bad(sel, E, W):
+            T, k = sel.shape
+            Tl = T // W
+            return np.stack([orc.histc(sel[max(0, r * Tl - 1):(r + 1) * Tl - 1].reshape(-1), E, 0, E)
+                             for r in range(W)])
+        monkeypatch.setattr(orc, "rank_counts", bad)
+    failures = 0
+    for fn in (test_counts_worked_example, test_permute_then_unpermute_is_identity,
+               test_swiglu_closed_form, lambda: test_block_matches_python_brute_force(0),
+               lambda: test_block_matches_rankwise_alltoallv_flow(0),
+               lambda: test_counts_brute_force_and_invariants(0),
+               lambda: test_permutation_is_stable_sort_by_expert(0)):
+        try:
+            fn()
+        except (AssertionError, ValueError, IndexError):
+            failures += 1
+    assert failures > 0, f"no pin caught the planted mistake {mutation}"
