@@ -1,0 +1,185 @@
+/*
+ * mc2moe.h -- C ABI of the GB300 (sm_103a) MoE expert block.
+ *
+ * The block is the expert-parallel forward of "NPU Training Operators - MC2"
+ * (shaojiemike.top), section "Execution path": histc per-expert token counts,
+ * the all_gather of those counts, send_counts / recv_counts, permute, the
+ * fc1 grouped matmul, SwiGLU, the fc2 grouped matmul and the routing-weighted
+ * unpermute.  Here the W expert-parallel ranks are logical: rank r owns tokens
+ * [r*T/W, (r+1)*T/W) and experts [r*E/W, (r+1)*E/W) of one GPU, so the two
+ * AllToAllv exchanges become a row gather folded into the fc1 operand load
+ * and a scatter/sum folded into the fc2 epilogue.  The int8 variant uses the
+ * dequantisation of "torch_npu.npu_mm_reduce_scatter_base" (Ascend op-plugin
+ * docs), section "Function description": (x1_scale * x2_scale) * (x1 @ x2),
+ * with no bias.
+ *
+ * Conventions for every entry point
+ *  - Pointers marked [dev] are CUDA device pointers; the caller owns every
+ *    buffer, including the workspace `ws` and the device status word.  The
+ *    library never allocates, frees or synchronises; all work is enqueued on
+ *    `stream`, in order.  Inputs are read-only; outputs are fully written.
+ *  - Tensors are dense row-major with the shapes given; element types follow
+ *    mc2_shape_t.act (activations and weights) and mc2_shape_t.out.
+ *  - A synchronous return other than MC2_OK means nothing was enqueued.
+ *  - Conditions found on the device (an expert id outside [0, E); a bounded
+ *    device-side wait that expired) are OR-ed into *dev_status as
+ *    MC2_DEV_* bits; read it after synchronising `stream`.  dev_status may be
+ *    NULL, in which case those conditions are not reported.
+ *  - Ids outside [0, E) are never used as addresses: they are left out of
+ *    every count, sorted after every valid pair in the permutation, skipped
+ *    by both matmuls and contribute zero to the combine.
+ */
+#ifndef MC2MOE_H
+#define MC2MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MC2_OK = 0,
+  MC2_ERR_INVALID_ARG = 1,    /* shape rule or pointer rule broken; nothing launched */
+  MC2_ERR_UNSUPPORTED = 2,    /* valid request this build does not implement */
+  MC2_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
+  MC2_ERR_DEVICE_TIMEOUT = 4, /* never returned synchronously: the device reports MC2_DEV_TIMEOUT;
+                                 the code exists so callers can map that bit to a status */
+  MC2_ERR_BAD_EXPERT_ID = 5   /* likewise, for the MC2_DEV_BAD_EXPERT_ID bit */
+} mc2_status_t;
+
+/* bits of the device status word */
+#define MC2_DEV_BAD_EXPERT_ID 0x1
+#define MC2_DEV_TIMEOUT 0x2
+
+typedef enum {
+  MC2_F32 = 0,   /* fp32 values; matmuls on tensor cores in tf32 (inputs rounded to nearest) */
+  MC2_BF16 = 1,  /* bf16 values, fp32 accumulation */
+  MC2_I8 = 2,    /* int8 values with fp32 per-token / per-channel scales, exact int32 accumulation */
+  MC2_I32 = 3    /* out only, with act = MC2_I8: raw int32 accumulators (test mode) */
+} mc2_dtype_t;
+
+typedef struct {
+  int32_t T;    /* tokens (rows of hidden_states after view(-1, H)) */
+  int32_t H;    /* hidden size; multiple of 64 */
+  int32_t I;    /* per-expert intermediate size; fc1 emits 2I (gate | up); multiple of 64 */
+  int32_t E;    /* experts, 1..1024; E % W == 0 */
+  int32_t k;    /* top-k, 1..E */
+  int32_t W;    /* logical expert-parallel ranks; T % W == 0 and E % W == 0 */
+  int32_t act;  /* mc2_dtype_t of x, w1, w2 (and of h for F32/BF16) */
+  int32_t out;  /* mc2_dtype_t of the block output: F32 (act F32), BF16 (act BF16 or I8),
+                   or I32 (act I8, accumulator test mode) */
+} mc2_shape_t;
+
+/* Check a shape against the rules above.  Host only, pure. */
+mc2_status_t mc2_check_shape(const mc2_shape_t* s);
+
+/* Bytes of device workspace the block needs for this shape (0 for an invalid
+ * shape).  Host only, pure and deterministic; the same workspace serves all
+ * entry points below.  Alignment: 256 bytes. */
+size_t mc2_workspace_bytes(const mc2_shape_t* s);
+
+/*
+ * mc2_moe_counts -- steps 2-6 of the execution path: per-rank histc, the
+ * logical all_gather, send/recv counts and the permutation indices.
+ *   sel            [dev] int32 [T, k]  selected_experts (flat index i = t*k + j)
+ *   cnt            [dev] int32 [W, E]  out: num_global_tokens_per_expert; row r is
+ *                                      rank r's histc(bins=E, min=0, max=E) of its
+ *                                      own tokens, i.e. its send_counts
+ *   recv           [dev] int32 [W, W*E/W] out: recv_counts of rank r =
+ *                                      cnt[:, r*E_l:(r+1)*E_l].reshape(-1)
+ *                                      (source-rank-major), E_l = E/W
+ *   offsets        [dev] int32 [E + 1] out: first permuted row of each expert;
+ *                                      offsets[E] = number of valid pairs
+ *   permute_src    [dev] int32 [T*k]   out: flat index of the pair in permuted row p;
+ *                                      rows ordered by (expert, t, j) -- a stable
+ *                                      sort by expert; invalid ids last
+ *   unpermute_dst  [dev] int32 [T*k]   out: inverse of permute_src
+ *   ws             [dev] workspace of mc2_workspace_bytes(s)
+ */
+mc2_status_t mc2_moe_counts(const mc2_shape_t* s, const int32_t* sel, int32_t* cnt,
+                            int32_t* recv, int32_t* offsets, int32_t* permute_src,
+                            int32_t* unpermute_dst, void* ws, int32_t* dev_status,
+                            void* stream);
+
+/*
+ * mc2_alltoallv_gmm -- dispatch segment, steps 6-8: the permute (a gather of
+ * token rows by permute_src), the fc1 grouped matmul and SwiGLU, named after
+ * npu_alltoallv_gmm of the same page, section "Low-level API comparison".
+ *   x         [dev] [T, H] act                 hidden_states
+ *   x_scale   [dev] fp32 [T]                   per-token scale (act I8 only, else NULL)
+ *   w1        [dev] [E, H, 2I] act             fc1_weight = gate_up_proj; columns
+ *                                              [0, I) gate, [I, 2I) up; y = x @ w1[e]
+ *   w1_scale  [dev] fp32 [E, 2I]               per-channel scale (act I8 only, else NULL)
+ *   offsets, permute_src                       from mc2_moe_counts
+ *   h         [dev] out, permuted (expert-major) rows:
+ *                act BF16/F32: [T*k, I] act, h = silu(gate) * up
+ *                act I8, out BF16: [T*k, I] int8, h re-quantised per row
+ *                act I8, out I32: [T*k, 2I] int32, the raw fc1 accumulators
+ *             rows p >= offsets[E] are not written.
+ *   h_scale   [dev] fp32 [T*k] out (act I8 and out BF16 only, else NULL):
+ *             per-row scale of the int8 h (max|h| / 127, 1 for an all-zero row)
+ */
+mc2_status_t mc2_alltoallv_gmm(const mc2_shape_t* s, const void* x, const float* x_scale,
+                               const void* w1, const float* w1_scale, const int32_t* offsets,
+                               const int32_t* permute_src, void* ws, void* h, float* h_scale,
+                               int32_t* dev_status, void* stream);
+
+/*
+ * mc2_gmm_alltoallv -- combine segment, steps 9-10: the fc2 grouped matmul
+ * and the unpermute with probs, named after npu_gmm_alltoallv.
+ *   h, h_scale         [dev] as produced by mc2_alltoallv_gmm (h_scale: act I8 only)
+ *   w2        [dev] [E, I, H] act              fc2_weight = down_proj
+ *   w2_scale  [dev] fp32 [E, H]                per-channel scale (act I8 only, else NULL)
+ *   offsets, permute_src, unpermute_dst        from mc2_moe_counts
+ *   probs     [dev] fp32 [T, k]                routing_weights
+ *   out       [dev] out dtype:
+ *                F32/BF16: [T, H], out[t] = sum_j probs[t, j] * y(t, j), summed in
+ *                          fp32 in ascending j, one rounding at the end; the sum is
+ *                          bit-identical from run to run
+ *                I32 (act I8): [T*k, H] int32 raw fc2 accumulators, permuted rows;
+ *                          h is then the int8 h of an out=BF16 fc1 call
+ */
+mc2_status_t mc2_gmm_alltoallv(const mc2_shape_t* s, const void* h, const float* h_scale,
+                               const void* w2, const float* w2_scale, const int32_t* offsets,
+                               const int32_t* permute_src, const int32_t* unpermute_dst,
+                               const float* probs, void* ws, void* out, int32_t* dev_status,
+                               void* stream);
+
+/*
+ * mc2_moe_forward -- the whole block (the three calls above, in order) on
+ * device buffers.  cnt/recv/offsets/permute_src/unpermute_dst/h/h_scale are
+ * outputs as above (h_scale may be NULL unless act is I8); out is [T, H].
+ */
+mc2_status_t mc2_moe_forward(const mc2_shape_t* s, const void* x, const float* x_scale,
+                             const int32_t* sel, const float* probs, const void* w1,
+                             const float* w1_scale, const void* w2, const float* w2_scale,
+                             int32_t* cnt, int32_t* recv, int32_t* offsets,
+                             int32_t* permute_src, int32_t* unpermute_dst, void* h,
+                             float* h_scale, void* out, void* ws, int32_t* dev_status,
+                             void* stream);
+
+/*
+ * mc2_selftest_wait -- exercises the bounded device-side wait used by every
+ * kernel: one CTA waits on an mbarrier phase that nothing completes, gives up
+ * after `limit_ns` nanoseconds, ORs MC2_DEV_TIMEOUT into *dev_status and
+ * returns.  Test hook only; never hangs the GPU.
+ */
+mc2_status_t mc2_selftest_wait(uint64_t limit_ns, int32_t* dev_status, void* stream);
+
+/* Set the device-side wait limit (nanoseconds) used by later launches of
+ * this process; 0 restores the default (2 s). Host only. */
+void mc2_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Number of kernel launches the last successful call on this host thread
+ * enqueued. Host only. */
+int32_t mc2_last_launch_count(void);
+
+const char* mc2_status_str(mc2_status_t st);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MC2MOE_H */

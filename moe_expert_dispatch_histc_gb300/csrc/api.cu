@@ -1,0 +1,237 @@
+// api.cu -- the C ABI of libmc2moe: argument rules, workspace layout and the
+// order of launches for each entry point.  No allocation, no synchronisation.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+
+#include "internal.h"
+
+namespace mc2 {
+
+static std::atomic<uint64_t> g_wait_limit_ns{0};
+static thread_local int tl_launches = 0;
+
+uint64_t wait_limit_ns() {
+  const uint64_t v = g_wait_limit_ns.load();
+  return v ? v : 2000000000ull;  // 2 s
+}
+
+void note_launches(int n) { tl_launches += n; }
+
+WsLayout ws_layout(const mc2_shape_t& s) {
+  WsLayout L;
+  std::memset(&L, 0, sizeof(L));
+  const CountsGeom g = counts_geom(s);
+  const size_t R = static_cast<size_t>(s.T) * s.k;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, kWsAlign);
+    return at;
+  };
+  L.hist = take(static_cast<size_t>(g.EB) * g.G * 4);
+  L.base = take(static_cast<size_t>(g.EB) * g.G * 4);
+  L.slots = take(R * s.H * 4);
+  if (s.act == MC2_F32) {
+    L.x_t32 = take(static_cast<size_t>(s.T) * s.H * 4);
+    L.w1_t32 = take(static_cast<size_t>(s.E) * s.H * 2 * s.I * 4);
+    L.w2_t32 = take(static_cast<size_t>(s.E) * s.I * s.H * 4);
+  }
+  L.total = off > kWsAlign ? off : kWsAlign;  // never 0: 0 means "shape rejected"
+  return L;
+}
+
+}  // namespace mc2
+
+using namespace mc2;
+
+namespace {
+
+bool shape_ok(const mc2_shape_t* s) {
+  if (!s) return false;
+  if (s->T < 0 || s->H < 64 || s->I < 64 || s->H % 64 || s->I % 64) return false;
+  if (s->E < 1 || s->E > 1024 || s->k < 1 || s->k > s->E || s->W < 1) return false;
+  if (s->E % s->W || s->T % s->W) return false;
+  const int64_t R = static_cast<int64_t>(s->T) * s->k;
+  if (R >= (int64_t(1) << 31)) return false;
+  const bool combo = (s->act == MC2_F32 && s->out == MC2_F32) ||
+                     (s->act == MC2_BF16 && s->out == MC2_BF16) ||
+                     (s->act == MC2_I8 && (s->out == MC2_BF16 || s->out == MC2_I32));
+  return combo;
+}
+
+mc2_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MC2_OK : MC2_ERR_CUDA; }
+
+mc2_status_t do_counts(const mc2_shape_t* s, const int32_t* sel, int32_t* cnt, int32_t* recv,
+                       int32_t* offsets, int32_t* permute_src, int32_t* unpermute_dst, void* ws,
+                       int32_t* dev_status, cudaStream_t st) {
+  if (!cnt || !recv || !offsets || !ws) return MC2_ERR_INVALID_ARG;
+  if (s->T > 0 && (!sel || !permute_src || !unpermute_dst)) return MC2_ERR_INVALID_ARG;
+  return cuda_status(launch_counts(*s, sel, cnt, recv, offsets, permute_src, unpermute_dst,
+                                   static_cast<char*>(ws), dev_status, st));
+}
+
+mc2_status_t do_fc1(const mc2_shape_t* s, const void* x, const float* x_scale, const void* w1,
+                    const float* w1_scale, const int32_t* offsets, const int32_t* permute_src,
+                    void* ws, void* h, float* h_scale, int32_t* dev_status, cudaStream_t st) {
+  if (s->act == MC2_I8) return MC2_ERR_UNSUPPORTED;
+  if (x_scale || w1_scale || h_scale) return MC2_ERR_INVALID_ARG;
+  if (!offsets || !ws) return MC2_ERR_INVALID_ARG;
+  if (s->T > 0 && (!x || !w1 || !permute_src || !h)) return MC2_ERR_INVALID_ARG;
+  if (s->T == 0) return MC2_OK;
+  const WsLayout L = ws_layout(*s);
+  char* w = static_cast<char*>(ws);
+  GemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  g.s = s;
+  g.offsets = offsets;
+  g.permute_src = permute_src;
+  g.out = h;
+  g.dev_status = dev_status;
+  g.mode = 0;
+  if (s->act == MC2_F32) {
+    float* xr = reinterpret_cast<float*>(w + L.x_t32);
+    float* w1r = reinterpret_cast<float*>(w + L.w1_t32);
+    cudaError_t e = launch_round_tf32(static_cast<const float*>(x), xr,
+                                      static_cast<size_t>(s->T) * s->H, st);
+    if (e == cudaSuccess)  // [E, H, 2I] -> [E, 2I, H]
+      e = launch_transpose_round_tf32(static_cast<const float*>(w1), w1r, s->E, s->H, 2 * s->I, st);
+    if (e != cudaSuccess) return MC2_ERR_CUDA;
+    g.a = xr;
+    g.b = w1r;
+    g.a_elem_bytes = 4;
+  } else {
+    g.a = x;
+    g.b = w1;
+    g.a_elem_bytes = 2;
+  }
+  return cuda_status(launch_gemm(g, st));
+}
+
+mc2_status_t do_fc2(const mc2_shape_t* s, const void* h, const float* h_scale, const void* w2,
+                    const float* w2_scale, const int32_t* offsets, const int32_t* permute_src,
+                    const int32_t* unpermute_dst, const float* probs, void* ws, void* out,
+                    int32_t* dev_status, cudaStream_t st) {
+  if (s->act == MC2_I8) return MC2_ERR_UNSUPPORTED;
+  if (h_scale || w2_scale) return MC2_ERR_INVALID_ARG;
+  if (!offsets || !ws) return MC2_ERR_INVALID_ARG;
+  if (s->T > 0 && (!h || !w2 || !permute_src || !unpermute_dst || !probs || !out))
+    return MC2_ERR_INVALID_ARG;
+  if (s->T == 0) return MC2_OK;
+  const WsLayout L = ws_layout(*s);
+  char* w = static_cast<char*>(ws);
+  float* slots = reinterpret_cast<float*>(w + L.slots);
+  GemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  g.s = s;
+  g.a = h;
+  g.offsets = offsets;
+  g.permute_src = permute_src;
+  g.probs = probs;
+  g.out = slots;
+  g.dev_status = dev_status;
+  g.mode = 1;
+  if (s->act == MC2_F32) {
+    float* w2r = reinterpret_cast<float*>(w + L.w2_t32);
+    // [E, I, H] -> [E, H, I]
+    if (launch_transpose_round_tf32(static_cast<const float*>(w2), w2r, s->E, s->I, s->H, st) !=
+        cudaSuccess)
+      return MC2_ERR_CUDA;
+    g.b = w2r;
+    g.a_elem_bytes = 4;
+  } else {
+    g.b = w2;
+    g.a_elem_bytes = 2;
+  }
+  cudaError_t e = launch_gemm(g, st);
+  if (e == cudaSuccess) e = launch_combine(*s, slots, offsets, unpermute_dst, out, s->out, st);
+  return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+mc2_status_t mc2_check_shape(const mc2_shape_t* s) {
+  return shape_ok(s) ? MC2_OK : MC2_ERR_INVALID_ARG;
+}
+
+size_t mc2_workspace_bytes(const mc2_shape_t* s) {
+  if (!shape_ok(s)) return 0;
+  return ws_layout(*s).total;
+}
+
+mc2_status_t mc2_moe_counts(const mc2_shape_t* s, const int32_t* sel, int32_t* cnt,
+                            int32_t* recv, int32_t* offsets, int32_t* permute_src,
+                            int32_t* unpermute_dst, void* ws, int32_t* dev_status,
+                            void* stream) {
+  tl_launches = 0;
+  if (!shape_ok(s)) return MC2_ERR_INVALID_ARG;
+  return do_counts(s, sel, cnt, recv, offsets, permute_src, unpermute_dst, ws, dev_status,
+                   static_cast<cudaStream_t>(stream));
+}
+
+mc2_status_t mc2_alltoallv_gmm(const mc2_shape_t* s, const void* x, const float* x_scale,
+                               const void* w1, const float* w1_scale, const int32_t* offsets,
+                               const int32_t* permute_src, void* ws, void* h, float* h_scale,
+                               int32_t* dev_status, void* stream) {
+  tl_launches = 0;
+  if (!shape_ok(s)) return MC2_ERR_INVALID_ARG;
+  return do_fc1(s, x, x_scale, w1, w1_scale, offsets, permute_src, ws, h, h_scale, dev_status,
+                static_cast<cudaStream_t>(stream));
+}
+
+mc2_status_t mc2_gmm_alltoallv(const mc2_shape_t* s, const void* h, const float* h_scale,
+                               const void* w2, const float* w2_scale, const int32_t* offsets,
+                               const int32_t* permute_src, const int32_t* unpermute_dst,
+                               const float* probs, void* ws, void* out, int32_t* dev_status,
+                               void* stream) {
+  tl_launches = 0;
+  if (!shape_ok(s)) return MC2_ERR_INVALID_ARG;
+  return do_fc2(s, h, h_scale, w2, w2_scale, offsets, permute_src, unpermute_dst, probs, ws, out,
+                dev_status, static_cast<cudaStream_t>(stream));
+}
+
+mc2_status_t mc2_moe_forward(const mc2_shape_t* s, const void* x, const float* x_scale,
+                             const int32_t* sel, const float* probs, const void* w1,
+                             const float* w1_scale, const void* w2, const float* w2_scale,
+                             int32_t* cnt, int32_t* recv, int32_t* offsets,
+                             int32_t* permute_src, int32_t* unpermute_dst, void* h,
+                             float* h_scale, void* out, void* ws, int32_t* dev_status,
+                             void* stream) {
+  tl_launches = 0;
+  if (!shape_ok(s)) return MC2_ERR_INVALID_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  mc2_status_t r =
+      do_counts(s, sel, cnt, recv, offsets, permute_src, unpermute_dst, ws, dev_status, st);
+  if (r != MC2_OK) return r;
+  r = do_fc1(s, x, x_scale, w1, w1_scale, offsets, permute_src, ws, h, h_scale, dev_status, st);
+  if (r != MC2_OK) return r;
+  return do_fc2(s, h, h_scale, w2, w2_scale, offsets, permute_src, unpermute_dst, probs, ws, out,
+                dev_status, st);
+}
+
+mc2_status_t mc2_selftest_wait(uint64_t limit_ns, int32_t* dev_status, void* stream) {
+  tl_launches = 0;
+  if (!dev_status) return MC2_ERR_INVALID_ARG;
+  return cuda_status(launch_selftest_wait(limit_ns, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+void mc2_set_wait_limit_ns(uint64_t limit_ns) { g_wait_limit_ns.store(limit_ns); }
+
+int32_t mc2_last_launch_count(void) { return tl_launches; }
+
+const char* mc2_status_str(mc2_status_t st) {
+  switch (st) {
+    case MC2_OK: return "ok";
+    case MC2_ERR_INVALID_ARG: return "invalid argument";
+    case MC2_ERR_UNSUPPORTED: return "unsupported";
+    case MC2_ERR_CUDA: return "CUDA error";
+    case MC2_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case MC2_ERR_BAD_EXPERT_ID: return "expert id outside [0, E)";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

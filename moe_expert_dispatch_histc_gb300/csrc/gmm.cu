@@ -1,0 +1,612 @@
+// gmm.cu -- the two grouped matmuls of the block on 5th-generation tensor
+// cores, with the data movement of the expert-parallel exchange folded in
+// ("NPU Training Operators - MC2", sections "Background constraints" and
+// "Execution path", steps 6-10):
+//
+//   fc1 (dispatch segment):  h[p, :] = SwiGLU( x[permute_src[p] / k, :] @ w1[e] )
+//        the permute is a TMA gather4 of token rows straight into the
+//        swizzled A tile; SwiGLU runs on the fp32 accumulator in TMEM.
+//   fc2 (combine segment):   slot[permute_src[p], :] = probs[permute_src[p]] * (h[p, :] @ w2[e])
+//        each (token, slot) pair owns one fp32 row of `slots`, written once,
+//        so the sum over slots (combine kernel) has a fixed order.
+//
+// One persistent kernel per segment, one CTA per SM, 6 warps:
+//   warp 0      TMA producer (A rows + B tiles into a 4-stage smem ring)
+//   warp 1      TMEM allocator and tcgen05.mma issuer (one lane)
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, math, global stores
+// Two 128x256 fp32 accumulators in TMEM (all 512 columns) let the epilogue of
+// tile i overlap the mainloop of tile i+1.  Tiles are (expert, n-tile,
+// m-tile) triples over a per-expert tile prefix that each CTA builds from
+// `offsets`, so empty experts cost nothing and skewed ones just own more
+// tiles; CTAs take tiles round-robin.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mc2 {
+
+enum { MODE_FC1 = 0, MODE_FC2 = 1 };
+
+constexpr int BM = 128;            // rows per tile (UMMA M)
+constexpr int BN = 256;            // accumulator columns per tile (UMMA N)
+constexpr int STAGES = 4;
+constexpr int A_STAGE = BM * 128;  // 128 rows x 128 bytes of K
+constexpr int B_STAGE = 32768;     // (128/es) K rows x 256 columns x es bytes
+constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 512;
+
+struct GemmParams {
+  const int32_t* offsets;
+  const int32_t* permute_src;
+  const float* probs;
+  void* out;
+  int32_t* dev_status;
+  int E, k, K, n_tiles, out_cols, I;
+  uint64_t wait_limit_ns;
+};
+
+template <int ES>
+struct ElemTraits;
+template <>
+struct ElemTraits<2> {  // bf16, kind::f16; weights used as stored ([K, N], N contiguous)
+  static constexpr int BK = 64;
+  static constexpr int KIND = 0;
+  static constexpr uint32_t FMT = 1;
+  static constexpr bool B_KMAJOR = false;
+};
+template <>
+struct ElemTraits<4> {  // fp32 storage, kind::tf32; weights pre-transposed to [N, K]
+  static constexpr int BK = 32;
+  static constexpr int KIND = 1;
+  static constexpr uint32_t FMT = 2;
+  static constexpr bool B_KMAJOR = true;
+};
+
+__device__ __forceinline__ void decode_tile(int tile, const int32_t* prefix, int E, int n_tiles,
+                                            const int32_t* offsets, int& e, int& n, int& row0,
+                                            int& rows) {
+  int lo = 0, hi = E;  // prefix[lo] <= tile < prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= tile) lo = mid; else hi = mid;
+  }
+  e = lo;
+  const int local = tile - prefix[e];
+  const int m_tiles = (prefix[e + 1] - prefix[e]) / n_tiles;
+  n = local / m_tiles;
+  const int m = local - n * m_tiles;
+  const int off = __ldg(offsets + e);
+  row0 = off + m * BM;
+  const int end = __ldg(offsets + e + 1);
+  rows = min(BM, end - row0);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float round_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+template <int MODE, int ES>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const GemmParams p) {
+  using TR = ElemTraits<ES>;
+  constexpr int BK = TR::BK;
+  constexpr int BNB = 128 / ES;              // columns per 128-byte B block
+  constexpr int NB = BN / BNB;               // B blocks per stage
+  constexpr int B_BLOCK = BK * 128;          // bytes per B block (BK rows x 128 B)
+  constexpr int KK_B = (32 / ES) * 128;      // B bytes per UMMA K step
+  constexpr bool BKM = TR::B_KMAJOR;
+  constexpr uint32_t IDESC = instr_desc(TR::FMT, false, !BKM, BM, BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_STAGE);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_sh = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
+  int32_t* prefix = reinterpret_cast<int32_t*>(tmem_base_sh + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4 * 32);
+    }
+    mbar_init(mma_done, 1);
+    *abort_sh = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_base_sh, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 2) {  // per-expert tile prefix: ceil(rows_e / BM) * n_tiles
+    int run = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      int t = 0;
+      if (e < E) {
+        const int rows = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+        t = ((rows + BM - 1) / BM) * p.n_tiles;
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += y;
+      }
+      if (e < E) prefix[e + 1] = run + t;
+      run += __shfl_sync(0xffffffffu, t, 31);
+    }
+    if (lane == 0) prefix[0] = 0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_sh;
+  const int total = prefix[E];
+  WaitCtl ctl{abort_sh, p.wait_limit_ns, p.dev_status};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int s = 0;
+    uint32_t ph = 0;
+    int n_arm = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, n, row0, rows;
+      decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
+      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+      if (MODE == MODE_FC1) {  // token rows of this lane's four permuted rows
+        const int tok0 = __ldg(p.permute_src + row0) / p.k;
+        int rr[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int row = lane * 4 + q;
+          rr[q] = row < rows ? __ldg(p.permute_src + row0 + row) / p.k : tok0;
+        }
+        r0 = rr[0]; r1 = rr[1]; r2 = rr[2]; r3 = rr[3];
+      }
+      bool ok = true;
+      for (int kb = 0; kb < p.K / BK; ++kb) {
+        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, ctl);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+        __syncwarp();
+        uint8_t* a_dst = sA + s * A_STAGE;
+        uint8_t* b_dst = sB + s * B_STAGE;
+        const int k0 = kb * BK;
+        if (MODE == MODE_FC1) {
+          tma_gather4(a_dst + lane * 512, &tmA, &full[s], k0, r0, r1, r2, r3);
+        } else if (lane == 0) {
+          tma_load_2d(a_dst, &tmA, &full[s], k0, row0);
+        }
+        if (lane == 0) {
+          if constexpr (BKM) {
+            // K-major B: N rows of 128 bytes of K; fc1 loads the gate rows
+            // and the up rows of the same output columns as two boxes
+            if (MODE == MODE_FC1) {
+              tma_load_3d(b_dst, &tmB, &full[s], k0, n * (BN / 2), e);
+              tma_load_3d(b_dst + (BN / 2) * 128, &tmB, &full[s], k0, p.I + n * (BN / 2), e);
+            } else {
+              tma_load_3d(b_dst, &tmB, &full[s], k0, n * BN, e);
+            }
+          } else {
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              int ncol;
+              if (MODE == MODE_FC1) {
+                const int half = b / (NB / 2), bb = b % (NB / 2);
+                ncol = half * p.I + n * (BN / 2) + bb * BNB;
+              } else {
+                ncol = n * BN + b * BNB;
+              }
+              tma_load_3d(b_dst + b * B_BLOCK, &tmB, &full[s], ncol, k0, e);
+            }
+          }
+        }
+        ++n_arm;
+        if (++s == STAGES) { s = 0; ph ^= 1; }
+      }
+      if (!ok) break;
+    }
+    // Let every armed stage land before the CTA can exit (bounded).
+    if (lane == 0) {
+      volatile int never = 0;
+      WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
+      for (int st = 0; st < STAGES && st < n_arm; ++st) {
+        const int last = st + STAGES * ((n_arm - 1 - st) / STAGES);
+        mbar_wait(&full[st], (last / STAGES) & 1, drain);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int s = 0;
+    uint32_t ph = 0;
+    int acc = 0;
+    uint32_t aph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      if (lane == 0) ok = mbar_wait(&tempty[acc], aph ^ 1, ctl);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < p.K / BK; ++kb) {
+        if (lane == 0) ok = mbar_wait(&full[s], ph, ctl);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a_base = smem_u32(sA + s * A_STAGE);
+          const uint32_t b_base = smem_u32(sB + s * B_STAGE);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bdesc = BKM ? smem_desc_sw128(b_base + kk * 32, 16, 1024)
+                                       : smem_desc_sw128(b_base + kk * KK_B, B_BLOCK, 1024);
+            umma<TR::KIND>(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0);
+          }
+          umma_commit(&empty[s]);
+        }
+        __syncwarp();
+        if (++s == STAGES) { s = 0; ph ^= 1; }
+      }
+      if (!ok) break;
+      if (lane == 0) umma_commit(&tfull[acc]);
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) aph ^= 1;
+    }
+    if (lane == 0) {  // every issued MMA has finished reading smem / writing TMEM
+      umma_commit(mma_done);
+      volatile int never = 0;
+      WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
+      mbar_wait(mma_done, 0, drain);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;         // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;  // accumulator row = TMEM lane
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, n, row0, rows;
+      decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&tfull[acc], aph, ctl);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+      const bool valid = row < rows;
+      if (MODE == MODE_FC1) {
+        const int grow = row0 + row;
+#pragma unroll 1
+        for (int c = 0; c < (BN / 2) / 32; ++c) {
+          const int col0 = n * (BN / 2) + c * 32;
+          if (col0 >= p.out_cols) break;
+          uint32_t g[32], u[32];
+          tmem_ld32(tbase + c * 32, g);
+          tmem_ld32(tbase + BN / 2 + c * 32, u);
+          tmem_ld_wait();
+          if (valid) {
+            if (ES == 2) {
+              uint32_t packed[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float h0 = silu_f(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+                const float h1 =
+                    silu_f(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+                packed[i] = pack_bf16x2(h0, h1);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                    static_cast<int64_t>(grow) * p.out_cols + col0);
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                    packed[4 * v + 3]);
+            } else {
+              float hv[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                hv[i] = round_tf32(silu_f(__uint_as_float(g[i])) * __uint_as_float(u[i]));
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) +
+                                                      static_cast<int64_t>(grow) * p.out_cols + col0);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                dst[v] = make_float4(hv[4 * v], hv[4 * v + 1], hv[4 * v + 2], hv[4 * v + 3]);
+            }
+          }
+        }
+      } else {
+        int flat = 0;
+        float prob = 0.f;
+        if (valid) {
+          flat = __ldg(p.permute_src + row0 + row);
+          prob = __ldg(p.probs + flat);
+        }
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int col0 = n * BN + c * 32;
+          if (col0 >= p.out_cols) break;
+          uint32_t v[32];
+          tmem_ld32(tbase + c * 32, v);
+          tmem_ld_wait();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) +
+                                                    static_cast<int64_t>(flat) * p.out_cols + col0);
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+              dst[w] = make_float4(prob * __uint_as_float(v[4 * w]), prob * __uint_as_float(v[4 * w + 1]),
+                                   prob * __uint_as_float(v[4 * w + 2]), prob * __uint_as_float(v[4 * w + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) aph ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ----------------------------------------------------------------------------
+// combine: out[t, :] = sum_j slots[t*k + j, :] over valid pairs, j ascending
+// ----------------------------------------------------------------------------
+__global__ void combine_kernel(const float* __restrict__ slots, const int32_t* __restrict__ offsets,
+                               const int32_t* __restrict__ unpermute_dst, void* __restrict__ out,
+                               int64_t T, int H, int k, int E, int out_bf16) {
+  const int64_t H4 = H / 4;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= T * H4) return;
+  const int64_t t = idx / H4;
+  const int c = static_cast<int>(idx - t * H4) * 4;
+  const int32_t nvalid = __ldg(offsets + E);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < k; ++j) {
+    const int64_t flat = t * k + j;
+    if (__ldg(unpermute_dst + flat) >= nvalid) continue;
+    const float4 v = __ldg(reinterpret_cast<const float4*>(slots + flat * H + c));
+    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  }
+  if (out_bf16) {
+    uint2 w;
+    w.x = pack_bf16x2(acc.x, acc.y);
+    w.y = pack_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + t * H + c) = w;
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + t * H + c) = acc;
+  }
+}
+
+__global__ void round_tf32_kernel(const float* __restrict__ src, float* __restrict__ dst, size_t n) {
+  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (; i < n; i += stride) dst[i] = round_tf32(src[i]);
+}
+
+// dst[b, c, r] = tf32_round(src[b, r, c]) for src [batch, rows, cols]
+__global__ void transpose_round_tf32_kernel(const float* __restrict__ src, float* __restrict__ dst,
+                                            int rows, int cols) {
+  __shared__ float tile[32][33];
+  const int64_t b = blockIdx.z;
+  const float* s = src + b * rows * static_cast<int64_t>(cols);
+  float* d = dst + b * rows * static_cast<int64_t>(cols);
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[i][threadIdx.x] = s[static_cast<int64_t>(r) * cols + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) d[static_cast<int64_t>(c) * rows + r] = round_tf32(tile[threadIdx.x][i]);
+  }
+}
+
+__global__ void selftest_wait_kernel(uint64_t limit_ns, int32_t* dev_status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    WaitCtl ctl{&abort_flag, limit_ns, dev_status};
+    mbar_wait(&bar, 0, ctl);  // nothing ever arrives: runs out after limit_ns
+  }
+}
+
+// ----------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+static bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int es, const void* base,
+                      uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * es};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, int es, const void* base,
+                      uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * es, d0 * d1 * es};
+  cuuint32_t box[3] = {b0, b1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+template <int MODE, int ES>
+static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
+  const mc2_shape_t& s = *g.s;
+  using TR = ElemTraits<ES>;
+  const CUtensorMapDataType dt =
+      ES == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const int64_t R = static_cast<int64_t>(s.T) * s.k;
+  CUtensorMap tA, tB;
+  GemmParams p;
+  p.offsets = g.offsets;
+  p.permute_src = g.permute_src;
+  p.probs = g.probs;
+  p.out = g.out;
+  p.dev_status = g.dev_status;
+  p.E = s.E;
+  p.k = s.k;
+  p.I = s.I;
+  p.wait_limit_ns = wait_limit_ns();
+  bool ok;
+  if (MODE == MODE_FC1) {
+    p.K = s.H;
+    p.n_tiles = (s.I + BN / 2 - 1) / (BN / 2);
+    p.out_cols = s.I;
+    ok = encode_2d(&tA, dt, ES, g.a, s.H, s.T, 128 / ES, 1) &&
+         (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.H, 2ull * s.I, s.E, TR::BK, BN / 2)
+                       : encode_3d(&tB, dt, ES, g.b, 2ull * s.I, s.H, s.E, 128 / ES, TR::BK));
+  } else {
+    p.K = s.I;
+    p.n_tiles = (s.H + BN - 1) / BN;
+    p.out_cols = s.H;
+    ok = encode_2d(&tA, dt, ES, g.a, s.I, R, 128 / ES, BM) &&
+         (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.I, s.H, s.E, TR::BK, BN)
+                       : encode_3d(&tB, dt, ES, g.b, s.H, s.I, s.E, 128 / ES, TR::BK));
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  const size_t smem = 1024 + STAGES * STAGE_BYTES + 256 + (s.E + 1) * sizeof(int32_t);
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(gmm_kernel<MODE, ES>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    1024 + STAGES * STAGE_BYTES + 256 + 1025 * 4);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int64_t tiles_upper = (R / BM + s.E) * static_cast<int64_t>(p.n_tiles);
+  const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_upper, 1)));
+  gmm_kernel<MODE, ES><<<grid, NUM_THREADS, smem, st>>>(tA, tB, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
+  if (static_cast<int64_t>(g.s->T) * g.s->k == 0) return cudaSuccess;
+  cudaError_t e;
+  if (g.mode == MODE_FC1)
+    e = g.a_elem_bytes == 2 ? launch_one<MODE_FC1, 2>(g, st) : launch_one<MODE_FC1, 4>(g, st);
+  else
+    e = g.a_elem_bytes == 2 ? launch_one<MODE_FC2, 2>(g, st) : launch_one<MODE_FC2, 4>(g, st);
+  note_launches(1);
+  return e;
+}
+
+cudaError_t launch_combine(const mc2_shape_t& s, const float* slots, const int32_t* offsets,
+                           const int32_t* unpermute_dst, void* out, int out_dtype,
+                           cudaStream_t st) {
+  const int64_t n = static_cast<int64_t>(s.T) * (s.H / 4);
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (n + threads - 1) / threads;
+  combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+      slots, offsets, unpermute_dst, out, s.T, s.H, s.k, s.E, out_dtype == MC2_BF16 ? 1 : 0);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_round_tf32(const float* src, float* dst, size_t n, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  const size_t want = (n + threads - 1) / threads;
+  const unsigned blocks = static_cast<unsigned>(std::min<size_t>(want, 152 * 16));
+  round_tf32_kernel<<<blocks, threads, 0, st>>>(src, dst, n);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_round_tf32(const float* src, float* dst, int batch, int rows,
+                                       int cols, cudaStream_t st) {
+  if (static_cast<int64_t>(batch) * rows * cols == 0) return cudaSuccess;
+  dim3 grid((cols + 31) / 32, (rows + 31) / 32, batch);
+  transpose_round_tf32_kernel<<<grid, dim3(32, 8), 0, st>>>(src, dst, rows, cols);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_wait(uint64_t limit_ns, int32_t* dev_status, cudaStream_t st) {
+  selftest_wait_kernel<<<1, 32, 0, st>>>(limit_ns, dev_status);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace mc2

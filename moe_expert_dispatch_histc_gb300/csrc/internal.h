@@ -1,0 +1,75 @@
+// internal.h -- declarations shared by the translation units of libmc2moe.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/mc2moe.h"
+
+namespace mc2 {
+
+constexpr int kCountsSub = 256;       // flat (token, slot) entries per warp in the counts pass
+constexpr int kCountsWarpsPerBlock = 8;
+constexpr size_t kWsAlign = 256;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Sub-chunk geometry of the counts pass: every logical rank's entries
+// [r*RW, (r+1)*RW) are split into CPR chunks of kCountsSub (last one ragged),
+// one warp each, so chunks never straddle ranks and G = W*CPR warps walk the
+// flat order in sequence.
+struct CountsGeom {
+  int64_t R, RW, CPR, G, EB;  // EB = E + 1 bins (bin E collects invalid ids)
+};
+CountsGeom counts_geom(const mc2_shape_t& s);
+
+// Workspace layout (byte offsets from ws).
+struct WsLayout {
+  size_t hist, base;     // int32 [EB * G] each
+  size_t slots;          // fp32 [R, H] weighted fc2 rows (combine input)
+  size_t x_t32, w1_t32, w2_t32;  // fp32 tf32-rounded copies, weights transposed to [E, N, K] (act F32 only)
+  size_t h_f32;          // fp32 [R, I] pre-requant SwiGLU output (act I8 only)
+  size_t rowmax;         // uint32 [R] row absmax bits (act I8 only)
+  size_t x_b16, hq_b16;  // bf16 copies of int8 operands (act I8 only)
+  size_t w1_b16, w2_b16; // bf16 copies of int8 weights (act I8 only)
+  size_t total;
+};
+WsLayout ws_layout(const mc2_shape_t& s);
+
+uint64_t wait_limit_ns();
+void note_launches(int n);
+
+// Launch wrappers (return cudaSuccess or the launch error).
+cudaError_t launch_counts(const mc2_shape_t& s, const int32_t* sel, int32_t* cnt, int32_t* recv,
+                          int32_t* offsets, int32_t* permute_src, int32_t* unpermute_dst,
+                          char* ws, int32_t* dev_status, cudaStream_t st);
+
+struct GemmArgs {
+  const mc2_shape_t* s;
+  const void* a;            // fc1: x [T, H]; fc2: h [R, I]
+  const void* b;            // fc1: w1 [E, H, 2I]; fc2: w2 [E, I, H]
+  const int32_t* offsets;
+  const int32_t* permute_src;
+  const float* probs;       // fc2 only
+  const float* a_scale;     // int8: per-token (fc1) or per-row (fc2)
+  const float* b_scale;     // int8: per-channel
+  void* out;                // fc1: h; fc2: fp32 slots [R, H]
+  float* out_scale;         // unused by the GEMM itself
+  uint32_t* rowmax;         // int8 fc1: row absmax bits
+  int32_t* dev_status;
+  int a_elem_bytes;         // 2 (bf16) or 4 (f32)
+  int mode;                 // see gmm.cu
+};
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st);
+
+cudaError_t launch_combine(const mc2_shape_t& s, const float* slots, const int32_t* offsets,
+                           const int32_t* unpermute_dst, void* out, int out_dtype,
+                           cudaStream_t st);
+cudaError_t launch_round_tf32(const float* src, float* dst, size_t n, cudaStream_t st);
+cudaError_t launch_transpose_round_tf32(const float* src, float* dst, int batch, int rows,
+                                       int cols, cudaStream_t st);
+cudaError_t launch_selftest_wait(uint64_t limit_ns, int32_t* dev_status, cudaStream_t st);
+
+int num_sms();
+
+}  // namespace mc2

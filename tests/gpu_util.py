@@ -1,0 +1,53 @@
+"""Helpers shared by the GPU tests: run the CUDA path on seeded inputs and
+bring results back; lazily widen stored weights to float64 for the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from moe_expert_dispatch_histc_gb300 import block as blk
+from moe_expert_dispatch_histc_gb300.build import build
+from moe_expert_dispatch_histc_gb300.workloads import as_f64, make_inputs
+
+_built = False
+
+
+def ensure_built():
+    global _built
+    if not _built:
+        build()
+        _built = True
+
+
+class LazyF64:
+    """w[e] -> float64 copy of expert e's weights, converted on first use."""
+
+    def __init__(self, arr, act):
+        self.arr, self.act, self.cache = arr, act, {}
+        self.shape = arr.shape
+
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self.cache:
+            self.cache[e] = as_f64(self.arr[e], self.act)
+        return self.cache[e]
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        t = t.float()
+    return t.numpy()
+
+
+def run_gpu(wl, seed=0, inputs=None, segments=False, out=None):
+    ensure_built()
+    inp = make_inputs(wl, seed) if inputs is None else inputs
+    d = blk.inputs_to_device(inp, wl)
+    b = blk.alloc_buffers(wl, out=out)
+    if segments:
+        blk.run_segments(wl, d, b, out=out)
+    else:
+        blk.run_block(wl, d, b, out=out)
+    torch.cuda.synchronize()
+    return inp, d, b

@@ -1,0 +1,102 @@
+"""Host-side checks of the C ABI: the library loads, exports what the header
+declares, applies its argument rules and launches nothing on bad input.
+None of these calls reaches the GPU."""
+import ctypes
+
+import pytest
+
+from moe_expert_dispatch_histc_gb300 import binding as B
+from moe_expert_dispatch_histc_gb300.build import build
+from moe_expert_dispatch_histc_gb300.workloads import WORKLOADS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build()
+    return B.lib()
+
+
+def test_header_symbols_are_exported():
+    names = B.header_functions()
+    assert "mc2_moe_counts" in names and "mc2_alltoallv_gmm" in names
+    assert "mc2_gmm_alltoallv" in names
+    L = B.lib()
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/mc2moe.h but not exported"
+
+
+def test_binding_covers_header():
+    assert set(B.header_functions()) <= set(B._SIGS)
+
+
+def _shape(**kw):
+    base = dict(T=64, H=256, I=128, E=8, k=2, W=2, act="bf16", out=None)
+    base.update(kw)
+    return B.Shape.make(**base)
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_named_workloads_are_valid(name):
+    wl = WORKLOADS[name]
+    s = B.Shape.make(wl.T, wl.H, wl.I, wl.E, wl.k, wl.W, wl.act)
+    assert B.mc2_check_shape(s) == B.MC2_OK
+    assert B.mc2_workspace_bytes(s) > 0
+
+
+@pytest.mark.parametrize("kw", [
+    dict(E=9), dict(T=63), dict(k=9), dict(k=0), dict(H=200), dict(I=100), dict(H=0),
+    dict(E=2048, W=2), dict(W=0), dict(T=-2), dict(act="i32", out="i32"), dict(act="f32", out="bf16"),
+    dict(act="bf16", out="i32"), dict(act="bf16", out="f32"),
+])
+def test_shape_rules_reject(kw):
+    s = _shape(**kw)
+    assert B.mc2_check_shape(s) == B.MC2_ERR_INVALID_ARG
+    assert B.mc2_workspace_bytes(s) == 0
+
+
+def test_shape_rules_accept_edges():
+    for kw in (dict(T=0), dict(k=8), dict(W=1, T=3), dict(E=1, k=1, W=1), dict(act="f32", out="f32"),
+               dict(act="i8", out="bf16"), dict(act="i8", out="i32"), dict(H=64, I=64)):
+        assert B.mc2_check_shape(_shape(**kw)) == B.MC2_OK, kw
+
+
+def test_workspace_is_deterministic_and_aligned():
+    s = _shape(T=4096, H=2048, I=768, E=64, k=8, W=4)
+    a, b = B.mc2_workspace_bytes(s), B.mc2_workspace_bytes(s)
+    assert a == b and a % 256 == 0
+    # the slot buffer of the combine dominates: R * H * 4 bytes
+    assert a >= 4096 * 8 * 2048 * 4
+
+
+def test_null_pointers_are_rejected_before_any_launch():
+    s = _shape()
+    fake = 1 << 40  # never dereferenced: validation fails first
+    assert B.mc2_moe_counts(s, fake, fake, fake, fake, fake, fake, None, None, stream=0,
+                            check=False) == B.MC2_ERR_INVALID_ARG
+    assert B.mc2_moe_counts(s, None, fake, fake, fake, fake, fake, fake, None, stream=0,
+                            check=False) == B.MC2_ERR_INVALID_ARG
+    assert B.mc2_alltoallv_gmm(s, fake, None, None, None, fake, fake, fake, fake, None,
+                               stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+    assert B.mc2_gmm_alltoallv(s, fake, None, fake, None, fake, fake, fake, None, fake, fake,
+                               stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+    # scales are for the int8 path only
+    assert B.mc2_alltoallv_gmm(s, fake, fake, fake, None, fake, fake, fake, fake, None,
+                               stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+    bad = _shape(E=9)
+    assert B.mc2_moe_forward(bad, *([fake] * 17), None, stream=0,
+                             check=False) == B.MC2_ERR_INVALID_ARG
+    assert B.mc2_selftest_wait(1000, None, stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+
+
+def test_status_strings():
+    for st in range(6):
+        assert B.status_str(st)
+    assert B.status_str(99) == "unknown status"
+    assert B.status_str(B.MC2_OK) == "ok"
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        B.lib()

@@ -1,0 +1,200 @@
+"""Parity of the CUDA path with the CPU oracle, through the C ABI.
+
+Integer outputs (counts, recv counts, offsets, permutation indices) must be
+bit-exact.  Floating-point outputs must satisfy the block's rule
+max|err| <= 1e-2 * max|ref| and sum|err| / sum|ref| <= 2e-3 against the
+float64 oracle (h is compared after the oracle rounds it to the activation
+dtype, as the block materialises it).  Small shapes are compared in full;
+the named full-size workloads in the launch configuration of the benchmark
+(one mc2_moe_forward call) are compared on sampled tokens and rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import mc2_oracle as orc
+from moe_expert_dispatch_histc_gb300 import binding as B
+from moe_expert_dispatch_histc_gb300.workloads import WORKLOADS, Workload, as_f64, make_inputs
+
+from gpu_util import LazyF64, ensure_built, run_gpu, to_np
+
+pytestmark = pytest.mark.gpu
+
+H_DTYPE = {"f32": "f32", "bf16": "bf16"}
+
+
+def _counts_exact(wl, inp, b):
+    res_cnt = orc.rank_counts(inp["sel"], wl.E, wl.W)
+    send, recv = orc.send_recv_counts(res_cnt, wl.W)
+    offsets = orc.expert_offsets(res_cnt)
+    _, src = orc.permute(np.arange(wl.T), inp["sel"], wl.E)
+    dst = np.empty_like(src)
+    dst[src] = np.arange(src.shape[0])
+    assert np.array_equal(to_np(b.cnt), res_cnt), "cnt (all_gather of histc) differs"
+    assert np.array_equal(to_np(b.recv), np.stack(recv)), "recv_counts differ"
+    assert np.array_equal(to_np(b.offsets), offsets), "expert offsets differ"
+    assert np.array_equal(to_np(b.permute_src), src), "permute_src differs"
+    assert np.array_equal(to_np(b.unpermute_dst), dst), "unpermute_dst differs"
+    return src, offsets
+
+
+def _tol(got, ref, what):
+    ok, a, m = orc.bf16_tolerance_ok(got, ref)
+    assert ok, f"{what}: max|err|/max|ref| = {a:.3e} (<= 1e-2), mean rel = {m:.3e} (<= 2e-3)"
+    return a, m
+
+
+def test_selftest_wait_times_out_and_reports():
+    ensure_built()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.mc2_selftest_wait(20_000_000, st)          # 20 ms on a barrier nothing completes
+    torch.cuda.synchronize()
+    assert int(st.item()) & B.MC2_DEV_TIMEOUT
+
+
+@pytest.mark.parametrize("name", ["tiny", "uniform", "skew", "int8", "decode"])
+def test_counts_bit_exact(name):
+    wl = WORKLOADS[name]
+    ensure_built()
+    inp = make_inputs(wl.scaled(act="bf16") if wl.act == "i8" else wl, 0)
+    wlc = wl.scaled(act="bf16") if wl.act == "i8" else wl
+    d_sel = torch.from_numpy(inp["sel"]).cuda()
+    from moe_expert_dispatch_histc_gb300 import block as blk
+    b = blk.alloc_buffers(wlc)
+    B.mc2_moe_counts(blk.shape_of(wlc), d_sel, b.cnt, b.recv, b.offsets, b.permute_src,
+                     b.unpermute_dst, b.ws, b.dev_status)
+    torch.cuda.synchronize()
+    _counts_exact(wlc, inp, b)
+    assert int(b.dev_status.item()) == 0
+
+
+SMALL = [
+    Workload("tiny", 64, 256, 128, 8, 2, 2, "f32"),
+    Workload("multi_mtile", 1024, 256, 128, 8, 2, 2, "bf16"),       # ~256 rows/expert, ragged
+    Workload("ragged_n", 384, 320, 192, 6, 3, 3, "bf16"),           # partial n-tiles of fc1 and fc2
+    Workload("many_experts", 256, 512, 256, 64, 8, 4, "bf16"),      # ~32 rows/expert
+    Workload("k1", 200, 128, 64, 4, 1, 2, "bf16"),
+    Workload("fp32_ragged", 96, 192, 64, 4, 2, 2, "f32"),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_block_parity_full(wl):
+    inp, d, b = run_gpu(wl, seed=1)
+    src, offsets = _counts_exact(wl, inp, b)
+    x, w1, w2 = (as_f64(inp[n], wl.act) for n in ("x", "w1", "w2"))
+    ref = orc.block_forward(x, w1, w2, inp["sel"], inp["probs"], wl.E, wl.W, h_dtype=H_DTYPE[wl.act])
+    nvalid = int(offsets[-1])
+    _tol(to_np(b.h)[:nvalid], ref["h"], "h (fc1 + SwiGLU)")
+    _tol(to_np(b.out), ref["out"], "out (fc2 + combine)")
+    assert int(b.dev_status.item()) == 0
+
+
+@pytest.mark.parametrize("wl", SMALL[:3], ids=lambda w: w.name)
+def test_segments_equal_single_call(wl):
+    _, _, b1 = run_gpu(wl, seed=2)
+    _, _, b2 = run_gpu(wl, seed=2, segments=True)
+    assert torch.equal(b1.out, b2.out) and torch.equal(b1.h, b2.h)
+
+
+def test_fc2_alone_on_oracle_h():
+    """fc2 + combine fed the oracle's h: isolates the combine segment."""
+    wl = SMALL[1]
+    inp, d, b = run_gpu(wl, seed=3)
+    x, w1, w2 = (as_f64(inp[n], wl.act) for n in ("x", "w1", "w2"))
+    ref = orc.block_forward(x, w1, w2, inp["sel"], inp["probs"], wl.E, wl.W, h_dtype="bf16")
+    h_ref = torch.from_numpy(ref["h"].astype(np.float32)).to(torch.bfloat16).cuda()
+    h = torch.zeros_like(b.h)
+    h[:h_ref.shape[0]] = h_ref
+    from moe_expert_dispatch_histc_gb300 import block as blk
+    B.mc2_gmm_alltoallv(blk.shape_of(wl), h, None, d["w2"], None, b.offsets, b.permute_src,
+                        b.unpermute_dst, d["probs"], b.ws, b.out, b.dev_status)
+    torch.cuda.synchronize()
+    _tol(to_np(b.out), ref["out"], "out from oracle h")
+
+
+def test_determinism_bitwise():
+    wl = SMALL[3]
+    _, _, b1 = run_gpu(wl, seed=4)
+    _, _, b2 = run_gpu(wl, seed=4)
+    assert torch.equal(b1.out.view(torch.int16), b2.out.view(torch.int16))
+    assert torch.equal(b1.h.view(torch.int16), b2.h.view(torch.int16))
+
+
+# ------------------------------------------------------------------ edge cases
+def _custom(wl, sel, seed=5):
+    inp = make_inputs(wl, seed)
+    inp["sel"] = np.ascontiguousarray(sel.astype(np.int32))
+    return inp
+
+
+def _check_custom(wl, inp, expect_bad=False):
+    inp, d, b = run_gpu(wl, inputs=inp)
+    src, offsets = _counts_exact(wl, inp, b)
+    x, w1, w2 = (as_f64(inp[n], wl.act) for n in ("x", "w1", "w2"))
+    ref = orc.block_forward(x, w1, w2, inp["sel"], inp["probs"], wl.E, wl.W, h_dtype="bf16")
+    nvalid = int(offsets[-1])
+    if nvalid:
+        _tol(to_np(b.h)[:nvalid], ref["h"], "h")
+    _tol(to_np(b.out), ref["out"], "out")
+    status = int(b.dev_status.item())
+    assert bool(status & B.MC2_DEV_BAD_EXPERT_ID) == expect_bad
+    assert not status & B.MC2_DEV_TIMEOUT
+
+
+def test_all_tokens_to_one_expert():
+    wl = Workload("one_expert", 512, 256, 128, 8, 1, 2, "bf16")
+    _check_custom(wl, _custom(wl, np.full((512, 1), 5)))
+
+
+def test_most_experts_empty():
+    wl = Workload("sparse", 300, 256, 128, 16, 2, 2, "bf16")
+    sel = np.stack([np.full(300, 3), np.full(300, 12)], axis=1)
+    _check_custom(wl, _custom(wl, sel))
+
+
+def test_invalid_ids_are_flagged_and_skipped():
+    wl = Workload("bad_ids", 64, 256, 128, 8, 2, 2, "bf16")
+    inp = make_inputs(wl, 6)
+    sel = inp["sel"].copy()
+    sel[3, 0], sel[17, 1], sel[40, 0] = 8, -1, 1000
+    _check_custom(wl, _custom(wl, sel, seed=6), expect_bad=True)
+
+
+def test_empty_input():
+    wl = Workload("empty", 0, 256, 128, 8, 2, 2, "bf16")
+    inp, d, b = run_gpu(wl)
+    assert to_np(b.cnt).sum() == 0 and to_np(b.offsets).sum() == 0
+
+
+# ------------------------------------------------------------------ full size
+@pytest.mark.parametrize("name", ["uniform", "skew", "decode"])
+def test_full_size_sampled(name):
+    wl = WORKLOADS[name]
+    inp, d, b = run_gpu(wl, seed=0)
+    src, offsets = _counts_exact(wl, inp, b)
+    x = as_f64(inp["x"], wl.act)
+    w1, w2 = LazyF64(inp["w1"], wl.act), LazyF64(inp["w2"], wl.act)
+    rng = np.random.default_rng(123)
+    toks = np.unique(np.concatenate([rng.choice(wl.T, 24, replace=False), [0, wl.T - 1]]))
+    out = to_np(b.out)
+    got, ref = [], []
+    for t in toks:
+        ref.append(orc.brute_force_token(x[t], w1, w2, inp["sel"][t], inp["probs"][t], wl.E,
+                                         h_dtype="bf16"))
+        got.append(out[t])
+    _tol(np.array(got), np.array(ref), f"{name}: sampled out rows")
+    # sampled h rows, including the first and last row of the busiest expert
+    cnt = np.diff(offsets)
+    e_big = int(np.argmax(cnt))
+    rows = np.unique(np.concatenate([rng.choice(int(offsets[-1]), 24, replace=False),
+                                     [offsets[e_big], offsets[e_big + 1] - 1]]))
+    h = to_np(b.h)
+    hg, hr = [], []
+    for p in rows:
+        t, e = int(src[p]) // wl.k, int(np.searchsorted(offsets, p, side="right") - 1)
+        g = x[t][None, :] @ w1[e]
+        hr.append(orc.round_to_bf16(orc.swiglu(g))[0])
+        hg.append(h[p])
+    _tol(np.array(hg), np.array(hr), f"{name}: sampled h rows")
+    assert int(b.dev_status.item()) == 0
