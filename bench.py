@@ -1,0 +1,330 @@
+"""Benchmark of the MoE expert block on GB300.
+
+A step is one pass of the whole block (counts -> fc1 + SwiGLU -> fc2 +
+weighted combine) over the ``uniform`` workload (T=4096 tokens, H=2048,
+I=768, E=64 experts, top-8, W=4 logical ranks, bf16), inputs already in HBM.
+L2 is flushed (a 256 MB write) between timed steps, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Prints one JSON line.  N > 1 (under torchrun) runs one independent replica
+per GPU (weak scaling): the block has no exchange step on one GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_expert_dispatch_histc_gb300.workloads import WORKLOADS, as_f64, make_inputs  # noqa: E402
+
+METRIC = "MoE expert-block tokens/s (1 GPU); grouped-GEMM TFLOP/s as fraction of GB300 bf16 peak"
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+GMM_SRC = os.path.join(ROOT, "moe_expert_dispatch_histc_gb300", "csrc", "gmm.cu")
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def _src_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _ncu_traffic(kernel_key, workload):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    p = os.path.join(PROFILE_DIR, "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(f"{kernel_key}:{workload}")
+    if not ent or ent.get("src_sha256_16") != _src_hash(GMM_SRC):
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.06)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(wl, inp, budget_s=12.0):
+    """The oracle as it stands, on host cores, on the first T_s tokens of the
+    same workload (all experts' weights, same routing)."""
+    from oracle import mc2_oracle as orc
+    x = as_f64(inp["x"], wl.act)
+    w1 = as_f64(inp["w1"], wl.act)
+    w2 = as_f64(inp["w2"], wl.act)
+    Ts, spent, done = 0, 0.0, 0
+    step = max(wl.W, (256 // wl.W) * wl.W)
+    while spent < budget_s and Ts < wl.T:
+        n = min(step, wl.T - Ts)
+        t0 = time.perf_counter()
+        orc.block_forward(x[Ts:Ts + n], w1, w2, inp["sel"][Ts:Ts + n], inp["probs"][Ts:Ts + n],
+                          wl.E, wl.W, h_dtype=wl.act)
+        spent += time.perf_counter() - t0
+        Ts += n
+        done += 1
+    return {"value": Ts / spent, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {Ts} of {wl.T} tokens of the {wl.name} workload in {done} chunks of "
+                      f"{step} tokens (float64 numpy oracle, all experts), {spent:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl, 0)
+    from oracle import mc2_oracle as orc
+    x = as_f64(inp["x"], wl.act)
+    w1 = as_f64(inp["w1"], wl.act)
+    w2 = as_f64(inp["w2"], wl.act)
+    Ts = max(wl.W, (64 // wl.W) * wl.W)   # bounded sample of the workload per step
+
+    def step(i):
+        a = (i * Ts) % wl.T
+        orc.block_forward(x[a:a + Ts], w1, w2, inp["sel"][a:a + Ts], inp["probs"][a:a + Ts],
+                          wl.E, wl.W, h_dtype=wl.act)
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = Ts * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(wl, l2="n/a (CPU)"),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"{Ts} tokens of the {wl.name} workload per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(wl, l2):
+    return {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+            "W": wl.W, "act": wl.act, "routing": wl.routing, "l2": l2,
+            "parallelism": "replicas" if int(os.environ.get("WORLD_SIZE", "1")) > 1 else "1gpu"}
+
+
+def run_cuda(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from moe_expert_dispatch_histc_gb300 import binding as B, block as blk
+    from moe_expert_dispatch_histc_gb300.build import build
+    build()
+    B.lib()
+
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl, 0)
+    d = blk.inputs_to_device(inp, wl)
+    b = blk.alloc_buffers(wl)
+    shape = blk.shape_of(wl)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")  # 256 MB > L2
+
+    def step():
+        B.mc2_moe_counts(shape, d["sel"], b.cnt, b.recv, b.offsets, b.permute_src,
+                         b.unpermute_dst, b.ws, b.dev_status, stream=stream)
+        n = B.mc2_last_launch_count()
+        ev[1].record(stream)
+        B.mc2_alltoallv_gmm(shape, d["x"], d["xs"], d["w1"], d["w1s"], b.offsets, b.permute_src,
+                            b.ws, b.h, b.h_scale, b.dev_status, stream=stream)
+        n += B.mc2_last_launch_count()
+        ev[2].record(stream)
+        B.mc2_gmm_alltoallv(shape, b.h, b.h_scale, d["w2"], d["w2s"], b.offsets, b.permute_src,
+                            b.unpermute_dst, d["probs"], b.ws, b.out, b.dev_status, stream=stream)
+        n += B.mc2_last_launch_count()
+        return n
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(args.warmup):
+        flush.zero_()
+        ev[0].record(stream)
+        step()
+        ev[3].record(stream)
+    torch.cuda.synchronize()
+    if int(b.dev_status.item()) != 0:
+        raise RuntimeError(f"device status {int(b.dev_status.item())} after warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    launches = 0
+    for i in range(args.steps):
+        flush.zero_()
+        ev = events[i]
+        ev[0].record(stream)
+        launches += step()
+        ev[3].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    seg = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
+                    for e in events])  # ms: counts, fc1, fc2+combine
+    total_ms = float(seg.sum())
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = wl.T * world * args.steps / (total_ms / 1e3)
+
+    # e2e: inputs from pinned host memory, result back to pinned host memory
+    h_x = torch.empty(d["x"].shape, dtype=d["x"].dtype).pin_memory()
+    h_x.copy_(d["x"].cpu())
+    h_sel = torch.from_numpy(inp["sel"]).pin_memory()
+    h_probs = torch.from_numpy(inp["probs"]).pin_memory()
+    h_out = torch.empty(b.out.shape, dtype=b.out.dtype).pin_memory()
+    e2e_steps = max(3, args.steps // 4)
+
+    def e2e_step():
+        d["x"].copy_(h_x, non_blocking=True)
+        d["sel"].copy_(h_sel, non_blocking=True)
+        d["probs"].copy_(h_probs, non_blocking=True)
+        blk.run_block(wl, d, b, stream=stream)
+        h_out.copy_(b.out, non_blocking=True)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = 0.0
+    for _ in range(e2e_steps):
+        flush.zero_()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms += s0.elapsed_time(s1)
+    bi = h_x.numel() * h_x.element_size() + h_sel.numel() * 4 + h_probs.numel() * 4
+    bo = h_out.numel() * h_out.element_size()
+    e2e_val = wl.T * world * e2e_steps / (e2e_ms / 1e3)
+
+    if rank != 0:
+        dist.barrier() if world > 1 else None
+        return
+    peaks, src = _peaks()
+    fc1_ms = float(seg[:, 1].mean())
+    fc2_ms = float(seg[:, 2].mean())
+    fc1_flops = 2 * wl.R * wl.H * 2 * wl.I
+    achieved = fc1_flops / (fc1_ms / 1e3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    tflops = wl.flops / ((fc1_ms + fc2_ms) / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": _config(wl, l2="flushed (256 MB write) between steps"),
+        "tflops": tflops, "tflops_frac_of_peak": tflops / peak,
+        "segments_ms": {"counts": float(seg[:, 0].mean()), "fc1_swiglu": fc1_ms,
+                        "fc2_combine": fc2_ms},
+        "roofline": {"kernel": "gmm_kernel<fc1> (permute gather + fc1 + SwiGLU)",
+                     "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": f"{src} bf16_tflops (burst)",
+                     "traffic": _ncu_traffic("gmm_fc1", wl.name)},
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, inp)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--workload", default="uniform", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_cuda(args)
+
+
+if __name__ == "__main__":
+    main()
