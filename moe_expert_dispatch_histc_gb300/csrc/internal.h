@@ -4,7 +4,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/mc2moe.h"
+#include "mc2moe.h"
 
 namespace mc2 {
 
