@@ -148,6 +148,28 @@ mc2_status_t mc2_gmm_alltoallv(const mc2_shape_t* s, const void* h, const float*
                                void* stream);
 
 /*
+ * mc2_moe_counts_static -- mc2_moe_counts for callers that cannot allocate
+ * device memory: same arguments and results, minus the workspace.  The paper
+ * has no counterpart; it exists because some callers cannot call cudaMalloc
+ * (a plugin inside a host application that owns all device memory through its
+ * own pool, a service whose device-memory budget is fixed at start-up).
+ *   - Scratch is a fixed array inside this library's device image (1 MiB on
+ *     every GPU that loads the library, held until the process exits).  The
+ *     shape must satisfy (E + 1) * W * ceil(T*k / W / 256) <= 131072, else the
+ *     call returns MC2_ERR_UNSUPPORTED and launches nothing.
+ *   - The first call on a device looks up that array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Allocates nothing and calls no allocating routine.
+ *   - Every call shares the one array: calls whose kernels may overlap on the
+ *     GPU (other streams, other host threads) race and corrupt each other's
+ *     results.  Serialise them, e.g. on one stream.
+ */
+mc2_status_t mc2_moe_counts_static(const mc2_shape_t* s, const int32_t* sel, int32_t* cnt,
+                                   int32_t* recv, int32_t* offsets, int32_t* permute_src,
+                                   int32_t* unpermute_dst, int32_t* dev_status, void* stream);
+
+/*
  * mc2_moe_forward -- the whole block (the three calls above, in order) on
  * device buffers.  cnt/recv/offsets/permute_src/unpermute_dst/h/h_scale are
  * outputs as above (h_scale may be NULL unless act is I8); out is [T, H].

@@ -46,6 +46,7 @@ _SIGS = {
     "mc2_check_shape": (ctypes.c_int, [_SP]),
     "mc2_workspace_bytes": (ctypes.c_size_t, [_SP]),
     "mc2_moe_counts": (ctypes.c_int, [_SP] + [_P] * 9),
+    "mc2_moe_counts_static": (ctypes.c_int, [_SP] + [_P] * 8),
     "mc2_alltoallv_gmm": (ctypes.c_int, [_SP] + [_P] * 11),
     "mc2_gmm_alltoallv": (ctypes.c_int, [_SP] + [_P] * 12),
     "mc2_moe_forward": (ctypes.c_int, [_SP] + [_P] * 19),
@@ -120,6 +121,18 @@ def mc2_moe_counts(shape, sel, cnt, recv, offsets, permute_src, unpermute_dst, w
                               _stream(stream))
     if check:
         _check("mc2_moe_counts", st)
+    return st
+
+
+def mc2_moe_counts_static(shape, sel, cnt, recv, offsets, permute_src, unpermute_dst,
+                          dev_status=None, stream=None, check=True):
+    """mc2_moe_counts without a workspace, for callers that cannot allocate
+    device memory; its scratch is a fixed array inside the library."""
+    st = lib().mc2_moe_counts_static(ctypes.byref(shape), _p(sel), _p(cnt), _p(recv),
+                                     _p(offsets), _p(permute_src), _p(unpermute_dst),
+                                     _p(dev_status), _stream(stream))
+    if check:
+        _check("mc2_moe_counts_static", st)
     return st
 
 

@@ -19,6 +19,8 @@ uint64_t wait_limit_ns() {
 
 void note_launches(int n) { tl_launches += n; }
 
+void reset_launches() { tl_launches = 0; }
+
 WsLayout ws_layout(const mc2_shape_t& s) {
   WsLayout L;
   std::memset(&L, 0, sizeof(L));

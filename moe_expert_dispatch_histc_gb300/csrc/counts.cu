@@ -17,6 +17,8 @@
 //                     a lane-mask popcount, giving a stable position.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "internal.h"
 
 namespace mc2 {
@@ -220,4 +222,92 @@ cudaError_t launch_counts(const mc2_shape_t& s, const int32_t* sel, int32_t* cnt
   return cudaGetLastError();
 }
 
+// ----------------------------------------------------------------------------
+// Counts with library-owned scratch (mc2_moe_counts_static).
+//
+// Some callers cannot allocate device memory on their own: for example a
+// plugin running inside a host application that owns every device
+// allocation through its own pool, or a service whose device-memory budget
+// is fixed when it starts.  For them the counts pass can use a fixed scratch
+// array that lives in this library's device image instead of a caller
+// workspace.  The array holds the two per-warp tables of the pass
+// (histogram and scan base), kStaticCountsEntries int32 each (1 MiB in
+// total); every GPU that loads the library keeps it until the process exits.
+// The kernels write every entry they later read, so nothing in it needs
+// clearing between calls.
+// ----------------------------------------------------------------------------
+constexpr int64_t kStaticCountsEntries = 131072;
+constexpr int kStaticMaxDevices = 64;
+
+static __device__ __align__(256) int32_t g_counts_scratch[2 * kStaticCountsEntries];
+
+static std::mutex g_counts_scratch_mu;
+static int32_t* g_counts_scratch_ptr[kStaticMaxDevices] = {};
+
+// Device address of g_counts_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+static cudaError_t counts_scratch_on_current_device(int32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kStaticMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_counts_scratch_mu);
+  if (!g_counts_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_counts_scratch);
+    if (e != cudaSuccess) return e;
+    g_counts_scratch_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_counts_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
 }  // namespace mc2
+
+extern "C" mc2_status_t mc2_moe_counts_static(const mc2_shape_t* s, const int32_t* sel,
+                                              int32_t* cnt, int32_t* recv, int32_t* offsets,
+                                              int32_t* permute_src, int32_t* unpermute_dst,
+                                              int32_t* dev_status, void* stream) {
+  using namespace mc2;
+  reset_launches();
+  if (mc2_check_shape(s) != MC2_OK) return MC2_ERR_INVALID_ARG;
+  if (!cnt || !recv || !offsets) return MC2_ERR_INVALID_ARG;
+  if (s->T > 0 && (!sel || !permute_src || !unpermute_dst)) return MC2_ERR_INVALID_ARG;
+  const CountsGeom geo = counts_geom(*s);
+  if (geo.EB * geo.G > kStaticCountsEntries) return MC2_ERR_UNSUPPORTED;  // beyond the fixed scratch
+  int32_t* scratch = nullptr;
+  if (counts_scratch_on_current_device(&scratch) != cudaSuccess) return MC2_ERR_CUDA;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CountsParams p;
+  p.sel = sel;
+  p.hist = scratch;
+  p.base = scratch + kStaticCountsEntries;
+  p.cnt = cnt;
+  p.recv = recv;
+  p.offsets = offsets;
+  p.permute_src = permute_src;
+  p.unpermute_dst = unpermute_dst;
+  p.dev_status = dev_status;
+  p.RW = geo.RW;
+  p.CPR = geo.CPR;
+  p.G = geo.G;
+  p.E = s->E;
+  p.W = s->W;
+  p.EB = static_cast<int>(geo.EB);
+  const size_t smem = static_cast<size_t>(kCountsWarpsPerBlock) * geo.EB * sizeof(int32_t);
+  const int blocks = static_cast<int>((geo.G + kCountsWarpsPerBlock - 1) / kCountsWarpsPerBlock);
+  int launches = 0;
+  if (blocks > 0) {
+    histc_warps<<<blocks, kCountsWarpsPerBlock * 32, smem, st>>>(p);
+    ++launches;
+  }
+  scan_counts<<<1, 1024, 0, st>>>(p);
+  ++launches;
+  if (blocks > 0) {
+    scatter_warps<<<blocks, kCountsWarpsPerBlock * 32, smem, st>>>(p);
+    ++launches;
+  }
+  note_launches(launches);
+  return cudaGetLastError() == cudaSuccess ? MC2_OK : MC2_ERR_CUDA;
+}

@@ -38,6 +38,7 @@ WsLayout ws_layout(const mc2_shape_t& s);
 
 uint64_t wait_limit_ns();
 void note_launches(int n);
+void reset_launches();
 
 // Launch wrappers (return cudaSuccess or the launch error).
 cudaError_t launch_counts(const mc2_shape_t& s, const int32_t* sel, int32_t* cnt, int32_t* recv,
