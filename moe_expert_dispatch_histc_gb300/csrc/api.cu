@@ -34,7 +34,7 @@ WsLayout ws_layout(const mc2_shape_t& s) {
   };
   L.hist = take(static_cast<size_t>(g.EB) * g.G * 4);
   L.base = take(static_cast<size_t>(g.EB) * g.G * 4);
-  L.slots = take(R * s.H * 4);
+  L.y = take(R * s.H * 4);
   if (s.act == MC2_F32) {
     L.x_t32 = take(static_cast<size_t>(s.T) * s.H * 4);
     L.w1_t32 = take(static_cast<size_t>(s.E) * s.H * 2 * s.I * 4);
@@ -123,15 +123,14 @@ mc2_status_t do_fc2(const mc2_shape_t* s, const void* h, const float* h_scale, c
   if (s->T == 0) return MC2_OK;
   const WsLayout L = ws_layout(*s);
   char* w = static_cast<char*>(ws);
-  float* slots = reinterpret_cast<float*>(w + L.slots);
+  float* y = reinterpret_cast<float*>(w + L.y);
   GemmArgs g;
   std::memset(&g, 0, sizeof(g));
   g.s = s;
   g.a = h;
   g.offsets = offsets;
   g.permute_src = permute_src;
-  g.probs = probs;
-  g.out = slots;
+  g.out = y;
   g.dev_status = dev_status;
   g.mode = 1;
   if (s->act == MC2_F32) {
@@ -147,7 +146,7 @@ mc2_status_t do_fc2(const mc2_shape_t* s, const void* h, const float* h_scale, c
     g.a_elem_bytes = 2;
   }
   cudaError_t e = launch_gemm(g, st);
-  if (e == cudaSuccess) e = launch_combine(*s, slots, offsets, unpermute_dst, out, s->out, st);
+  if (e == cudaSuccess) e = launch_combine(*s, y, probs, offsets, unpermute_dst, out, s->out, st);
   return cuda_status(e);
 }
 

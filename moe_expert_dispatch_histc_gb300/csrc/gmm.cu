@@ -4,21 +4,31 @@
 // "Execution path", steps 6-10):
 //
 //   fc1 (dispatch segment):  h[p, :] = SwiGLU( x[permute_src[p] / k, :] @ w1[e] )
-//        the permute is a TMA gather4 of token rows straight into the
-//        swizzled A tile; SwiGLU runs on the fp32 accumulator in TMEM.
-//   fc2 (combine segment):   slot[permute_src[p], :] = probs[permute_src[p]] * (h[p, :] @ w2[e])
-//        each (token, slot) pair owns one fp32 row of `slots`, written once,
-//        so the sum over slots (combine kernel) has a fixed order.
+//        the permute is a row gather straight into the swizzled A tile
+//        (cp.async by four gather warps); SwiGLU runs on the fp32
+//        accumulator in TMEM; h tiles leave through TMA stores.
+//   fc2 (combine segment):   y[p, :] = h[p, :] @ w2[e]   (fp32, expert-major)
+//        then combine_kernel: out[t] = sum_j probs[t, j] * y[unpermute_dst[t*k+j]]
+//        in ascending j -- every y row is written once, so the sum has a
+//        fixed order and the result is bitwise reproducible.
 //
-// One persistent kernel per segment, one CTA per SM, 6 warps:
-//   warp 0      TMA producer (A rows + B tiles into a 4-stage smem ring)
+// One persistent kernel per segment, one CTA per SM:
+//   warp 0      TMA producer of the B (weight) tiles (and of fc2's A tiles)
 //   warp 1      TMEM allocator and tcgen05.mma issuer (one lane)
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, math, global stores
-// Two 128x256 fp32 accumulators in TMEM (all 512 columns) let the epilogue of
-// tile i overlap the mainloop of tile i+1.  Tiles are (expert, n-tile,
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, math, swizzled smem
+//               staging, TMA store of 32-row boxes
+//   warps 6..9  fc1 only: gather of the A rows (cp.async, 16 B per lane)
+// A 4-stage ring of 48 KB stages (128-byte swizzle) feeds 128x256 UMMA tiles;
+// two 256-column fp32 accumulators in TMEM (all 512 columns) let the epilogue
+// of tile i overlap the mainloop of tile i+1.  Tiles are (expert, n-tile,
 // m-tile) triples over a per-expert tile prefix that each CTA builds from
 // `offsets`, so empty experts cost nothing and skewed ones just own more
-// tiles; CTAs take tiles round-robin.
+// tiles; CTAs take tiles round-robin, and the m-tiles of one (expert,
+// n-tile) are adjacent so concurrently running CTAs share its weight tile in L2.
+//
+// Why a cp.async gather and not TMA tile::gather4: on GB300 the gather4
+// version of fc1 took 537 us on the 4096-token workload against 237 us for
+// this one (and 183 us when x is pre-permuted), with bit-identical h.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -41,14 +51,13 @@ constexpr int STAGES = 4;
 constexpr int A_STAGE = BM * 128;  // 128 rows x 128 bytes of K
 constexpr int B_STAGE = 32768;     // (128/es) K rows x 256 columns x es bytes
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 512;
 
 struct GemmParams {
+  const void* a_ptr;            // fc1: x (rows gathered by the gather warps)
   const int32_t* offsets;
   const int32_t* permute_src;
-  const float* probs;
-  void* out;
+  void* out;                    // fc1: h [R, I]; fc2: y [R, H] fp32
   int32_t* dev_status;
   int E, k, K, n_tiles, out_cols, I;
   uint64_t wait_limit_ns;
@@ -103,10 +112,19 @@ __device__ __forceinline__ float round_tf32(float x) {
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
+template <int MODE>
+struct Roles {
+  static constexpr int kGatherWarps = MODE == MODE_FC1 ? 4 : 0;
+  static constexpr int kThreads = (6 + kGatherWarps) * 32;
+};
+
+constexpr int OUT_STAGE = 4096;  // per epilogue warp: 32 rows x 128 bytes
+constexpr size_t SMEM_BYTES_FIXED = 1024 + STAGES * STAGE_BYTES + 4 * OUT_STAGE + 256;
+
 template <int MODE, int ES>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const GemmParams p) {
+               const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
   using TR = ElemTraits<ES>;
   constexpr int BK = TR::BK;
   constexpr int BNB = 128 / ES;              // columns per 128-byte B block
@@ -115,13 +133,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int KK_B = (32 / ES) * 128;      // B bytes per UMMA K step
   constexpr bool BKM = TR::B_KMAJOR;
   constexpr uint32_t IDESC = instr_desc(TR::FMT, false, !BKM, BM, BN);
+  constexpr bool GATHER = MODE == MODE_FC1;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_STAGE);
+  uint8_t* sOut = sB + STAGES * B_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * OUT_STAGE);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -135,7 +155,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      // fc1: the TMA arm of the B tile plus one arrival per gather thread
+      mbar_init(&full[s], GATHER ? 1 + 32 * Roles<MODE>::kGatherWarps : 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -148,8 +169,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fence_proxy_async_smem();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
+    if (!GATHER) tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmOut);
   }
   if (warp == 1) {
     tmem_alloc(tmem_base_sh, TMEM_COLS);
@@ -180,42 +202,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_base_sh;
   const int total = prefix[E];
   WaitCtl ctl{abort_sh, p.wait_limit_ns, p.dev_status};
+  const int kblocks = p.K / BK;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ TMA producer
     int s = 0;
     uint32_t ph = 0;
     int n_arm = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       int e, n, row0, rows;
       decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
-      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-      if (MODE == MODE_FC1) {  // token rows of this lane's four permuted rows
-        const int tok0 = __ldg(p.permute_src + row0) / p.k;
-        int rr[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int row = lane * 4 + q;
-          rr[q] = row < rows ? __ldg(p.permute_src + row0 + row) / p.k : tok0;
-        }
-        r0 = rr[0]; r1 = rr[1]; r2 = rr[2]; r3 = rr[3];
-      }
-      bool ok = true;
-      for (int kb = 0; kb < p.K / BK; ++kb) {
+      for (int kb = 0; kb < kblocks; ++kb) {
         if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, ctl);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-        __syncwarp();
-        uint8_t* a_dst = sA + s * A_STAGE;
-        uint8_t* b_dst = sB + s * B_STAGE;
-        const int k0 = kb * BK;
-        if (MODE == MODE_FC1) {
-          tma_gather4(a_dst + lane * 512, &tmA, &full[s], k0, r0, r1, r2, r3);
-        } else if (lane == 0) {
-          tma_load_2d(a_dst, &tmA, &full[s], k0, row0);
-        }
         if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], GATHER ? B_STAGE : STAGE_BYTES);
+          uint8_t* b_dst = sB + s * B_STAGE;
+          const int k0 = kb * BK;
+          if (!GATHER) tma_load_2d(sA + s * A_STAGE, &tmA, &full[s], k0, row0);
           if constexpr (BKM) {
             // K-major B: N rows of 128 bytes of K; fc1 loads the gate rows
             // and the up rows of the same output columns as two boxes
@@ -229,7 +235,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
               int ncol;
-              if (MODE == MODE_FC1) {
+              if (MODE == MODE_FC1) {  // gate half, then up half of the same columns
                 const int half = b / (NB / 2), bb = b % (NB / 2);
                 ncol = half * p.I + n * (BN / 2) + bb * BNB;
               } else {
@@ -239,10 +245,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
         }
+        __syncwarp();
         ++n_arm;
         if (++s == STAGES) { s = 0; ph ^= 1; }
       }
-      if (!ok) break;
     }
     // Let every armed stage land before the CTA can exit (bounded).
     if (lane == 0) {
@@ -266,7 +272,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
-      for (int kb = 0; kb < p.K / BK; ++kb) {
+      for (int kb = 0; kb < kblocks; ++kb) {
         if (lane == 0) ok = mbar_wait(&full[s], ph, ctl);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -299,10 +305,68 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_wait(mma_done, 0, drain);
     }
     __syncwarp();
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ fc1 row gather
+    // Thread t copies 16-byte chunk (t % 8) of rows t/8 + 16*i, i = 0..7, of
+    // the 128-row A tile: 8 lanes cover one 128-byte row segment, so each
+    // warp instruction reads four whole rows.  The chunk lands at its 128B
+    // swizzle position.  Up to STAGES-1 cp.async groups stay in flight; a
+    // stage is signalled (full[s]) once this thread's copies into it are
+    // complete and made visible to the tensor core's async proxy.  (With
+    // STAGES groups in flight the signal for stage g-3 would wait until the
+    // MMA released stage g-4, idling the tensor core once per stage.)
+    const int t = threadIdx.x - 6 * 32;
+    const int chunk = t & 7, rsub = t >> 3;
+    const char* xg = static_cast<const char*>(p.a_ptr);
+    const int64_t row_bytes = static_cast<int64_t>(p.K) * ES;
+    int s = 0;
+    uint32_t ph = 0;
+    int issued = 0, arrived = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int e, n, row0, rows;
+      decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
+      const int tok0 = __ldg(p.permute_src + row0) / p.k;  // tail rows repeat a valid row
+      const char* src[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = rsub + 16 * i;
+        const int tok = r < rows ? __ldg(p.permute_src + row0 + r) / p.k : tok0;
+        src[i] = xg + tok * row_bytes + chunk * 16;
+      }
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, ctl);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const uint32_t a_dst = smem_u32(sA + s * A_STAGE);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = rsub + 16 * i;
+          cp_async16(a_dst + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + kb * 128);
+        }
+        cp_async_commit();
+        ++issued;
+        if (issued - arrived == STAGES - 1) {
+          cp_async_wait<STAGES - 2>();
+          fence_proxy_async_smem();
+          mbar_arrive(&full[arrived % STAGES]);
+          ++arrived;
+        }
+        if (++s == STAGES) { s = 0; ph ^= 1; }
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (; arrived < issued; ++arrived) mbar_arrive(&full[arrived % STAGES]);
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;         // TMEM lane quarter this warp may access
-    const int row = q * 32 + lane;  // accumulator row = TMEM lane
+    // Warp q owns accumulator rows 32q..32q+31 (TMEM lane quarter q).  Each
+    // 128-byte column group of its rows is staged in swizzled smem and
+    // written by one TMA store of a 32-row box; a warp whose rows run past
+    // the end of the expert stores its valid rows directly instead.
+    const int q = warp & 3;
+    uint8_t* stage = sOut + q * OUT_STAGE;
+    const uint32_t row_off = static_cast<uint32_t>(lane) * 128;
     int acc = 0;
     uint32_t aph = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -314,68 +378,76 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
-      const bool valid = row < rows;
-      if (MODE == MODE_FC1) {
-        const int grow = row0 + row;
+      const int wrows = min(32, rows - q * 32);       // valid rows of this warp
+      const int grow0 = row0 + q * 32;                 // first global row of this warp
+      if (wrows > 0) {
+        constexpr int GROUP_COLS = 128 / (MODE == MODE_FC1 ? ES : 4);  // output cols per 128 B
+        constexpr int NGROUPS = (MODE == MODE_FC1 ? BN / 2 : BN) / GROUP_COLS;
 #pragma unroll 1
-        for (int c = 0; c < (BN / 2) / 32; ++c) {
-          const int col0 = n * (BN / 2) + c * 32;
+        for (int gi = 0; gi < NGROUPS; ++gi) {
+          const int col0 = n * (MODE == MODE_FC1 ? BN / 2 : BN) + gi * GROUP_COLS;
           if (col0 >= p.out_cols) break;
-          uint32_t g[32], u[32];
-          tmem_ld32(tbase + c * 32, g);
-          tmem_ld32(tbase + BN / 2 + c * 32, u);
-          tmem_ld_wait();
-          if (valid) {
-            if (ES == 2) {
-              uint32_t packed[16];
+          // the previous store out of this warp's staging buffer has read it
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+          if (MODE == MODE_FC1 && ES == 2) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float h0 = silu_f(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
-                const float h1 =
-                    silu_f(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-                packed[i] = pack_bf16x2(h0, h1);
+            for (int half = 0; half < 2; ++half) {
+              uint32_t g[32], u[32];
+              const int c = gi * 64 + half * 32;
+              tmem_ld32(tbase + c, g);
+              tmem_ld32(tbase + BN / 2 + c, u);
+              tmem_ld_wait();
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                pk[i] = pack_bf16x2(silu_f(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]),
+                                    silu_f(__uint_as_float(g[2 * i + 1])) *
+                                        __uint_as_float(u[2 * i + 1]));
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const int ch = half * 4 + v;
+                *reinterpret_cast<uint4*>(stage + row_off + ((ch ^ (lane & 7)) << 4)) =
+                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
               }
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                                    static_cast<int64_t>(grow) * p.out_cols + col0);
-#pragma unroll
-              for (int v = 0; v < 4; ++v)
-                dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                                    packed[4 * v + 3]);
-            } else {
-              float hv[32];
+            }
+          } else {
+            uint32_t v32[32];
+            if (MODE == MODE_FC1) {  // fp32 h, tf32-rounded for the fc2 tensor-core pass
+              uint32_t g[32];
+              tmem_ld32(tbase + gi * 32, g);
+              tmem_ld32(tbase + BN / 2 + gi * 32, v32);
+              tmem_ld_wait();
 #pragma unroll
               for (int i = 0; i < 32; ++i)
-                hv[i] = round_tf32(silu_f(__uint_as_float(g[i])) * __uint_as_float(u[i]));
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) +
-                                                      static_cast<int64_t>(grow) * p.out_cols + col0);
-#pragma unroll
-              for (int v = 0; v < 8; ++v)
-                dst[v] = make_float4(hv[4 * v], hv[4 * v + 1], hv[4 * v + 2], hv[4 * v + 3]);
+                v32[i] = __float_as_uint(
+                    round_tf32(silu_f(__uint_as_float(g[i])) * __uint_as_float(v32[i])));
+            } else {
+              tmem_ld32(tbase + gi * 32, v32);
+              tmem_ld_wait();
             }
-          }
-        }
-      } else {
-        int flat = 0;
-        float prob = 0.f;
-        if (valid) {
-          flat = __ldg(p.permute_src + row0 + row);
-          prob = __ldg(p.probs + flat);
-        }
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          const int col0 = n * BN + c * 32;
-          if (col0 >= p.out_cols) break;
-          uint32_t v[32];
-          tmem_ld32(tbase + c * 32, v);
-          tmem_ld_wait();
-          if (valid) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) +
-                                                    static_cast<int64_t>(flat) * p.out_cols + col0);
 #pragma unroll
-            for (int w = 0; w < 8; ++w)
-              dst[w] = make_float4(prob * __uint_as_float(v[4 * w]), prob * __uint_as_float(v[4 * w + 1]),
-                                   prob * __uint_as_float(v[4 * w + 2]), prob * __uint_as_float(v[4 * w + 3]));
+            for (int v = 0; v < 8; ++v)
+              *reinterpret_cast<uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4)) =
+                  make_uint4(v32[4 * v], v32[4 * v + 1], v32[4 * v + 2], v32[4 * v + 3]);
           }
+          if (wrows == 32) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmOut, stage, col0, grow0);
+              bulk_commit();
+            }
+          } else if (lane < wrows) {  // tail rows: plain stores of this lane's row
+            char* dst = static_cast<char*>(p.out) +
+                        (static_cast<int64_t>(grow0 + lane) * p.out_cols + col0) *
+                            (MODE == MODE_FC1 ? ES : 4);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              reinterpret_cast<uint4*>(dst)[v] =
+                  *reinterpret_cast<const uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4));
+          }
+          __syncwarp();
         }
       }
       tc_fence_before();
@@ -383,6 +455,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       acc ^= 1;
       if (acc == 0) aph ^= 1;
     }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -392,9 +466,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ----------------------------------------------------------------------------
-// combine: out[t, :] = sum_j slots[t*k + j, :] over valid pairs, j ascending
+// combine (unpermute with probs): out[t, :] = sum_j probs[t, j] * y[unpermute_dst[t*k + j], :]
+// over valid pairs, products rounded to fp32 and summed in ascending j.
 // ----------------------------------------------------------------------------
-__global__ void combine_kernel(const float* __restrict__ slots, const int32_t* __restrict__ offsets,
+__global__ void combine_kernel(const float* __restrict__ y, const float* __restrict__ probs,
+                               const int32_t* __restrict__ offsets,
                                const int32_t* __restrict__ unpermute_dst, void* __restrict__ out,
                                int64_t T, int H, int k, int E, int out_bf16) {
   const int64_t H4 = H / 4;
@@ -406,9 +482,14 @@ __global__ void combine_kernel(const float* __restrict__ slots, const int32_t* _
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int j = 0; j < k; ++j) {
     const int64_t flat = t * k + j;
-    if (__ldg(unpermute_dst + flat) >= nvalid) continue;
-    const float4 v = __ldg(reinterpret_cast<const float4*>(slots + flat * H + c));
-    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    const int32_t row = __ldg(unpermute_dst + flat);
+    if (row >= nvalid) continue;
+    const float pj = __ldg(probs + flat);
+    const float4 v = __ldg(reinterpret_cast<const float4*>(y + static_cast<int64_t>(row) * H + c));
+    acc.x += __fmul_rn(pj, v.x);
+    acc.y += __fmul_rn(pj, v.y);
+    acc.z += __fmul_rn(pj, v.z);
+    acc.w += __fmul_rn(pj, v.w);
   }
   if (out_bf16) {
     uint2 w;
@@ -517,11 +598,11 @@ static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
   const CUtensorMapDataType dt =
       ES == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const int64_t R = static_cast<int64_t>(s.T) * s.k;
-  CUtensorMap tA, tB;
+  CUtensorMap tA, tB, tOut;
   GemmParams p;
+  p.a_ptr = g.a;
   p.offsets = g.offsets;
   p.permute_src = g.permute_src;
-  p.probs = g.probs;
   p.out = g.out;
   p.dev_status = g.dev_status;
   p.E = s.E;
@@ -533,30 +614,32 @@ static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
     p.K = s.H;
     p.n_tiles = (s.I + BN / 2 - 1) / (BN / 2);
     p.out_cols = s.I;
-    ok = encode_2d(&tA, dt, ES, g.a, s.H, s.T, 128 / ES, 1) &&
-         (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.H, 2ull * s.I, s.E, TR::BK, BN / 2)
-                       : encode_3d(&tB, dt, ES, g.b, 2ull * s.I, s.H, s.E, 128 / ES, TR::BK));
+    ok = (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.H, 2ull * s.I, s.E, TR::BK, BN / 2)
+                       : encode_3d(&tB, dt, ES, g.b, 2ull * s.I, s.H, s.E, 128 / ES, TR::BK)) &&
+         encode_2d(&tOut, dt, ES, g.out, s.I, R, 128 / ES, 32);
+    tA = tB;  // unused: fc1's A rows are gathered with cp.async
   } else {
     p.K = s.I;
     p.n_tiles = (s.H + BN - 1) / BN;
     p.out_cols = s.H;
     ok = encode_2d(&tA, dt, ES, g.a, s.I, R, 128 / ES, BM) &&
          (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.I, s.H, s.E, TR::BK, BN)
-                       : encode_3d(&tB, dt, ES, g.b, s.H, s.I, s.E, 128 / ES, TR::BK));
+                       : encode_3d(&tB, dt, ES, g.b, s.H, s.I, s.E, 128 / ES, TR::BK)) &&
+         encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.out, s.H, R, 32, 32);
   }
   if (!ok) return cudaErrorInvalidValue;
-  const size_t smem = 1024 + STAGES * STAGE_BYTES + 256 + (s.E + 1) * sizeof(int32_t);
+  const size_t smem = SMEM_BYTES_FIXED + (s.E + 1) * sizeof(int32_t);
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(gmm_kernel<MODE, ES>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    1024 + STAGES * STAGE_BYTES + 256 + 1025 * 4);
+                                    static_cast<int>(SMEM_BYTES_FIXED + 1025 * sizeof(int32_t)));
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t tiles_upper = (R / BM + s.E) * static_cast<int64_t>(p.n_tiles);
   const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_upper, 1)));
-  gmm_kernel<MODE, ES><<<grid, NUM_THREADS, smem, st>>>(tA, tB, p);
+  gmm_kernel<MODE, ES><<<grid, Roles<MODE>::kThreads, smem, st>>>(tA, tB, tOut, p);
   return cudaGetLastError();
 }
 
@@ -571,15 +654,15 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
   return e;
 }
 
-cudaError_t launch_combine(const mc2_shape_t& s, const float* slots, const int32_t* offsets,
-                           const int32_t* unpermute_dst, void* out, int out_dtype,
-                           cudaStream_t st) {
+cudaError_t launch_combine(const mc2_shape_t& s, const float* y, const float* probs,
+                           const int32_t* offsets, const int32_t* unpermute_dst, void* out,
+                           int out_dtype, cudaStream_t st) {
   const int64_t n = static_cast<int64_t>(s.T) * (s.H / 4);
   if (n == 0) return cudaSuccess;
   const int threads = 256;
   const int64_t blocks = (n + threads - 1) / threads;
   combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
-      slots, offsets, unpermute_dst, out, s.T, s.H, s.k, s.E, out_dtype == MC2_BF16 ? 1 : 0);
+      y, probs, offsets, unpermute_dst, out, s.T, s.H, s.k, s.E, out_dtype == MC2_BF16 ? 1 : 0);
   note_launches(1);
   return cudaGetLastError();
 }

@@ -26,7 +26,7 @@ CountsGeom counts_geom(const mc2_shape_t& s);
 // Workspace layout (byte offsets from ws).
 struct WsLayout {
   size_t hist, base;     // int32 [EB * G] each
-  size_t slots;          // fp32 [R, H] weighted fc2 rows (combine input)
+  size_t y;              // fp32 [R, H] fc2 rows, expert-major (combine input)
   size_t x_t32, w1_t32, w2_t32;  // fp32 tf32-rounded copies, weights transposed to [E, N, K] (act F32 only)
   size_t h_f32;          // fp32 [R, I] pre-requant SwiGLU output (act I8 only)
   size_t rowmax;         // uint32 [R] row absmax bits (act I8 only)
@@ -51,10 +51,9 @@ struct GemmArgs {
   const void* b;            // fc1: w1 [E, H, 2I]; fc2: w2 [E, I, H]
   const int32_t* offsets;
   const int32_t* permute_src;
-  const float* probs;       // fc2 only
   const float* a_scale;     // int8: per-token (fc1) or per-row (fc2)
   const float* b_scale;     // int8: per-channel
-  void* out;                // fc1: h; fc2: fp32 slots [R, H]
+  void* out;                // fc1: h [R, I]; fc2: y [R, H] fp32
   float* out_scale;         // unused by the GEMM itself
   uint32_t* rowmax;         // int8 fc1: row absmax bits
   int32_t* dev_status;
@@ -63,9 +62,9 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st);
 
-cudaError_t launch_combine(const mc2_shape_t& s, const float* slots, const int32_t* offsets,
-                           const int32_t* unpermute_dst, void* out, int out_dtype,
-                           cudaStream_t st);
+cudaError_t launch_combine(const mc2_shape_t& s, const float* y, const float* probs,
+                           const int32_t* offsets, const int32_t* unpermute_dst, void* out,
+                           int out_dtype, cudaStream_t st);
 cudaError_t launch_round_tf32(const float* src, float* dst, size_t n, cudaStream_t st);
 cudaError_t launch_transpose_round_tf32(const float* src, float* dst, int batch, int rows,
                                        int cols, cudaStream_t st);

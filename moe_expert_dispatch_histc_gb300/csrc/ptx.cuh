@@ -1,5 +1,5 @@
 // ptx.cuh -- inline-PTX building blocks for sm_103a: mbarriers with bounded
-// waits, TMA tile / gather4 loads, and the tcgen05 (TMEM + UMMA) instructions.
+// waits, TMA tile loads and stores, cp.async, and the tcgen05 (TMEM + UMMA) instructions.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -120,17 +120,44 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
-// Four rows (r0..r3) of a 2-D tensor, columns [col, col + box width), into
-// four consecutive box rows of `dst`.  The tensor map's box is one row high.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar,
-                                            int32_t col, int32_t r0, int32_t r1, int32_t r2,
-                                            int32_t r3) {
+// Shared -> global tile store through a tensor map (bulk async-group).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int32_t c0,
+                                             int32_t c1) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(col), "r"(r0), "r"(r1),
-      "r"(r2), "r"(r3)
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1)
       : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// The smem sources of every committed bulk store may be overwritten.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Every committed bulk store has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// ----------------------------------------------------------------------------
+// cp.async (16-byte, L2-cached) for row gathers the tensor maps cannot express
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ----------------------------------------------------------------------------
