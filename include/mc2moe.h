@@ -52,6 +52,7 @@ typedef enum {
 /* bits of the device status word */
 #define MC2_DEV_BAD_EXPERT_ID 0x1
 #define MC2_DEV_TIMEOUT 0x2
+#define MC2_DEV_INTERNAL 0x4  /* the two CTAs of a pair were given different TMEM; work skipped */
 
 typedef enum {
   MC2_F32 = 0,   /* fp32 values; matmuls on tensor cores in tf32 (inputs rounded to nearest) */
@@ -193,6 +194,13 @@ mc2_status_t mc2_selftest_wait(uint64_t limit_ns, int32_t* dev_status, void* str
 /* Set the device-side wait limit (nanoseconds) used by later launches of
  * this process; 0 restores the default (2 s). Host only. */
 void mc2_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Grouped-GEMM tiling for later launches of this process: 0 = automatic
+ * (fc2 on CTA pairs with 256x256 tiles when experts average >= 256 rows,
+ * everything else on one CTA per 128x256 tile), 1 = always single CTAs,
+ * 2 = always CTA pairs.  The choice does not change any result bit: both
+ * tilings accumulate each output in the same K order.  Host only. */
+void mc2_set_tile_pairing(int32_t mode);
 
 /* Number of kernel launches the last successful call on this host thread
  * enqueued. Host only. */

@@ -18,7 +18,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "mc2moe.h")
 
 MC2_OK, MC2_ERR_INVALID_ARG, MC2_ERR_UNSUPPORTED, MC2_ERR_CUDA = 0, 1, 2, 3
 MC2_ERR_DEVICE_TIMEOUT, MC2_ERR_BAD_EXPERT_ID = 4, 5
-MC2_DEV_BAD_EXPERT_ID, MC2_DEV_TIMEOUT = 0x1, 0x2
+MC2_DEV_BAD_EXPERT_ID, MC2_DEV_TIMEOUT, MC2_DEV_INTERNAL = 0x1, 0x2, 0x4
 DTYPE = {"f32": 0, "bf16": 1, "i8": 2, "i32": 3}
 
 
@@ -52,6 +52,7 @@ _SIGS = {
     "mc2_moe_forward": (ctypes.c_int, [_SP] + [_P] * 19),
     "mc2_selftest_wait": (ctypes.c_int, [ctypes.c_uint64, _P, _P]),
     "mc2_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+    "mc2_set_tile_pairing": (None, [ctypes.c_int32]),
     "mc2_last_launch_count": (ctypes.c_int32, []),
     "mc2_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -177,6 +178,10 @@ def mc2_selftest_wait(limit_ns, dev_status, stream=None, check=True):
 
 def mc2_set_wait_limit_ns(limit_ns: int) -> None:
     lib().mc2_set_wait_limit_ns(int(limit_ns))
+
+
+def mc2_set_tile_pairing(mode: int) -> None:
+    lib().mc2_set_tile_pairing(int(mode))
 
 
 def mc2_last_launch_count() -> int:

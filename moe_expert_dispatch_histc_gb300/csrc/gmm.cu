@@ -53,6 +53,17 @@ constexpr int B_STAGE = 32768;     // (128/es) K rows x 256 columns x es bytes
 constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int TMEM_COLS = 512;
 
+// cp.async groups a gather thread keeps in flight before it signals the
+// oldest stage.  Stage g is signalled when stage g+depth-1 is issued, which
+// needs the MMA to have released stage g+depth-1-STAGES; the smaller the
+// depth, the earlier the signal relative to the MMA's need for stage g.
+#ifndef MC2_GATHER_DEPTH
+#define MC2_GATHER_DEPTH 2
+#endif
+#ifndef MC2_PAIR_GATHER_DEPTH
+#define MC2_PAIR_GATHER_DEPTH 3
+#endif
+
 struct GemmParams {
   const void* a_ptr;            // fc1: x (rows gathered by the gather warps)
   const int32_t* offsets;
@@ -110,7 +121,10 @@ __device__ __forceinline__ float round_tf32(float x) {
   return __uint_as_float(r);
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+// silu(g) = g / (1 + e^-g) with the fast exponential and division
+// (relative error of a few fp32 ulp, far below the bf16 rounding of h).
+// For g << 0, e^-g overflows to +inf and the quotient is -0.
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 template <int MODE>
 struct Roles {
@@ -310,11 +324,9 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     // Thread t copies 16-byte chunk (t % 8) of rows t/8 + 16*i, i = 0..7, of
     // the 128-row A tile: 8 lanes cover one 128-byte row segment, so each
     // warp instruction reads four whole rows.  The chunk lands at its 128B
-    // swizzle position.  Up to STAGES-1 cp.async groups stay in flight; a
+    // swizzle position.  MC2_GATHER_DEPTH cp.async groups stay in flight; a
     // stage is signalled (full[s]) once this thread's copies into it are
-    // complete and made visible to the tensor core's async proxy.  (With
-    // STAGES groups in flight the signal for stage g-3 would wait until the
-    // MMA released stage g-4, idling the tensor core once per stage.)
+    // complete and made visible to the tensor core's async proxy.
     const int t = threadIdx.x - 6 * 32;
     const int chunk = t & 7, rsub = t >> 3;
     const char* xg = static_cast<const char*>(p.a_ptr);
@@ -346,8 +358,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
         }
         cp_async_commit();
         ++issued;
-        if (issued - arrived == STAGES - 1) {
-          cp_async_wait<STAGES - 2>();
+        if (issued - arrived == MC2_GATHER_DEPTH) {
+          cp_async_wait<MC2_GATHER_DEPTH - 1>();
           fence_proxy_async_smem();
           mbar_arrive(&full[arrived % STAGES]);
           ++arrived;
@@ -463,6 +475,397 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ----------------------------------------------------------------------------
+// CTA-pair variant: one 256x256 UMMA tile per cluster of two CTAs
+// (tcgen05 cta_group::2).  Each CTA owns 128 rows of A and 128 columns of B
+// -- fc1: the even CTA the gate half, the odd CTA the up half of the same 128
+// output columns -- so each SM streams 32 KB per k-block instead of 48 KB,
+// and six stages fit.  The even CTA issues the MMAs and commits to barriers
+// in both CTAs; the odd CTA's idle MMA warp relays "stage s landed here" to
+// the even CTA.  Each CTA's TMEM holds all 256 accumulator columns of its 128
+// rows, so the epilogue is the single-CTA one; two accumulators in TMEM let
+// the epilogue of tile i overlap the mainloop of tile i+1.
+// ----------------------------------------------------------------------------
+constexpr int P_STAGES = 6;
+constexpr int P_B_STAGE = 16384;                 // (128/es) K rows x 128 columns x es
+constexpr int P_STAGE_BYTES = A_STAGE + P_B_STAGE;
+constexpr int P_TMEM_COLS = 512;                 // two 256-column fp32 accumulators
+constexpr size_t P_SMEM_BYTES_FIXED = 1024 + P_STAGES * P_STAGE_BYTES + 4 * OUT_STAGE + 512;
+
+template <int MODE, int ES>
+__global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
+    gmm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+  using TR = ElemTraits<ES>;
+  constexpr int BK = TR::BK;
+  constexpr int BNB = 128 / ES;              // columns per 128-byte B block
+  constexpr int NBH = (BN / 2) / BNB;        // B blocks per CTA per stage
+  constexpr int B_BLOCK = BK * 128;
+  constexpr int KK_B = (32 / ES) * 128;
+  constexpr bool BKM = TR::B_KMAJOR;
+  constexpr uint32_t IDESC = instr_desc(TR::FMT, false, !BKM, 2 * BM, BN);
+  constexpr bool GATHER = MODE == MODE_FC1;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + P_STAGES * A_STAGE;
+  uint8_t* sOut = sB + P_STAGES * P_B_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * OUT_STAGE);
+  uint64_t* pfull = full + P_STAGES;       // even CTA: the odd CTA's stage landed
+  uint64_t* empty = pfull + P_STAGES;
+  uint64_t* tfull = empty + P_STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_sh = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
+  int32_t* prefix = reinterpret_cast<int32_t*>(tmem_base_sh + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(&full[s], GATHER ? 1 + 32 * Roles<MODE>::kGatherWarps : 1);
+      mbar_init(&pfull[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2 * 4);  // one arrival per epilogue warp of both CTAs
+    }
+    mbar_init(mma_done, 1);
+    *abort_sh = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    if (!GATHER) tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_base_sh, P_TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  if (warp == 2) {  // per-expert tile prefix: ceil(rows_e / 256) * n_tiles
+    int run = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      int t = 0;
+      if (e < E) {
+        const int rows = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+        t = ((rows + 2 * BM - 1) / (2 * BM)) * p.n_tiles;
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += y;
+      }
+      if (e < E) prefix[e + 1] = run + t;
+      run += __shfl_sync(0xffffffffu, t, 31);
+    }
+    if (lane == 0) prefix[0] = 0;
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_sh;
+  // Both CTAs of the pair must hold the same TMEM address: the MMA writes the
+  // accumulator at one address in both.  Anything else aborts the kernel.
+  const uint32_t peer_base = ld_shared_cluster_u32(map_to_rank(tmem_base_sh, rank ^ 1u));
+  int total = prefix[E];
+  if (peer_base != tmem_base) {
+    if (threadIdx.x == 0 && p.dev_status) atomicOr(p.dev_status, 0x4);
+    total = 0;
+  }
+  WaitCtl ctl{abort_sh, p.wait_limit_ns, p.dev_status};
+  const int kblocks = p.K / BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int s = 0;
+    uint32_t ph = 0;
+    int n_arm = 0;
+    bool ok = true;
+    for (int tile = cluster; tile < total && ok; tile += nclusters) {
+      int e, n, prow0, prows;
+      decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, prow0, prows);
+      (void)prows;
+      // decode_tile works in units of BM rows; a pair tile spans 2*BM rows
+      const int local = tile - prefix[e];
+      const int m_pairs = (prefix[e + 1] - prefix[e]) / p.n_tiles;
+      const int mp = local - (local / m_pairs) * m_pairs;
+      const int row0 = __ldg(p.offsets + e) + mp * 2 * BM + static_cast<int>(rank) * BM;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (lane == 0) ok = mbar_wait_cluster(&empty[s], ph ^ 1, ctl);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], GATHER ? P_B_STAGE : P_STAGE_BYTES);
+          uint8_t* b_dst = sB + s * P_B_STAGE;
+          const int k0 = kb * BK;
+          if (!GATHER) tma_load_2d(sA + s * A_STAGE, &tmA, &full[s], k0, row0);
+          // this CTA's 128 columns of B: fc1 gate (even) or up (odd) half;
+          // fc2 the first or second 128 of the 256-column tile
+          const int nbase = MODE == MODE_FC1 ? static_cast<int>(rank) * p.I + n * (BN / 2)
+                                             : n * BN + static_cast<int>(rank) * (BN / 2);
+          if constexpr (BKM) {
+            tma_load_3d(b_dst, &tmB, &full[s], k0, nbase, e);
+          } else {
+#pragma unroll
+            for (int b = 0; b < NBH; ++b)
+              tma_load_3d(b_dst + b * B_BLOCK, &tmB, &full[s], nbase + b * BNB, k0, e);
+          }
+        }
+        __syncwarp();
+        ++n_arm;
+        if (++s == P_STAGES) { s = 0; ph ^= 1; }
+      }
+    }
+    if (lane == 0) {  // every armed stage has landed and every commit to it has arrived
+      volatile int never = 0;
+      WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
+      for (int st = 0; st < P_STAGES && st < n_arm; ++st) {
+        const int last = st + P_STAGES * ((n_arm - 1 - st) / P_STAGES);
+        mbar_wait(&full[st], (last / P_STAGES) & 1, drain);
+        mbar_wait_cluster(&empty[st], (last / P_STAGES) & 1, drain);
+      }
+    }
+  } else if (warp == 1) {
+    if (leader) {
+      // ---------------------------------------------------------- MMA issuer
+      int s = 0, acc = 0;
+      uint32_t ph = 0, aph = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < total && ok; tile += nclusters) {
+        if (lane == 0) ok = mbar_wait_cluster(&tempty[acc], aph ^ 1, ctl);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (lane == 0) {
+            ok = mbar_wait(&full[s], ph, ctl);
+            if (ok) ok = mbar_wait_cluster(&pfull[s], ph, ctl);
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a_base = smem_u32(sA + s * A_STAGE);
+            const uint32_t b_base = smem_u32(sB + s * P_B_STAGE);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+              const uint64_t bdesc = BKM ? smem_desc_sw128(b_base + kk * 32, 16, 1024)
+                                         : smem_desc_sw128(b_base + kk * KK_B, B_BLOCK, 1024);
+              umma_pair<TR::KIND>(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0);
+            }
+            umma_commit_pair(&empty[s], 0x3);
+          }
+          __syncwarp();
+          if (++s == P_STAGES) { s = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        if (lane == 0) umma_commit_pair(&tfull[acc], 0x3);
+        __syncwarp();
+        acc ^= 1;
+        if (acc == 0) aph ^= 1;
+      }
+      if (lane == 0) {
+        umma_commit_pair(mma_done, 0x1);
+        volatile int never = 0;
+        WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
+        mbar_wait_cluster(mma_done, 0, drain);
+      }
+      __syncwarp();
+    } else {
+      // ---------------------------------------------------------- relay (odd CTA)
+      const uint32_t leader_pfull = map_to_rank(pfull, 0);
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < total && ok; tile += nclusters) {
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (lane == 0) {
+            ok = mbar_wait(&full[s], ph, ctl);
+            if (ok) mbar_arrive_remote_relaxed(leader_pfull + s * 8);
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (++s == P_STAGES) { s = 0; ph ^= 1; }
+        }
+      }
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ fc1 row gather
+    const int t = threadIdx.x - 6 * 32;
+    const int chunk = t & 7, rsub = t >> 3;
+    const char* xg = static_cast<const char*>(p.a_ptr);
+    const int64_t row_bytes = static_cast<int64_t>(p.K) * ES;
+    int s = 0;
+    uint32_t ph = 0;
+    int issued = 0, arrived = 0;
+    bool ok = true;
+    for (int tile = cluster; tile < total && ok; tile += nclusters) {
+      int e, n, prow0, prows;
+      decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, prow0, prows);
+      const int local = tile - prefix[e];
+      const int m_pairs = (prefix[e + 1] - prefix[e]) / p.n_tiles;
+      const int mp = local - (local / m_pairs) * m_pairs;
+      const int pair0 = __ldg(p.offsets + e) + mp * 2 * BM;
+      const int row0 = pair0 + static_cast<int>(rank) * BM;
+      const int rows = __ldg(p.offsets + e + 1) - row0;       // may be <= 0 for the odd CTA
+      const int tok0 = __ldg(p.permute_src + pair0) / p.k;    // a valid row for padding
+      const char* src[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = rsub + 16 * i;
+        const int tok = r < rows ? __ldg(p.permute_src + row0 + r) / p.k : tok0;
+        src[i] = xg + tok * row_bytes + chunk * 16;
+      }
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (lane == 0) ok = mbar_wait_cluster(&empty[s], ph ^ 1, ctl);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const uint32_t a_dst = smem_u32(sA + s * A_STAGE);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = rsub + 16 * i;
+          cp_async16(a_dst + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + kb * 128);
+        }
+        cp_async_commit();
+        ++issued;
+        if (issued - arrived == MC2_PAIR_GATHER_DEPTH) {
+          cp_async_wait<MC2_PAIR_GATHER_DEPTH - 1>();
+          fence_proxy_async_smem();
+          mbar_arrive(&full[arrived % P_STAGES]);
+          ++arrived;
+        }
+        if (++s == P_STAGES) { s = 0; ph ^= 1; }
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (; arrived < issued; ++arrived) mbar_arrive(&full[arrived % P_STAGES]);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    uint8_t* stage = sOut + q * OUT_STAGE;
+    const uint32_t row_off = static_cast<uint32_t>(lane) * 128;
+    const uint32_t leader_tempty = map_to_rank(tempty, 0);
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int tile = cluster; tile < total; tile += nclusters) {
+      int e, n, prow0, prows;
+      decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, prow0, prows);
+      const int local = tile - prefix[e];
+      const int m_pairs = (prefix[e + 1] - prefix[e]) / p.n_tiles;
+      const int mp = local - (local / m_pairs) * m_pairs;
+      const int row0 = __ldg(p.offsets + e) + mp * 2 * BM + static_cast<int>(rank) * BM;
+      const int rows = __ldg(p.offsets + e + 1) - row0;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait_cluster(&tfull[acc], aph, ctl);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16);
+      const int wrows = min(32, rows - q * 32);
+      const int grow0 = row0 + q * 32;
+      if (wrows > 0) {
+        constexpr int GROUP_COLS = 128 / (MODE == MODE_FC1 ? ES : 4);
+        constexpr int NGROUPS = (MODE == MODE_FC1 ? BN / 2 : BN) / GROUP_COLS;
+#pragma unroll 1
+        for (int gi = 0; gi < NGROUPS; ++gi) {
+          const int col0 = n * (MODE == MODE_FC1 ? BN / 2 : BN) + gi * GROUP_COLS;
+          if (col0 >= p.out_cols) break;
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+          if (MODE == MODE_FC1 && ES == 2) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              uint32_t g[32], u[32];
+              const int c = gi * 64 + half * 32;
+              tmem_ld32(tbase + c, g);
+              tmem_ld32(tbase + BN / 2 + c, u);
+              tmem_ld_wait();
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                pk[i] = pack_bf16x2(silu_f(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]),
+                                    silu_f(__uint_as_float(g[2 * i + 1])) *
+                                        __uint_as_float(u[2 * i + 1]));
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const int ch = half * 4 + v;
+                *reinterpret_cast<uint4*>(stage + row_off + ((ch ^ (lane & 7)) << 4)) =
+                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+              }
+            }
+          } else {
+            uint32_t v32[32];
+            if (MODE == MODE_FC1) {
+              uint32_t g[32];
+              tmem_ld32(tbase + gi * 32, g);
+              tmem_ld32(tbase + BN / 2 + gi * 32, v32);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                v32[i] = __float_as_uint(
+                    round_tf32(silu_f(__uint_as_float(g[i])) * __uint_as_float(v32[i])));
+            } else {
+              tmem_ld32(tbase + gi * 32, v32);
+              tmem_ld_wait();
+            }
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              *reinterpret_cast<uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4)) =
+                  make_uint4(v32[4 * v], v32[4 * v + 1], v32[4 * v + 2], v32[4 * v + 3]);
+          }
+          if (wrows == 32) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmOut, stage, col0, grow0);
+              bulk_commit();
+            }
+          } else if (lane < wrows) {
+            char* dst = static_cast<char*>(p.out) +
+                        (static_cast<int64_t>(grow0 + lane) * p.out_cols + col0) *
+                            (MODE == MODE_FC1 ? ES : 4);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              reinterpret_cast<uint4*>(dst)[v] =
+                  *reinterpret_cast<const uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4));
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(&tempty[acc]);
+        else mbar_arrive_remote_relaxed(leader_tempty + acc * 8);  // after tcgen05.wait::ld
+      }
+      acc ^= 1;
+      if (acc == 0) aph ^= 1;
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, P_TMEM_COLS);
 }
 
 // ----------------------------------------------------------------------------
@@ -643,13 +1046,110 @@ static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <int MODE, int ES>
+static cudaError_t launch_pair(const GemmArgs& g, cudaStream_t st) {
+  const mc2_shape_t& s = *g.s;
+  using TR = ElemTraits<ES>;
+  const CUtensorMapDataType dt =
+      ES == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const int64_t R = static_cast<int64_t>(s.T) * s.k;
+  CUtensorMap tA, tB, tOut;
+  GemmParams p;
+  p.a_ptr = g.a;
+  p.offsets = g.offsets;
+  p.permute_src = g.permute_src;
+  p.out = g.out;
+  p.dev_status = g.dev_status;
+  p.E = s.E;
+  p.k = s.k;
+  p.I = s.I;
+  p.wait_limit_ns = wait_limit_ns();
+  bool ok;
+  if (MODE == MODE_FC1) {
+    p.K = s.H;
+    p.n_tiles = (s.I + BN / 2 - 1) / (BN / 2);
+    p.out_cols = s.I;
+    ok = (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.H, 2ull * s.I, s.E, TR::BK, BN / 2)
+                       : encode_3d(&tB, dt, ES, g.b, 2ull * s.I, s.H, s.E, 128 / ES, TR::BK)) &&
+         encode_2d(&tOut, dt, ES, g.out, s.I, R, 128 / ES, 32);
+    tA = tB;  // unused: fc1's A rows are gathered with cp.async
+  } else {
+    p.K = s.I;
+    p.n_tiles = (s.H + BN - 1) / BN;
+    p.out_cols = s.H;
+    ok = encode_2d(&tA, dt, ES, g.a, s.I, R, 128 / ES, BM) &&
+         (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.I, s.H, s.E, TR::BK, BN / 2)
+                       : encode_3d(&tB, dt, ES, g.b, s.H, s.I, s.E, 128 / ES, TR::BK)) &&
+         encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.out, s.H, R, 32, 32);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  const size_t smem = P_SMEM_BYTES_FIXED + (s.E + 1) * sizeof(int32_t);
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(gmm_pair_kernel<MODE, ES>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(P_SMEM_BYTES_FIXED + 1025 * sizeof(int32_t)));
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(Roles<MODE>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // Persistent grid: exactly as many pairs as can be resident at once.  A
+  // pair needs two SMs of one GPC, so this can be fewer than SMs / 2; any
+  // cluster beyond it would run its whole tile list as a second wave.
+  static std::once_flag once_clusters;
+  static int max_clusters = 0;
+  std::call_once(once_clusters, [&] {
+    cfg.gridDim = dim3(num_sms() & ~1, 1, 1);
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, gmm_pair_kernel<MODE, ES>, &cfg) !=
+        cudaSuccess)
+      max_clusters = 0;
+  });
+  if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+  const int64_t pair_tiles_upper = (R / (2 * BM) + s.E) * static_cast<int64_t>(p.n_tiles);
+  const int grid = 2 * static_cast<int>(std::min<int64_t>(max_clusters,
+                                                          std::max<int64_t>(pair_tiles_upper, 1)));
+  cfg.gridDim = dim3(grid, 1, 1);
+  return cudaLaunchKernelEx(&cfg, gmm_pair_kernel<MODE, ES>, tA, tB, tOut, p);
+}
+
+// Automatic choice, from measurements on GB300 (4096- and 16384-token
+// workloads): CTA pairs win for fc2 when experts average >= 256 rows (fc2
+// 173 vs 185 us and 544 vs 593 us) and tie or lose for fc1 (205 vs 203 us,
+// 615 vs 600 us); with few rows per expert (decode-like batches) single CTAs
+// waste less tensor work on padding and are already bound by weight streaming.
+static bool use_pairs(const mc2_shape_t& s, int mode) {
+  const int forced = tile_pairing_override();
+  if (forced == 1) return false;
+  if (forced == 2) return num_sms() >= 2;
+  const int64_t R = static_cast<int64_t>(s.T) * s.k;
+  return mode == MODE_FC2 && num_sms() >= 2 && R >= 2 * BM * static_cast<int64_t>(s.E);
+}
+
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
   if (static_cast<int64_t>(g.s->T) * g.s->k == 0) return cudaSuccess;
   cudaError_t e;
-  if (g.mode == MODE_FC1)
-    e = g.a_elem_bytes == 2 ? launch_one<MODE_FC1, 2>(g, st) : launch_one<MODE_FC1, 4>(g, st);
-  else
-    e = g.a_elem_bytes == 2 ? launch_one<MODE_FC2, 2>(g, st) : launch_one<MODE_FC2, 4>(g, st);
+  const bool pairs = use_pairs(*g.s, g.mode);
+  if (g.mode == MODE_FC1) {
+    if (pairs)
+      e = g.a_elem_bytes == 2 ? launch_pair<MODE_FC1, 2>(g, st) : launch_pair<MODE_FC1, 4>(g, st);
+    else
+      e = g.a_elem_bytes == 2 ? launch_one<MODE_FC1, 2>(g, st) : launch_one<MODE_FC1, 4>(g, st);
+  } else {
+    if (pairs)
+      e = g.a_elem_bytes == 2 ? launch_pair<MODE_FC2, 2>(g, st) : launch_pair<MODE_FC2, 4>(g, st);
+    else
+      e = g.a_elem_bytes == 2 ? launch_one<MODE_FC2, 2>(g, st) : launch_one<MODE_FC2, 4>(g, st);
+  }
   note_launches(1);
   return e;
 }

@@ -37,6 +37,7 @@ struct WsLayout {
 WsLayout ws_layout(const mc2_shape_t& s);
 
 uint64_t wait_limit_ns();
+int tile_pairing_override();  // 0 auto, 1 single CTAs, 2 CTA pairs
 void note_launches(int n);
 void reset_launches();
 

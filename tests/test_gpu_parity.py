@@ -78,8 +78,17 @@ SMALL = [
 ]
 
 
+@pytest.fixture(params=[1, 2], ids=["single_cta", "cta_pairs"])
+def pairing(request):
+    """Force one grouped-GEMM tiling (single CTAs or CTA pairs) for the test."""
+    ensure_built()
+    B.mc2_set_tile_pairing(request.param)
+    yield request.param
+    B.mc2_set_tile_pairing(0)
+
+
 @pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
-def test_block_parity_full(wl):
+def test_block_parity_full(wl, pairing):
     inp, d, b = run_gpu(wl, seed=1)
     src, offsets = _counts_exact(wl, inp, b)
     x, w1, w2 = (as_f64(inp[n], wl.act) for n in ("x", "w1", "w2"))
@@ -113,8 +122,8 @@ def test_fc2_alone_on_oracle_h():
     _tol(to_np(b.out), ref["out"], "out from oracle h")
 
 
-def test_determinism_bitwise():
-    wl = SMALL[3]
+def test_determinism_bitwise(pairing):
+    wl = SMALL[1]
     _, _, b1 = run_gpu(wl, seed=4)
     _, _, b2 = run_gpu(wl, seed=4)
     assert torch.equal(b1.out.view(torch.int16), b2.out.view(torch.int16))
@@ -142,18 +151,18 @@ def _check_custom(wl, inp, expect_bad=False):
     assert not status & B.MC2_DEV_TIMEOUT
 
 
-def test_all_tokens_to_one_expert():
+def test_all_tokens_to_one_expert(pairing):
     wl = Workload("one_expert", 512, 256, 128, 8, 1, 2, "bf16")
     _check_custom(wl, _custom(wl, np.full((512, 1), 5)))
 
 
-def test_most_experts_empty():
+def test_most_experts_empty(pairing):
     wl = Workload("sparse", 300, 256, 128, 16, 2, 2, "bf16")
     sel = np.stack([np.full(300, 3), np.full(300, 12)], axis=1)
     _check_custom(wl, _custom(wl, sel))
 
 
-def test_invalid_ids_are_flagged_and_skipped():
+def test_invalid_ids_are_flagged_and_skipped(pairing):
     wl = Workload("bad_ids", 64, 256, 128, 8, 2, 2, "bf16")
     inp = make_inputs(wl, 6)
     sel = inp["sel"].copy()
