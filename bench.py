@@ -105,26 +105,41 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(wl, inp, budget_s=12.0):
-    """The oracle as it stands, on host cores, on the first T_s tokens of the
-    same workload (all experts' weights, same routing)."""
+def _oracle_sample(wl, inp):
+    """A callable running the oracle on tokens [a, a + n) of the workload."""
     from oracle import mc2_oracle as orc
+    if wl.act == "i8":
+        def run(a, n):
+            orc.quant_block_forward(inp["x"][a:a + n], inp["xs"][a:a + n], inp["w1"], inp["w1s"],
+                                    inp["w2"], inp["w2s"], inp["sel"][a:a + n],
+                                    inp["probs"][a:a + n], wl.E, wl.W)
+        return run
     x = as_f64(inp["x"], wl.act)
     w1 = as_f64(inp["w1"], wl.act)
     w2 = as_f64(inp["w2"], wl.act)
+
+    def run(a, n):
+        orc.block_forward(x[a:a + n], w1, w2, inp["sel"][a:a + n], inp["probs"][a:a + n],
+                          wl.E, wl.W, h_dtype=wl.act)
+    return run
+
+
+def cpu_baseline(wl, inp, budget_s=12.0):
+    """The oracle as it stands, on host cores, on the first T_s tokens of the
+    same workload (all experts' weights, same routing)."""
+    run = _oracle_sample(wl, inp)
     Ts, spent, done = 0, 0.0, 0
     step = max(wl.W, (256 // wl.W) * wl.W)
     while spent < budget_s and Ts < wl.T:
         n = min(step, wl.T - Ts)
         t0 = time.perf_counter()
-        orc.block_forward(x[Ts:Ts + n], w1, w2, inp["sel"][Ts:Ts + n], inp["probs"][Ts:Ts + n],
-                          wl.E, wl.W, h_dtype=wl.act)
+        run(Ts, n)
         spent += time.perf_counter() - t0
         Ts += n
         done += 1
     return {"value": Ts / spent, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"first {Ts} of {wl.T} tokens of the {wl.name} workload in {done} chunks of "
-                      f"{step} tokens (float64 numpy oracle, all experts), {spent:.1f} s"}
+                      f"{step} tokens (numpy oracle, float64 / int64, all experts), {spent:.1f} s"}
 
 
 def run_reference(args):
@@ -133,16 +148,11 @@ def run_reference(args):
         return
     wl = WORKLOADS[args.workload]
     inp = make_inputs(wl, 0)
-    from oracle import mc2_oracle as orc
-    x = as_f64(inp["x"], wl.act)
-    w1 = as_f64(inp["w1"], wl.act)
-    w2 = as_f64(inp["w2"], wl.act)
+    run = _oracle_sample(wl, inp)
     Ts = max(wl.W, (64 // wl.W) * wl.W)   # bounded sample of the workload per step
 
     def step(i):
-        a = (i * Ts) % wl.T
-        orc.block_forward(x[a:a + Ts], w1, w2, inp["sel"][a:a + Ts], inp["probs"][a:a + Ts],
-                          wl.E, wl.W, h_dtype=wl.act)
+        run((i * Ts) % wl.T, Ts)
     for i in range(args.warmup):
         step(i)
     t0 = time.perf_counter()
@@ -192,6 +202,13 @@ def run_cuda(args):
     b = blk.alloc_buffers(wl)
     shape = blk.shape_of(wl)
     stream = torch.cuda.current_stream()
+    # int8 path: expand the weights to bf16 once (load-time weight transform,
+    # outside the timed region; a no-op for the float paths)
+    torch.cuda.synchronize()
+    t_prepack = time.perf_counter()
+    blk.prepack(wl, d, b, stream=stream)
+    torch.cuda.synchronize()
+    t_prepack = time.perf_counter() - t_prepack
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")  # 256 MB > L2
 
     def step():
@@ -302,6 +319,10 @@ def run_cuda(args):
         "gpu_launches": launches,
         "clocks": clk,
     }
+    if wl.act == "i8":
+        line["weight_prepack_ms"] = t_prepack * 1e3
+        line["dtype"] = "int8 (exact, on bf16 tensor cores)"
+        line["roofline"]["peak_source"] += "; int8 runs at the bf16 rate (no integer tcgen05 MMA on sm_103a)"
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp)
     print(json.dumps(line), flush=True)

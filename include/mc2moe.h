@@ -171,6 +171,20 @@ mc2_status_t mc2_moe_counts_static(const mc2_shape_t* s, const int32_t* sel, int
                                    int32_t* unpermute_dst, int32_t* dev_status, void* stream);
 
 /*
+ * mc2_prepack_weights -- int8 path only (a no-op returning MC2_OK for other
+ * activation types): expands the int8 weights w1 [E, H, 2I] and w2 [E, I, H]
+ * into bf16 copies held in `ws`.  Every int8 value is exact in bf16; the
+ * int8 GEMMs run on the bf16 tensor cores (sm_103a has no integer tcgen05
+ * MMA) and read these copies, so call this once whenever the weights change
+ * and before any act=I8 mc2_alltoallv_gmm / mc2_gmm_alltoallv / mc2_moe_forward
+ * that uses this workspace.  w1/w2 passed to those calls must be the same
+ * tensors.  The int8 path requires H <= 4096 and I <= 4096 (K is summed in
+ * exact chunks of 1024 in at most four TMEM accumulators).
+ */
+mc2_status_t mc2_prepack_weights(const mc2_shape_t* s, const void* w1, const void* w2, void* ws,
+                                 void* stream);
+
+/*
  * mc2_moe_forward -- the whole block (the three calls above, in order) on
  * device buffers.  cnt/recv/offsets/permute_src/unpermute_dst/h/h_scale are
  * outputs as above (h_scale may be NULL unless act is I8); out is [T, H].

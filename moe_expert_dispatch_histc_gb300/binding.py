@@ -50,6 +50,7 @@ _SIGS = {
     "mc2_alltoallv_gmm": (ctypes.c_int, [_SP] + [_P] * 11),
     "mc2_gmm_alltoallv": (ctypes.c_int, [_SP] + [_P] * 12),
     "mc2_moe_forward": (ctypes.c_int, [_SP] + [_P] * 19),
+    "mc2_prepack_weights": (ctypes.c_int, [_SP] + [_P] * 4),
     "mc2_selftest_wait": (ctypes.c_int, [ctypes.c_uint64, _P, _P]),
     "mc2_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "mc2_set_tile_pairing": (None, [ctypes.c_int32]),
@@ -166,6 +167,13 @@ def mc2_moe_forward(shape, x, x_scale, sel, probs, w1, w1_scale, w2, w2_scale, c
                                _p(h_scale), _p(out), _p(ws), _p(dev_status), _stream(stream))
     if check:
         _check("mc2_moe_forward", st)
+    return st
+
+
+def mc2_prepack_weights(shape, w1, w2, ws, stream=None, check=True):
+    st = lib().mc2_prepack_weights(ctypes.byref(shape), _p(w1), _p(w2), _p(ws), _stream(stream))
+    if check:
+        _check("mc2_prepack_weights", st)
     return st
 
 

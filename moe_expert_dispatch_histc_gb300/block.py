@@ -62,7 +62,7 @@ def alloc_buffers(wl: Workload, device="cuda", out: str | None = None) -> BlockB
     if wl.act == "i8":
         h = torch.empty((R, 2 * wl.I) if out == "i32" else (R, wl.I),
                         dtype=torch.int32 if out == "i32" else torch.int8, device=device)
-        h_scale = torch.empty(R, dtype=torch.float32, device=device)
+        h_scale = None if out == "i32" else torch.empty(R, dtype=torch.float32, device=device)
         o = torch.empty((R, wl.H) if out == "i32" else (wl.T, wl.H),
                         dtype=torch.int32 if out == "i32" else torch.bfloat16, device=device)
     else:
@@ -82,6 +82,12 @@ def alloc_buffers(wl: Workload, device="cuda", out: str | None = None) -> BlockB
         ws=torch.empty(ws_bytes, dtype=torch.uint8, device=device),
         dev_status=torch.zeros(1, dtype=i32, device=device),
     )
+
+
+def prepack(wl: Workload, d: dict, b: BlockBuffers, stream=None, out: str | None = None):
+    """Once per weight set: the int8 path's bf16 weight copies in the workspace
+    (a no-op for the other activation types)."""
+    return B.mc2_prepack_weights(shape_of(wl, out), d["w1"], d["w2"], b.ws, stream=stream)
 
 
 def run_block(wl: Workload, d: dict, b: BlockBuffers, stream=None, out: str | None = None):

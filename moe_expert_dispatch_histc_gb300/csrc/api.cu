@@ -43,6 +43,13 @@ WsLayout ws_layout(const mc2_shape_t& s) {
     L.w1_t32 = take(static_cast<size_t>(s.E) * s.H * 2 * s.I * 4);
     L.w2_t32 = take(static_cast<size_t>(s.E) * s.I * s.H * 4);
   }
+  if (s.act == MC2_I8) {
+    L.x_b16 = take(static_cast<size_t>(s.T) * s.H * 2);
+    L.w1_b16 = take(static_cast<size_t>(s.E) * s.H * 2 * s.I * 2);
+    L.w2_b16 = take(static_cast<size_t>(s.E) * s.I * s.H * 2);
+    L.h_f32 = take(R * s.I * 4);
+    L.hq_b16 = take(R * s.I * 2);
+  }
   L.total = off > kWsAlign ? off : kWsAlign;  // never 0: 0 means "shape rejected"
   return L;
 }
@@ -60,6 +67,7 @@ bool shape_ok(const mc2_shape_t* s) {
   if (s->E % s->W || s->T % s->W) return false;
   const int64_t R = static_cast<int64_t>(s->T) * s->k;
   if (R >= (int64_t(1) << 31)) return false;
+  if (s->act == MC2_I8 && (s->H > 4096 || s->I > 4096)) return false;  // <= 4 exact K chunks
   const bool combo = (s->act == MC2_F32 && s->out == MC2_F32) ||
                      (s->act == MC2_BF16 && s->out == MC2_BF16) ||
                      (s->act == MC2_I8 && (s->out == MC2_BF16 || s->out == MC2_I32));
@@ -77,10 +85,81 @@ mc2_status_t do_counts(const mc2_shape_t* s, const int32_t* sel, int32_t* cnt, i
                                    static_cast<char*>(ws), dev_status, st));
 }
 
+mc2_status_t do_fc1_i8(const mc2_shape_t* s, const void* x, const float* x_scale,
+                       const float* w1_scale, const int32_t* offsets, const int32_t* permute_src,
+                       void* ws, void* h, float* h_scale, int32_t* dev_status, cudaStream_t st) {
+  const bool raw = s->out == MC2_I32;
+  if (!offsets || !ws) return MC2_ERR_INVALID_ARG;
+  if (raw ? (h_scale != nullptr) : (!x_scale || !w1_scale || !h_scale)) return MC2_ERR_INVALID_ARG;
+  if (s->T > 0 && (!x || !permute_src || !h)) return MC2_ERR_INVALID_ARG;
+  if (s->T == 0) return MC2_OK;
+  const WsLayout L = ws_layout(*s);
+  char* w = static_cast<char*>(ws);
+  if (launch_i8_to_bf16(static_cast<const int8_t*>(x), w + L.x_b16,
+                        static_cast<size_t>(s->T) * s->H, st) != cudaSuccess)
+    return MC2_ERR_CUDA;
+  QArgs q;
+  std::memset(&q, 0, sizeof(q));
+  q.s = s;
+  q.a = w + L.x_b16;
+  q.b = w + L.w1_b16;
+  q.offsets = offsets;
+  q.permute_src = permute_src;
+  q.a_scale = x_scale;
+  q.b_scale = w1_scale;
+  q.out = raw ? h : static_cast<void*>(w + L.h_f32);
+  q.dev_status = dev_status;
+  q.mode = 0;
+  q.raw = raw;
+  cudaError_t e = launch_gemm_q(q, st);
+  if (e == cudaSuccess && !raw)
+    e = launch_requant(reinterpret_cast<const float*>(w + L.h_f32), offsets, *s,
+                       static_cast<int8_t*>(h), h_scale, st);
+  return cuda_status(e);
+}
+
+mc2_status_t do_fc2_i8(const mc2_shape_t* s, const void* h, const float* h_scale,
+                       const float* w2_scale, const int32_t* offsets, const int32_t* permute_src,
+                       const int32_t* unpermute_dst, const float* probs, void* ws, void* out,
+                       int32_t* dev_status, cudaStream_t st) {
+  const bool raw = s->out == MC2_I32;
+  if (!offsets || !ws) return MC2_ERR_INVALID_ARG;
+  if (!raw && (!h_scale || !w2_scale)) return MC2_ERR_INVALID_ARG;
+  if (s->T > 0 && (!h || !permute_src || !out || (!raw && (!unpermute_dst || !probs))))
+    return MC2_ERR_INVALID_ARG;
+  if (s->T == 0) return MC2_OK;
+  const WsLayout L = ws_layout(*s);
+  char* w = static_cast<char*>(ws);
+  const size_t R = static_cast<size_t>(s->T) * s->k;
+  if (launch_i8_to_bf16(static_cast<const int8_t*>(h), w + L.hq_b16, R * s->I, st) != cudaSuccess)
+    return MC2_ERR_CUDA;
+  QArgs q;
+  std::memset(&q, 0, sizeof(q));
+  q.s = s;
+  q.a = w + L.hq_b16;
+  q.b = w + L.w2_b16;
+  q.offsets = offsets;
+  q.permute_src = permute_src;
+  q.a_scale = h_scale;
+  q.b_scale = w2_scale;
+  q.out = raw ? out : static_cast<void*>(w + L.y);
+  q.dev_status = dev_status;
+  q.mode = 1;
+  q.raw = raw;
+  cudaError_t e = launch_gemm_q(q, st);
+  if (e == cudaSuccess && !raw)
+    e = launch_combine(*s, reinterpret_cast<const float*>(w + L.y), probs, offsets, unpermute_dst,
+                       out, MC2_BF16, st);
+  return cuda_status(e);
+}
+
 mc2_status_t do_fc1(const mc2_shape_t* s, const void* x, const float* x_scale, const void* w1,
                     const float* w1_scale, const int32_t* offsets, const int32_t* permute_src,
                     void* ws, void* h, float* h_scale, int32_t* dev_status, cudaStream_t st) {
-  if (s->act == MC2_I8) return MC2_ERR_UNSUPPORTED;
+  if (s->act == MC2_I8) {
+    if (s->T > 0 && !w1) return MC2_ERR_INVALID_ARG;
+    return do_fc1_i8(s, x, x_scale, w1_scale, offsets, permute_src, ws, h, h_scale, dev_status, st);
+  }
   if (x_scale || w1_scale || h_scale) return MC2_ERR_INVALID_ARG;
   if (!offsets || !ws) return MC2_ERR_INVALID_ARG;
   if (s->T > 0 && (!x || !w1 || !permute_src || !h)) return MC2_ERR_INVALID_ARG;
@@ -118,7 +197,11 @@ mc2_status_t do_fc2(const mc2_shape_t* s, const void* h, const float* h_scale, c
                     const float* w2_scale, const int32_t* offsets, const int32_t* permute_src,
                     const int32_t* unpermute_dst, const float* probs, void* ws, void* out,
                     int32_t* dev_status, cudaStream_t st) {
-  if (s->act == MC2_I8) return MC2_ERR_UNSUPPORTED;
+  if (s->act == MC2_I8) {
+    if (s->T > 0 && !w2) return MC2_ERR_INVALID_ARG;
+    return do_fc2_i8(s, h, h_scale, w2_scale, offsets, permute_src, unpermute_dst, probs, ws, out,
+                     dev_status, st);
+  }
   if (h_scale || w2_scale) return MC2_ERR_INVALID_ARG;
   if (!offsets || !ws) return MC2_ERR_INVALID_ARG;
   if (s->T > 0 && (!h || !w2 || !permute_src || !unpermute_dst || !probs || !out))
@@ -214,6 +297,23 @@ mc2_status_t mc2_moe_forward(const mc2_shape_t* s, const void* x, const float* x
   if (r != MC2_OK) return r;
   return do_fc2(s, h, h_scale, w2, w2_scale, offsets, permute_src, unpermute_dst, probs, ws, out,
                 dev_status, st);
+}
+
+mc2_status_t mc2_prepack_weights(const mc2_shape_t* s, const void* w1, const void* w2, void* ws,
+                                 void* stream) {
+  tl_launches = 0;
+  if (!shape_ok(s)) return MC2_ERR_INVALID_ARG;
+  if (s->act != MC2_I8) return MC2_OK;
+  if (!w1 || !w2 || !ws) return MC2_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*s);
+  char* w = static_cast<char*>(ws);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_i8_to_bf16(static_cast<const int8_t*>(w1), w + L.w1_b16,
+                                    static_cast<size_t>(s->E) * s->H * 2 * s->I, st);
+  if (e == cudaSuccess)
+    e = launch_i8_to_bf16(static_cast<const int8_t*>(w2), w + L.w2_b16,
+                          static_cast<size_t>(s->E) * s->I * s->H, st);
+  return cuda_status(e);
 }
 
 mc2_status_t mc2_selftest_wait(uint64_t limit_ns, int32_t* dev_status, void* stream) {

@@ -29,102 +29,11 @@
 // Why a cp.async gather and not TMA tile::gather4: on GB300 the gather4
 // version of fc1 took 537 us on the 4096-token workload against 237 us for
 // this one (and 183 us when x is pre-permuted), with bit-identical h.
-#include <cuda.h>
-#include <cuda_runtime.h>
-#include <cudaTypedefs.h>
-#include <cuda_bf16.h>
-
 #include <algorithm>
 
-#include <mutex>
-
-#include "internal.h"
-#include "ptx.cuh"
+#include "gmm_common.cuh"
 
 namespace mc2 {
-
-enum { MODE_FC1 = 0, MODE_FC2 = 1 };
-
-constexpr int BM = 128;            // rows per tile (UMMA M)
-constexpr int BN = 256;            // accumulator columns per tile (UMMA N)
-constexpr int STAGES = 4;
-constexpr int A_STAGE = BM * 128;  // 128 rows x 128 bytes of K
-constexpr int B_STAGE = 32768;     // (128/es) K rows x 256 columns x es bytes
-constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-constexpr int TMEM_COLS = 512;
-
-// cp.async groups a gather thread keeps in flight before it signals the
-// oldest stage.  Stage g is signalled when stage g+depth-1 is issued, which
-// needs the MMA to have released stage g+depth-1-STAGES; the smaller the
-// depth, the earlier the signal relative to the MMA's need for stage g.
-#ifndef MC2_GATHER_DEPTH
-#define MC2_GATHER_DEPTH 2
-#endif
-#ifndef MC2_PAIR_GATHER_DEPTH
-#define MC2_PAIR_GATHER_DEPTH 3
-#endif
-
-struct GemmParams {
-  const void* a_ptr;            // fc1: x (rows gathered by the gather warps)
-  const int32_t* offsets;
-  const int32_t* permute_src;
-  void* out;                    // fc1: h [R, I]; fc2: y [R, H] fp32
-  int32_t* dev_status;
-  int E, k, K, n_tiles, out_cols, I;
-  uint64_t wait_limit_ns;
-};
-
-template <int ES>
-struct ElemTraits;
-template <>
-struct ElemTraits<2> {  // bf16, kind::f16; weights used as stored ([K, N], N contiguous)
-  static constexpr int BK = 64;
-  static constexpr int KIND = 0;
-  static constexpr uint32_t FMT = 1;
-  static constexpr bool B_KMAJOR = false;
-};
-template <>
-struct ElemTraits<4> {  // fp32 storage, kind::tf32; weights pre-transposed to [N, K]
-  static constexpr int BK = 32;
-  static constexpr int KIND = 1;
-  static constexpr uint32_t FMT = 2;
-  static constexpr bool B_KMAJOR = true;
-};
-
-__device__ __forceinline__ void decode_tile(int tile, const int32_t* prefix, int E, int n_tiles,
-                                            const int32_t* offsets, int& e, int& n, int& row0,
-                                            int& rows) {
-  int lo = 0, hi = E;  // prefix[lo] <= tile < prefix[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (prefix[mid] <= tile) lo = mid; else hi = mid;
-  }
-  e = lo;
-  const int local = tile - prefix[e];
-  const int m_tiles = (prefix[e + 1] - prefix[e]) / n_tiles;
-  n = local / m_tiles;
-  const int m = local - n * m_tiles;
-  const int off = __ldg(offsets + e);
-  row0 = off + m * BM;
-  const int end = __ldg(offsets + e + 1);
-  rows = min(BM, end - row0);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ float round_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return __uint_as_float(r);
-}
-
-// silu(g) = g / (1 + e^-g) with the fast exponential and division
-// (relative error of a few fp32 ulp, far below the bf16 rounding of h).
-// For g << 0, e^-g overflows to +inf and the quotient is -0.
-__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 template <int MODE>
 struct Roles {
@@ -132,7 +41,6 @@ struct Roles {
   static constexpr int kThreads = (6 + kGatherWarps) * 32;
 };
 
-constexpr int OUT_STAGE = 4096;  // per epilogue warp: 32 rows x 128 bytes
 constexpr size_t SMEM_BYTES_FIXED = 1024 + STAGES * STAGE_BYTES + 4 * OUT_STAGE + 256;
 
 template <int MODE, int ES>
@@ -947,46 +855,6 @@ __global__ void selftest_wait_kernel(uint64_t limit_ns, int32_t* dev_status) {
 // ----------------------------------------------------------------------------
 // host side
 // ----------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-static bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int es, const void* base,
-                      uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * es};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-static bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, int es, const void* base,
-                      uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {d0, d1, d2};
-  cuuint64_t strides[2] = {d0 * es, d0 * d1 * es};
-  cuuint32_t box[3] = {b0, b1, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int num_sms() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);

@@ -1,0 +1,523 @@
+// gmm_q.cu -- the int8 path of the block: the dequantised grouped matmuls of
+// "torch_npu.npu_mm_reduce_scatter_base" (Ascend op-plugin docs, "Function
+// description"): out = (x1_scale * x2_scale) * (x1 @ x2), per-token x1_scale,
+// per-channel x2_scale, no bias.
+//
+// sm_103a has no tcgen05 integer MMA (ptxas rejects .kind::i8 for it), so the
+// int8 products run exactly on the bf16 tensor cores: every int8 value is a
+// bf16 value, every product (|p| <= 127*127) is exact in the fp32
+// accumulator, and every partial sum stays exact while |sum| < 2^24.  K is
+// therefore cut into chunks of at most 1024 (1024 * 127^2 < 2^24), each chunk
+// accumulates into its own TMEM region, and the epilogue converts the chunk
+// sums to int32 and adds them: the result is the exact int32 product.
+//
+//   fc1: acc1 = x_q[tok] @ w1_q[e]; G = (xs[tok] * w1s[e, n]) * acc1;
+//        h = silu(G_gate) * G_up (fp32) -> requant_rows -> h_q (int8), hs
+//   fc2: acc2 = h_q @ w2_q[e];  y = (hs[p] * w2s[e, n]) * acc2 -> combine
+//
+// Tiles are 128 x 128 (fc1: 64 gate + 64 up columns), 6 stages of 32 KB, one
+// CTA per SM, the same warp roles as the bf16 kernel.  Operands are bf16
+// copies of the int8 tensors: weights expanded once by mc2_prepack_weights,
+// x and h_q per call.
+#include <algorithm>
+
+#include "gmm_common.cuh"
+
+namespace mc2 {
+
+constexpr int QBN = 128;                       // UMMA N
+constexpr int QSTAGES = 6;
+constexpr int QB_STAGE = 16384;                // 64 K rows x 128 columns x 2 B
+constexpr int QSTAGE_BYTES = A_STAGE + QB_STAGE;
+constexpr int QCHUNK_KB = 16;                  // k-blocks (of 64) per exact fp32 chunk: K 1024
+constexpr int QMAX_CHUNKS = 4;                 // K <= 4096
+constexpr int QGATHER_DEPTH = 3;
+constexpr size_t QSMEM_BYTES_FIXED = 1024 + QSTAGES * QSTAGE_BYTES + 4 * OUT_STAGE + 256;
+
+struct QParams {
+  const void* a_ptr;           // fc1: x as bf16 [T, H] (gathered)
+  const int32_t* offsets;
+  const int32_t* permute_src;
+  const float* a_scale;        // fc1: xs [T] (per token); fc2: hs [R] (per permuted row)
+  const float* b_scale;        // fc1: w1s [E, 2I]; fc2: w2s [E, H]
+  void* out;                   // raw: int32 acc; else fc1 h fp32 [R, I], fc2 y fp32 [R, H]
+  int32_t* dev_status;
+  int E, k, K, n_tiles, I, H, nchunk, raw;
+  uint64_t wait_limit_ns;
+};
+
+template <int MODE>
+struct QRoles {
+  static constexpr int kGatherWarps = MODE == MODE_FC1 ? 4 : 0;
+  static constexpr int kThreads = (6 + kGatherWarps) * 32;
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
+    gmm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmOut, const QParams p) {
+  constexpr int BK = 64;
+  constexpr int B_BLOCK = BK * 128;          // 64 K rows x 64 columns
+  constexpr int KK_B = 16 * 128;             // B bytes per UMMA K step
+  constexpr uint32_t IDESC = instr_desc(1, false, true, BM, QBN);
+  constexpr bool GATHER = MODE == MODE_FC1;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + QSTAGES * A_STAGE;
+  uint8_t* sOut = sB + QSTAGES * QB_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * OUT_STAGE);
+  uint64_t* empty = full + QSTAGES;
+  uint64_t* tfull = empty + QSTAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_sh = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
+  int32_t* prefix = reinterpret_cast<int32_t*>(tmem_base_sh + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+  const int nchunk = p.nchunk;
+  const int bufs = nchunk <= 2 ? 2 : 1;      // accumulator sets that fit in 512 columns
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < QSTAGES; ++s) {
+      mbar_init(&full[s], GATHER ? 1 + 32 * QRoles<MODE>::kGatherWarps : 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4 * 32);
+    }
+    mbar_init(mma_done, 1);
+    *abort_sh = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    if (!GATHER) tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (!p.raw) tma_prefetch_desc(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_base_sh, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 2) {
+    int run = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      int t = 0;
+      if (e < E) {
+        const int rows = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+        t = ((rows + BM - 1) / BM) * p.n_tiles;
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += y;
+      }
+      if (e < E) prefix[e + 1] = run + t;
+      run += __shfl_sync(0xffffffffu, t, 31);
+    }
+    if (lane == 0) prefix[0] = 0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_sh;
+  const int total = prefix[E];
+  WaitCtl ctl{abort_sh, p.wait_limit_ns, p.dev_status};
+  const int kblocks = p.K / BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int s = 0;
+    uint32_t ph = 0;
+    int n_arm = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int e, n, row0, rows;
+      decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, ctl);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], GATHER ? QB_STAGE : QSTAGE_BYTES);
+          uint8_t* b_dst = sB + s * QB_STAGE;
+          const int k0 = kb * BK;
+          if (!GATHER) tma_load_2d(sA + s * A_STAGE, &tmA, &full[s], k0, row0);
+          if (MODE == MODE_FC1) {  // 64 gate columns, then the 64 up columns
+            tma_load_3d(b_dst, &tmB, &full[s], n * 64, k0, e);
+            tma_load_3d(b_dst + B_BLOCK, &tmB, &full[s], p.I + n * 64, k0, e);
+          } else {
+            tma_load_3d(b_dst, &tmB, &full[s], n * QBN, k0, e);
+            tma_load_3d(b_dst + B_BLOCK, &tmB, &full[s], n * QBN + 64, k0, e);
+          }
+        }
+        __syncwarp();
+        ++n_arm;
+        if (++s == QSTAGES) { s = 0; ph ^= 1; }
+      }
+    }
+    if (lane == 0) {
+      volatile int never = 0;
+      WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
+      for (int st = 0; st < QSTAGES && st < n_arm; ++st) {
+        const int last = st + QSTAGES * ((n_arm - 1 - st) / QSTAGES);
+        mbar_wait(&full[st], (last / QSTAGES) & 1, drain);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int s = 0;
+    uint32_t ph = 0;
+    int acc = 0;
+    uint32_t aph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      if (lane == 0) ok = mbar_wait(&tempty[acc], aph ^ 1, ctl);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d0 = tmem_base + acc * 256;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (lane == 0) ok = mbar_wait(&full[s], ph, ctl);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a_base = smem_u32(sA + s * A_STAGE);
+          const uint32_t b_base = smem_u32(sB + s * QB_STAGE);
+          const int chunk = kb / QCHUNK_KB;
+          const bool first_of_chunk = (kb % QCHUNK_KB) == 0;
+          const uint32_t d = d0 + chunk * QBN;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bdesc = smem_desc_sw128(b_base + kk * KK_B, B_BLOCK, 1024);
+            umma<0>(d, adesc, bdesc, IDESC, (first_of_chunk && kk == 0) ? 0u : 1u);
+          }
+          umma_commit(&empty[s]);
+        }
+        __syncwarp();
+        if (++s == QSTAGES) { s = 0; ph ^= 1; }
+      }
+      if (!ok) break;
+      if (lane == 0) umma_commit(&tfull[acc]);
+      __syncwarp();
+      if (bufs == 2) acc ^= 1;
+      if (acc == 0) aph ^= 1;
+    }
+    if (lane == 0) {
+      umma_commit(mma_done);
+      volatile int never = 0;
+      WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
+      mbar_wait(mma_done, 0, drain);
+    }
+    __syncwarp();
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ fc1 row gather
+    const int t = threadIdx.x - 6 * 32;
+    const int chunk = t & 7, rsub = t >> 3;
+    const char* xg = static_cast<const char*>(p.a_ptr);
+    const int64_t row_bytes = static_cast<int64_t>(p.K) * 2;
+    int s = 0;
+    uint32_t ph = 0;
+    int issued = 0, arrived = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int e, n, row0, rows;
+      decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
+      const int tok0 = __ldg(p.permute_src + row0) / p.k;
+      const char* src[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = rsub + 16 * i;
+        const int tok = r < rows ? __ldg(p.permute_src + row0 + r) / p.k : tok0;
+        src[i] = xg + tok * row_bytes + chunk * 16;
+      }
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, ctl);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const uint32_t a_dst = smem_u32(sA + s * A_STAGE);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = rsub + 16 * i;
+          cp_async16(a_dst + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + kb * 128);
+        }
+        cp_async_commit();
+        ++issued;
+        if (issued - arrived == QGATHER_DEPTH) {
+          cp_async_wait<QGATHER_DEPTH - 1>();
+          fence_proxy_async_smem();
+          mbar_arrive(&full[arrived % QSTAGES]);
+          ++arrived;
+        }
+        if (++s == QSTAGES) { s = 0; ph ^= 1; }
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (; arrived < issued; ++arrived) mbar_arrive(&full[arrived % QSTAGES]);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    uint8_t* stage = sOut + q * OUT_STAGE;
+    const uint32_t row_off = static_cast<uint32_t>(lane) * 128;
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, n, row0, rows;
+      decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&tfull[acc], aph, ctl);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + acc * 256 + (static_cast<uint32_t>(q * 32) << 16);
+      const int wrows = min(32, rows - q * 32);
+      const int grow0 = row0 + q * 32;
+      const int grow = grow0 + lane;
+      const bool valid = lane < wrows;
+      if (wrows > 0) {
+        // per-row scale: fc1 the token's x scale, fc2 the row's h scale (the
+        // raw test mode has no scales: the pointers may be null there)
+        float rs = 0.f;
+        if (valid && !p.raw)
+          rs = MODE == MODE_FC1 ? __ldg(p.a_scale + __ldg(p.permute_src + grow) / p.k)
+                                : __ldg(p.a_scale + grow);
+        const float* cs = p.b_scale + static_cast<int64_t>(e) *
+                                          (MODE == MODE_FC1 ? 2 * p.I : p.H);
+        constexpr int NGROUPS = MODE == MODE_FC1 ? 2 : 4;   // 32-column groups
+#pragma unroll 1
+        for (int gi = 0; gi < NGROUPS; ++gi) {
+          if (MODE == MODE_FC2 && n * QBN + gi * 32 >= p.H) break;
+          // exact int32 sums over the K chunks of this group's columns
+          int32_t s0[32], s1[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) { s0[i] = 0; s1[i] = 0; }
+#pragma unroll 1
+          for (int c = 0; c < nchunk; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tbase + c * QBN + gi * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s0[i] += __float2int_rn(__uint_as_float(v[i]));
+            if (MODE == MODE_FC1) {
+              tmem_ld32(tbase + c * QBN + 64 + gi * 32, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) s1[i] += __float2int_rn(__uint_as_float(v[i]));
+            }
+          }
+          if (p.raw) {  // test mode: the int32 accumulators themselves
+            if (valid) {
+              int32_t* o = static_cast<int32_t*>(p.out);
+              if (MODE == MODE_FC1) {
+                int4* dg = reinterpret_cast<int4*>(o + static_cast<int64_t>(grow) * 2 * p.I + n * 64 + gi * 32);
+                int4* du = reinterpret_cast<int4*>(o + static_cast<int64_t>(grow) * 2 * p.I + p.I + n * 64 + gi * 32);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                  dg[v] = make_int4(s0[4 * v], s0[4 * v + 1], s0[4 * v + 2], s0[4 * v + 3]);
+                  du[v] = make_int4(s1[4 * v], s1[4 * v + 1], s1[4 * v + 2], s1[4 * v + 3]);
+                }
+              } else {
+                int4* d = reinterpret_cast<int4*>(o + static_cast<int64_t>(grow) * p.H + n * QBN + gi * 32);
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                  d[v] = make_int4(s0[4 * v], s0[4 * v + 1], s0[4 * v + 2], s0[4 * v + 3]);
+              }
+            }
+            continue;
+          }
+          // dequant: (row scale * column scale) * acc, in fp32
+          uint32_t outv[32];
+          if (MODE == MODE_FC1) {
+            const int cg = n * 64 + gi * 32;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float g = (rs * __ldg(cs + cg + i)) * static_cast<float>(s0[i]);
+              const float u = (rs * __ldg(cs + p.I + cg + i)) * static_cast<float>(s1[i]);
+              outv[i] = __float_as_uint(silu_f(g) * u);
+            }
+          } else {
+            const int cg = n * QBN + gi * 32;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              outv[i] = __float_as_uint((rs * __ldg(cs + cg + i)) * static_cast<float>(s0[i]));
+          }
+          const int out_cols = MODE == MODE_FC1 ? p.I : p.H;
+          const int col0 = MODE == MODE_FC1 ? n * 64 + gi * 32 : n * QBN + gi * 32;
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4)) =
+                make_uint4(outv[4 * v], outv[4 * v + 1], outv[4 * v + 2], outv[4 * v + 3]);
+          if (wrows == 32) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmOut, stage, col0, grow0);
+              bulk_commit();
+            }
+          } else if (valid) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) +
+                                                    static_cast<int64_t>(grow) * out_cols + col0);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = *reinterpret_cast<const float4*>(stage + row_off + ((v ^ (lane & 7)) << 4));
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (bufs == 2) acc ^= 1;
+      if (acc == 0) aph ^= 1;
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// int8 -> bf16 (exact), 16 values per thread step
+__global__ void i8_to_bf16_kernel(const int8_t* __restrict__ src, __nv_bfloat16* __restrict__ dst,
+                                  size_t n16) {
+  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (; i < n16; i += stride) {
+    const int4 v = __ldg(reinterpret_cast<const int4*>(src) + i);
+    const int8_t* b = reinterpret_cast<const int8_t*>(&v);
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      w[j] = pack_bf16x2(static_cast<float>(b[2 * j]), static_cast<float>(b[2 * j + 1]));
+    uint4* d = reinterpret_cast<uint4*>(dst) + 2 * i;
+    d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+// Symmetric per-row int8 re-quantisation of h (one warp per permuted row):
+// hs = max|h| / 127 (1 for an all-zero row), hq = rne(h / hs) clamped to
+// [-127, 127]; IEEE division, as a float32 program would do it.
+__global__ void requant_rows_kernel(const float* __restrict__ h, const int32_t* __restrict__ offsets,
+                                    int E, int I, int8_t* __restrict__ hq, float* __restrict__ hs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= __ldg(offsets + E)) return;
+  const float4* hr = reinterpret_cast<const float4*>(h + row * I);
+  float m = 0.f;
+  for (int c = lane; c < I / 4; c += 32) {
+    const float4 v = __ldg(hr + c);
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float scale = m > 0.f ? __fdiv_rn(m, 127.0f) : 1.0f;
+  if (lane == 0) hs[row] = scale;
+  char4* qr = reinterpret_cast<char4*>(hq + row * I);
+  for (int c = lane; c < I / 4; c += 32) {
+    const float4 v = __ldg(hr + c);
+    auto q = [&](float x) {
+      const float r = rintf(__fdiv_rn(x, scale));
+      return static_cast<signed char>(fminf(fmaxf(r, -127.f), 127.f));
+    };
+    qr[c] = make_char4(q(v.x), q(v.y), q(v.z), q(v.w));
+  }
+}
+
+cudaError_t launch_i8_to_bf16(const int8_t* src, void* dst, size_t n, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const size_t n16 = n / 16;  // every int8 tensor of the block has a multiple of 64 elements
+  const int threads = 256;
+  const unsigned blocks =
+      static_cast<unsigned>(std::min<size_t>((n16 + threads - 1) / threads, 152 * 32));
+  i8_to_bf16_kernel<<<blocks, threads, 0, st>>>(src, static_cast<__nv_bfloat16*>(dst), n16);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_requant(const float* h, const int32_t* offsets, const mc2_shape_t& s, int8_t* hq,
+                           float* hs, cudaStream_t st) {
+  const int64_t R = static_cast<int64_t>(s.T) * s.k;
+  if (R == 0) return cudaSuccess;
+  const int warps = 8;
+  requant_rows_kernel<<<static_cast<unsigned>((R + warps - 1) / warps), warps * 32, 0, st>>>(
+      h, offsets, s.E, s.I, hq, hs);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+static cudaError_t launch_q(const QArgs& g, cudaStream_t st) {
+  const mc2_shape_t& s = *g.s;
+  const int64_t R = static_cast<int64_t>(s.T) * s.k;
+  CUtensorMap tA, tB, tOut;
+  QParams p;
+  p.a_ptr = g.a;
+  p.offsets = g.offsets;
+  p.permute_src = g.permute_src;
+  p.a_scale = g.a_scale;
+  p.b_scale = g.b_scale;
+  p.out = g.out;
+  p.dev_status = g.dev_status;
+  p.E = s.E;
+  p.k = s.k;
+  p.I = s.I;
+  p.H = s.H;
+  p.raw = g.raw ? 1 : 0;
+  p.wait_limit_ns = wait_limit_ns();
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  bool ok;
+  if (MODE == MODE_FC1) {
+    p.K = s.H;
+    p.n_tiles = s.I / 64;
+    ok = encode_3d(&tB, bf, 2, g.b, 2ull * s.I, s.H, s.E, 64, 64);
+    tA = tB;  // unused: fc1's A rows are gathered with cp.async
+    tOut = tB;
+    if (!g.raw) ok = ok && encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.out, s.I, R, 32, 32);
+  } else {
+    p.K = s.I;
+    p.n_tiles = (s.H + QBN - 1) / QBN;  // H is a multiple of 64: the last tile may be half full
+    ok = encode_2d(&tA, bf, 2, g.a, s.I, R, 64, BM) &&
+         encode_3d(&tB, bf, 2, g.b, s.H, s.I, s.E, 64, 64);
+    tOut = tB;
+    if (!g.raw) ok = ok && encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.out, s.H, R, 32, 32);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  p.nchunk = (p.K / 64 + QCHUNK_KB - 1) / QCHUNK_KB;
+  if (p.nchunk > QMAX_CHUNKS) return cudaErrorInvalidValue;
+  const size_t smem = QSMEM_BYTES_FIXED + (s.E + 1) * sizeof(int32_t);
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(gmm_q_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(QSMEM_BYTES_FIXED + 1025 * sizeof(int32_t)));
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int64_t tiles_upper = (R / BM + s.E) * static_cast<int64_t>(p.n_tiles);
+  const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_upper, 1)));
+  gmm_q_kernel<MODE><<<grid, QRoles<MODE>::kThreads, smem, st>>>(tA, tB, tOut, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_q(const QArgs& g, cudaStream_t st) {
+  if (static_cast<int64_t>(g.s->T) * g.s->k == 0) return cudaSuccess;
+  const cudaError_t e = g.mode == MODE_FC1 ? launch_q<MODE_FC1>(g, st) : launch_q<MODE_FC2>(g, st);
+  note_launches(1);
+  return e;
+}
+
+}  // namespace mc2

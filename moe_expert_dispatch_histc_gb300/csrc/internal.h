@@ -63,6 +63,25 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st);
 
+// int8 path (bf16 tensor cores holding int8 values, exact int32 sums)
+struct QArgs {
+  const mc2_shape_t* s;
+  const void* a;            // fc1: x as bf16 [T, H]; fc2: h_q as bf16 [R, I]
+  const void* b;            // bf16 copy of w1 [E, H, 2I] or w2 [E, I, H]
+  const int32_t* offsets;
+  const int32_t* permute_src;
+  const float* a_scale;     // fc1: x scale [T]; fc2: h scale [R]
+  const float* b_scale;     // fc1: w1 scale [E, 2I]; fc2: w2 scale [E, H]
+  void* out;                // raw: int32 accumulators; else fc1 h fp32 [R, I], fc2 y fp32 [R, H]
+  int32_t* dev_status;
+  int mode;                 // 0 fc1, 1 fc2
+  bool raw;
+};
+cudaError_t launch_gemm_q(const QArgs& g, cudaStream_t st);
+cudaError_t launch_i8_to_bf16(const int8_t* src, void* dst, size_t n, cudaStream_t st);
+cudaError_t launch_requant(const float* h, const int32_t* offsets, const mc2_shape_t& s, int8_t* hq,
+                           float* hs, cudaStream_t st);
+
 cudaError_t launch_combine(const mc2_shape_t& s, const float* y, const float* probs,
                            const int32_t* offsets, const int32_t* unpermute_dst, void* out,
                            int out_dtype, cudaStream_t st);

@@ -45,6 +45,7 @@ def run_gpu(wl, seed=0, inputs=None, segments=False, out=None):
     inp = make_inputs(wl, seed) if inputs is None else inputs
     d = blk.inputs_to_device(inp, wl)
     b = blk.alloc_buffers(wl, out=out)
+    blk.prepack(wl, d, b, out=out)
     if segments:
         blk.run_segments(wl, d, b, out=out)
     else:

@@ -88,6 +88,20 @@ def test_null_pointers_are_rejected_before_any_launch():
     assert B.mc2_selftest_wait(1000, None, stream=0, check=False) == B.MC2_ERR_INVALID_ARG
 
 
+def test_prepack_is_a_noop_for_float_paths_and_checks_int8_args():
+    fake = 1 << 40
+    assert B.mc2_prepack_weights(_shape(), None, None, None, stream=0, check=False) == B.MC2_OK
+    s8 = _shape(act="i8")
+    assert B.mc2_prepack_weights(s8, fake, None, fake, stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+    assert B.mc2_check_shape(_shape(act="i8", H=4160)) == B.MC2_ERR_INVALID_ARG   # K > 4096
+    # int8 dequant mode needs every scale; the raw int32 test mode takes none for h
+    assert B.mc2_alltoallv_gmm(s8, fake, None, fake, fake, fake, fake, fake, fake, fake,
+                               stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+    s8raw = _shape(act="i8", out="i32")
+    assert B.mc2_alltoallv_gmm(s8raw, fake, None, fake, None, fake, fake, fake, fake, fake,
+                               stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+
+
 def test_status_strings():
     for st in range(6):
         assert B.status_str(st)

@@ -1,0 +1,123 @@
+"""Parity of the int8 path with the oracle (int64 accumulators, float64
+dequant), through the C ABI.
+
+The int8 products run on bf16 tensor cores with K summed in exact chunks, so
+the int32 accumulators must equal the oracle's exactly.  The per-row
+re-quantisation decides integers from floats; both sides decide in float32,
+so codes may differ only where h / hs lands within a few fp32 ulp of a .5 tie
+(the GPU's silu uses the fast exponential): at most 1 code, on a tiny fraction
+of elements.  fc2 is therefore checked exactly on the GPU's own h_q.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import mc2_oracle as orc
+from moe_expert_dispatch_histc_gb300 import binding as B
+from moe_expert_dispatch_histc_gb300 import block as blk
+from moe_expert_dispatch_histc_gb300.workloads import WORKLOADS, Workload, make_inputs
+
+from gpu_util import ensure_built, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(wl, inp, out):
+    ensure_built()
+    d = blk.inputs_to_device(inp, wl)
+    b = blk.alloc_buffers(wl, out=out)
+    blk.prepack(wl, d, b, out=out)
+    blk.run_segments(wl, d, b, out=out)
+    torch.cuda.synchronize()
+    return d, b
+
+
+SMALL_I8 = [
+    Workload("i8_small", 256, 256, 128, 8, 2, 2, "i8"),
+    Workload("i8_chunk_edge", 128, 2112, 192, 4, 2, 2, "i8"),    # K = 33 k-blocks: chunks 16+16+1
+    Workload("i8_k3072", 64, 3072, 1536, 4, 2, 2, "i8"),         # three full chunks, two in fc2
+]
+
+
+@pytest.mark.parametrize("wl", SMALL_I8, ids=lambda w: w.name)
+def test_int8_fc1_accumulators_exact(wl):
+    inp = make_inputs(wl, 7)
+    d, b = _run(wl, inp, out="i32")
+    ref = orc.quant_block_forward(inp["x"], inp["xs"], inp["w1"], inp["w1s"], inp["w2"],
+                                  inp["w2s"], inp["sel"], inp["probs"], wl.E, wl.W)
+    n = int(ref["offsets"][-1])
+    assert np.array_equal(to_np(b.h)[:n].astype(np.int64), ref["acc1"])
+    assert int(b.dev_status.item()) == 0
+
+
+def test_int8_worst_case_magnitudes_exact():
+    """All values +-127 at K = 3072: |acc| = 49.5M > 2^24, exact only by chunking."""
+    wl = Workload("i8_worst", 64, 3072, 128, 2, 1, 1, "i8")
+    inp = make_inputs(wl, 0)
+    inp["x"] = np.full_like(inp["x"], 127)
+    inp["x"][1::2] = -127
+    inp["w1"] = np.full_like(inp["w1"], -127)
+    inp["w1"][:, :, 1::3] = 127
+    d, b = _run(wl, inp, out="i32")
+    ref = orc.quant_block_forward(inp["x"], inp["xs"], inp["w1"], inp["w1s"], inp["w2"],
+                                  inp["w2s"], inp["sel"], inp["probs"], wl.E, wl.W)
+    assert np.abs(ref["acc1"]).max() == 3072 * 127 * 127
+    assert np.array_equal(to_np(b.h).astype(np.int64), ref["acc1"])
+
+
+@pytest.mark.parametrize("wl", SMALL_I8, ids=lambda w: w.name)
+def test_int8_block_parity(wl):
+    inp = make_inputs(wl, 8)
+    d, b = _run(wl, inp, out="bf16")
+    hq = to_np(b.h)
+    hs = to_np(b.h_scale)
+    ref = orc.quant_block_forward(inp["x"], inp["xs"], inp["w1"], inp["w1s"], inp["w2"],
+                                  inp["w2s"], inp["sel"], inp["probs"], wl.E, wl.W)
+    n = int(ref["offsets"][-1])
+    # re-quantisation: scales agree to fp32 rounding, codes to +-1 at ties
+    assert np.allclose(hs[:n], ref["hs"], rtol=1e-5, atol=0)
+    diff = np.abs(hq[:n].astype(int) - ref["hq"].astype(int))
+    assert diff.max() <= 1 and (diff > 0).mean() < 1e-3
+    # fc2 exactly on the GPU's own h_q
+    wl_raw = wl
+    shape_raw = blk.shape_of(wl_raw, "i32")
+    acc2 = torch.empty((wl.R, wl.H), dtype=torch.int32, device="cuda")
+    B.mc2_gmm_alltoallv(shape_raw, b.h, None, d["w2"], None, b.offsets, b.permute_src, None, None,
+                        b.ws, acc2, b.dev_status)
+    torch.cuda.synchronize()
+    ref2 = orc.quant_block_forward(inp["x"], inp["xs"], inp["w1"], inp["w1s"], inp["w2"],
+                                   inp["w2s"], inp["sel"], inp["probs"], wl.E, wl.W,
+                                   hq_override=(hq[:n], hs[:n]))
+    assert np.array_equal(to_np(acc2)[:n].astype(np.int64), ref2["acc2"])
+    # the block output (bf16) within the block's tolerance of the float64 oracle
+    ok, a, m = orc.bf16_tolerance_ok(to_np(b.out), ref["out"])
+    assert ok, f"out: max {a:.3e}, mean {m:.3e}"
+    assert int(b.dev_status.item()) == 0
+
+
+def _token_ref(inp, t, k, E):
+    """int8 block for one token, by the oracle's own pieces, int64 exact."""
+    out = np.zeros(inp["w2"].shape[2])
+    for j in range(k):
+        e = int(inp["sel"][t, j])
+        acc1 = inp["x"][t].astype(np.int64) @ inp["w1"][e].astype(np.int64)
+        g = (np.float64(inp["xs"][t]) * inp["w1s"][e].astype(np.float64)) * acc1
+        h = orc.swiglu(g[None, :])
+        hq, hs = orc.requant_rows(h)
+        acc2 = hq.astype(np.int64) @ inp["w2"][e].astype(np.int64)
+        y = (np.float64(hs[0]) * inp["w2s"][e].astype(np.float64)) * acc2[0]
+        out += float(inp["probs"][t, j]) * y
+    return out
+
+
+def test_int8_full_size_sampled():
+    wl = WORKLOADS["int8"]
+    inp = make_inputs(wl, 0)
+    d, b = _run(wl, inp, out="bf16")
+    out = to_np(b.out)
+    rng = np.random.default_rng(5)
+    toks = rng.choice(wl.T, 12, replace=False)
+    ref = np.stack([_token_ref(inp, int(t), wl.k, wl.E) for t in toks])
+    ok, a, m = orc.bf16_tolerance_ok(out[toks], ref)
+    assert ok, f"int8 sampled out: max {a:.3e}, mean {m:.3e}"
+    assert int(b.dev_status.item()) == 0
