@@ -37,7 +37,8 @@ WsLayout ws_layout(const mc2_shape_t& s) {
   };
   L.hist = take(static_cast<size_t>(g.EB) * g.G * 4);
   L.base = take(static_cast<size_t>(g.EB) * g.G * 4);
-  L.y = take(R * s.H * 4);
+  L.y = take(R * s.H * 2);
+  L.yscale = take(R * (s.H / 64) * 4);
   if (s.act == MC2_F32) {
     L.x_t32 = take(static_cast<size_t>(s.T) * s.H * 4);
     L.w1_t32 = take(static_cast<size_t>(s.E) * s.H * 2 * s.I * 4);
@@ -143,13 +144,14 @@ mc2_status_t do_fc2_i8(const mc2_shape_t* s, const void* h, const float* h_scale
   q.a_scale = h_scale;
   q.b_scale = w2_scale;
   q.out = raw ? out : static_cast<void*>(w + L.y);
+  q.yscale = reinterpret_cast<float*>(w + L.yscale);
   q.dev_status = dev_status;
   q.mode = 1;
   q.raw = raw;
   cudaError_t e = launch_gemm_q(q, st);
   if (e == cudaSuccess && !raw)
-    e = launch_combine(*s, reinterpret_cast<const float*>(w + L.y), probs, offsets, unpermute_dst,
-                       out, MC2_BF16, st);
+    e = launch_combine(*s, w + L.y, reinterpret_cast<const float*>(w + L.yscale), probs, offsets,
+                       unpermute_dst, out, MC2_BF16, st);
   return cuda_status(e);
 }
 
@@ -209,7 +211,8 @@ mc2_status_t do_fc2(const mc2_shape_t* s, const void* h, const float* h_scale, c
   if (s->T == 0) return MC2_OK;
   const WsLayout L = ws_layout(*s);
   char* w = static_cast<char*>(ws);
-  float* y = reinterpret_cast<float*>(w + L.y);
+  void* y = w + L.y;
+  float* yscale = reinterpret_cast<float*>(w + L.yscale);
   GemmArgs g;
   std::memset(&g, 0, sizeof(g));
   g.s = s;
@@ -217,6 +220,7 @@ mc2_status_t do_fc2(const mc2_shape_t* s, const void* h, const float* h_scale, c
   g.offsets = offsets;
   g.permute_src = permute_src;
   g.out = y;
+  g.yscale = yscale;
   g.dev_status = dev_status;
   g.mode = 1;
   if (s->act == MC2_F32) {
@@ -232,7 +236,8 @@ mc2_status_t do_fc2(const mc2_shape_t* s, const void* h, const float* h_scale, c
     g.a_elem_bytes = 2;
   }
   cudaError_t e = launch_gemm(g, st);
-  if (e == cudaSuccess) e = launch_combine(*s, y, probs, offsets, unpermute_dst, out, s->out, st);
+  if (e == cudaSuccess)
+    e = launch_combine(*s, y, yscale, probs, offsets, unpermute_dst, out, s->out, st);
   return cuda_status(e);
 }
 

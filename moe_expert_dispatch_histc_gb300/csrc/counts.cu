@@ -8,10 +8,10 @@
 //                     bins (bin E = invalid id) and writes it to
 //                     hist[bin * G + warp]  (bin-major, so the scan order
 //                     (bin asc, warp asc) equals (expert asc, flat index asc)).
-//   2. scan_counts:   one CTA: per-rank counts cnt[W, E] and recv counts from
-//                     hist, then an exclusive scan of hist in that order ->
+//   2. scan_counts:   one CTA: an exclusive scan of hist in that order ->
 //                     base[bin * G + warp] = first permuted row of the warp's
-//                     entries of that bin; offsets[e] = base[e * G].
+//                     entries of that bin; offsets[e] = base[e * G]; per-rank
+//                     counts cnt[W, E] and recv counts as differences of bases.
 //   3. scatter_warps: each warp re-walks its sub-chunk 32 entries at a time;
 //                     lanes with equal bins are ranked by __match_any_sync and
 //                     a lane-mask popcount, giving a stable position.
@@ -110,24 +110,14 @@ __device__ int64_t block_exclusive_scan(int64_t v, int64_t* warp_sums, int64_t& 
 
 __global__ void __launch_bounds__(1024) scan_counts(CountsParams p) {
   __shared__ int64_t warp_sums[32];
-  const int El = p.E / p.W;
-  // per-rank histograms (the all_gather result) and recv counts
-  for (int idx = threadIdx.x; idx < p.W * p.E; idx += blockDim.x) {
-    const int r = idx / p.E, e = idx % p.E;
-    int32_t c = 0;
-    const int32_t* h = p.hist + static_cast<int64_t>(e) * p.G + static_cast<int64_t>(r) * p.CPR;
-    for (int64_t j = 0; j < p.CPR; ++j) c += h[j];
-    p.cnt[idx] = c;
-    // recv_counts of rank d = e / El: position (source r, local expert e % El)
-    const int d = e / El, le = e % El;
-    p.recv[static_cast<int64_t>(d) * p.W * El + r * El + le] = c;
-  }
-  // exclusive scan of hist in (bin, warp) order
+  // exclusive scan of hist in (bin, warp) order; each thread scans a
+  // contiguous segment, loading it with independent (unrolled) loads
   const int64_t N = static_cast<int64_t>(p.EB) * p.G;
   const int64_t seg = (N + blockDim.x - 1) / blockDim.x;
   const int64_t lo = threadIdx.x * seg;
   const int64_t hi = lo + seg < N ? lo + seg : N;
   int64_t own = 0;
+#pragma unroll 8
   for (int64_t i = lo; i < hi; ++i) own += p.hist[i];
   int64_t total;
   int64_t run = block_exclusive_scan(own, warp_sums, total);
@@ -139,6 +129,20 @@ __global__ void __launch_bounds__(1024) scan_counts(CountsParams p) {
   __syncthreads();
   for (int e = threadIdx.x; e <= p.E; e += blockDim.x)
     p.offsets[e] = (p.G > 0) ? p.base[static_cast<int64_t>(e) * p.G] : 0;
+  // per-rank histograms (the all_gather result) and recv counts: rank r's
+  // warps are G-positions [r*CPR, (r+1)*CPR) of each bin, so its count of
+  // expert e is the difference of two scan bases (the position after the
+  // last warp of bin e is the first warp of bin e+1)
+  const int El = p.E / p.W;
+  for (int idx = threadIdx.x; idx < p.W * p.E; idx += blockDim.x) {
+    const int r = idx / p.E, e = idx % p.E;
+    const int64_t b0 = static_cast<int64_t>(e) * p.G + static_cast<int64_t>(r) * p.CPR;
+    const int32_t c = (p.G > 0) ? p.base[b0 + p.CPR] - p.base[b0] : 0;
+    p.cnt[idx] = c;
+    // recv_counts of rank d = e / El: position (source r, local expert e % El)
+    const int d = e / El, le = e % El;
+    p.recv[static_cast<int64_t>(d) * p.W * El + r * El + le] = c;
+  }
 }
 
 __global__ void __launch_bounds__(kCountsWarpsPerBlock * 32)

@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       const int wrows = min(32, rows - q * 32);       // valid rows of this warp
       const int grow0 = row0 + q * 32;                 // first global row of this warp
       if (wrows > 0) {
-        constexpr int GROUP_COLS = 128 / (MODE == MODE_FC1 ? ES : 4);  // output cols per 128 B
+        constexpr int GROUP_COLS = 128 / (MODE == MODE_FC1 ? ES : 2);  // output cols per 128 B
         constexpr int NGROUPS = (MODE == MODE_FC1 ? BN / 2 : BN) / GROUP_COLS;
 #pragma unroll 1
         for (int gi = 0; gi < NGROUPS; ++gi) {
@@ -331,6 +331,18 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
                     make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
               }
             }
+          } else if (MODE == MODE_FC2) {  // y as fp16 with a power-of-two scale per 64 columns
+            uint32_t a[32], b2[32], pk[32];
+            tmem_ld32(tbase + gi * 64, a);
+            tmem_ld32(tbase + gi * 64 + 32, b2);
+            tmem_ld_wait();
+            const float inv = pack_y16(a, b2, pk);
+            if (lane < wrows)
+              p.yscale[static_cast<int64_t>(grow0 + lane) * (p.out_cols / 64) + col0 / 64] = inv;
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              *reinterpret_cast<uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4)) =
+                  make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           } else {
             uint32_t v32[32];
             if (MODE == MODE_FC1) {  // fp32 h, tf32-rounded for the fc2 tensor-core pass
@@ -361,7 +373,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           } else if (lane < wrows) {  // tail rows: plain stores of this lane's row
             char* dst = static_cast<char*>(p.out) +
                         (static_cast<int64_t>(grow0 + lane) * p.out_cols + col0) *
-                            (MODE == MODE_FC1 ? ES : 4);
+                            (MODE == MODE_FC1 ? ES : 2);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               reinterpret_cast<uint4*>(dst)[v] =
@@ -689,7 +701,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       const int wrows = min(32, rows - q * 32);
       const int grow0 = row0 + q * 32;
       if (wrows > 0) {
-        constexpr int GROUP_COLS = 128 / (MODE == MODE_FC1 ? ES : 4);
+        constexpr int GROUP_COLS = 128 / (MODE == MODE_FC1 ? ES : 2);
         constexpr int NGROUPS = (MODE == MODE_FC1 ? BN / 2 : BN) / GROUP_COLS;
 #pragma unroll 1
         for (int gi = 0; gi < NGROUPS; ++gi) {
@@ -718,6 +730,18 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
                     make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
               }
             }
+          } else if (MODE == MODE_FC2) {  // y as fp16 with a power-of-two scale per 64 columns
+            uint32_t a[32], b2[32], pk[32];
+            tmem_ld32(tbase + gi * 64, a);
+            tmem_ld32(tbase + gi * 64 + 32, b2);
+            tmem_ld_wait();
+            const float inv = pack_y16(a, b2, pk);
+            if (lane < wrows)
+              p.yscale[static_cast<int64_t>(grow0 + lane) * (p.out_cols / 64) + col0 / 64] = inv;
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              *reinterpret_cast<uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4)) =
+                  make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           } else {
             uint32_t v32[32];
             if (MODE == MODE_FC1) {
@@ -748,7 +772,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           } else if (lane < wrows) {
             char* dst = static_cast<char*>(p.out) +
                         (static_cast<int64_t>(grow0 + lane) * p.out_cols + col0) *
-                            (MODE == MODE_FC1 ? ES : 4);
+                            (MODE == MODE_FC1 ? ES : 2);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               reinterpret_cast<uint4*>(dst)[v] =
@@ -777,11 +801,13 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
 }
 
 // ----------------------------------------------------------------------------
-// combine (unpermute with probs): out[t, :] = sum_j probs[t, j] * y[unpermute_dst[t*k + j], :]
-// over valid pairs, products rounded to fp32 and summed in ascending j.
+// combine (unpermute with probs): out[t, :] = sum_j probs[t, j] * y(t, j) over
+// valid pairs, y(t, j) the fc2 row unpermute_dst[t*k + j] decoded from fp16
+// times its exact power-of-two factor; products rounded to fp32 and summed in
+// ascending j, so the result is bitwise reproducible.
 // ----------------------------------------------------------------------------
-__global__ void combine_kernel(const float* __restrict__ y, const float* __restrict__ probs,
-                               const int32_t* __restrict__ offsets,
+__global__ void combine_kernel(const __half* __restrict__ y, const float* __restrict__ yscale,
+                               const float* __restrict__ probs, const int32_t* __restrict__ offsets,
                                const int32_t* __restrict__ unpermute_dst, void* __restrict__ out,
                                int64_t T, int H, int k, int E, int out_bf16) {
   const int64_t H4 = H / 4;
@@ -796,11 +822,14 @@ __global__ void combine_kernel(const float* __restrict__ y, const float* __restr
     const int32_t row = __ldg(unpermute_dst + flat);
     if (row >= nvalid) continue;
     const float pj = __ldg(probs + flat);
-    const float4 v = __ldg(reinterpret_cast<const float4*>(y + static_cast<int64_t>(row) * H + c));
-    acc.x += __fmul_rn(pj, v.x);
-    acc.y += __fmul_rn(pj, v.y);
-    acc.z += __fmul_rn(pj, v.z);
-    acc.w += __fmul_rn(pj, v.w);
+    const float f = __ldg(yscale + static_cast<int64_t>(row) * (H / 64) + c / 64);
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(y + static_cast<int64_t>(row) * H + c));
+    const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    acc.x += __fmul_rn(pj, v01.x * f);
+    acc.y += __fmul_rn(pj, v01.y * f);
+    acc.z += __fmul_rn(pj, v23.x * f);
+    acc.w += __fmul_rn(pj, v23.y * f);
   }
   if (out_bf16) {
     uint2 w;
@@ -872,6 +901,7 @@ static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
   CUtensorMap tA, tB, tOut;
   GemmParams p;
   p.a_ptr = g.a;
+  p.yscale = g.yscale;
   p.offsets = g.offsets;
   p.permute_src = g.permute_src;
   p.out = g.out;
@@ -896,7 +926,7 @@ static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
     ok = encode_2d(&tA, dt, ES, g.a, s.I, R, 128 / ES, BM) &&
          (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.I, s.H, s.E, TR::BK, BN)
                        : encode_3d(&tB, dt, ES, g.b, s.H, s.I, s.E, 128 / ES, TR::BK)) &&
-         encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.out, s.H, R, 32, 32);
+         encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.out, s.H, R, 64, 32);
   }
   if (!ok) return cudaErrorInvalidValue;
   const size_t smem = SMEM_BYTES_FIXED + (s.E + 1) * sizeof(int32_t);
@@ -924,6 +954,7 @@ static cudaError_t launch_pair(const GemmArgs& g, cudaStream_t st) {
   CUtensorMap tA, tB, tOut;
   GemmParams p;
   p.a_ptr = g.a;
+  p.yscale = g.yscale;
   p.offsets = g.offsets;
   p.permute_src = g.permute_src;
   p.out = g.out;
@@ -948,7 +979,7 @@ static cudaError_t launch_pair(const GemmArgs& g, cudaStream_t st) {
     ok = encode_2d(&tA, dt, ES, g.a, s.I, R, 128 / ES, BM) &&
          (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.I, s.H, s.E, TR::BK, BN / 2)
                        : encode_3d(&tB, dt, ES, g.b, s.H, s.I, s.E, 128 / ES, TR::BK)) &&
-         encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.out, s.H, R, 32, 32);
+         encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.out, s.H, R, 64, 32);
   }
   if (!ok) return cudaErrorInvalidValue;
   const size_t smem = P_SMEM_BYTES_FIXED + (s.E + 1) * sizeof(int32_t);
@@ -1022,15 +1053,17 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
   return e;
 }
 
-cudaError_t launch_combine(const mc2_shape_t& s, const float* y, const float* probs,
-                           const int32_t* offsets, const int32_t* unpermute_dst, void* out,
-                           int out_dtype, cudaStream_t st) {
+cudaError_t launch_combine(const mc2_shape_t& s, const void* y, const float* yscale,
+                           const float* probs, const int32_t* offsets,
+                           const int32_t* unpermute_dst, void* out, int out_dtype,
+                           cudaStream_t st) {
   const int64_t n = static_cast<int64_t>(s.T) * (s.H / 4);
   if (n == 0) return cudaSuccess;
   const int threads = 256;
   const int64_t blocks = (n + threads - 1) / threads;
   combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
-      y, probs, offsets, unpermute_dst, out, s.T, s.H, s.k, s.E, out_dtype == MC2_BF16 ? 1 : 0);
+      static_cast<const __half*>(y), yscale, probs, offsets, unpermute_dst, out, s.T, s.H, s.k, s.E,
+      out_dtype == MC2_BF16 ? 1 : 0);
   note_launches(1);
   return cudaGetLastError();
 }

@@ -3,6 +3,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -39,7 +40,8 @@ struct GemmParams {
   const void* a_ptr;            // fc1: x (rows gathered by the gather warps)
   const int32_t* offsets;
   const int32_t* permute_src;
-  void* out;                    // fc1: h [R, I]; fc2: y [R, H] fp32
+  void* out;                    // fc1: h [R, I]; fc2: y [R, H] fp16 (scaled)
+  float* yscale;                // fc2: decode factor per (row, 64 columns) [R, H/64]
   int32_t* dev_status;
   int E, k, K, n_tiles, out_cols, I;
   uint64_t wait_limit_ns;
@@ -84,6 +86,33 @@ __device__ __forceinline__ void decode_tile(int tile, const int32_t* prefix, int
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 64 fp32 values of one row (a: columns 0-31, b: 32-63) -> 64 fp16 values
+// scaled by a power of two 2^se that puts max|y| in [2^14, 2^15) (fp16 has
+// 11 significant bits, so each value keeps a relative error <= 2^-11).
+// Returns the exact decode factor 2^-se.
+__device__ __forceinline__ float pack_y16(const uint32_t (&a)[32], const uint32_t (&b)[32],
+                                          uint32_t (&pk)[32]) {
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    m = fmaxf(m, fmaxf(fabsf(__uint_as_float(a[i])), fabsf(__uint_as_float(b[i]))));
+  const int e = static_cast<int>((__float_as_uint(m) >> 23) & 0xffu) - 126;  // m = f * 2^e
+  const int se = max(-126, min(126, 15 - e));
+  const float scale = __uint_as_float(static_cast<uint32_t>(127 + se) << 23);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    pk[i] = pack_half2(__uint_as_float(a[2 * i]) * scale, __uint_as_float(a[2 * i + 1]) * scale);
+    pk[16 + i] =
+        pack_half2(__uint_as_float(b[2 * i]) * scale, __uint_as_float(b[2 * i + 1]) * scale);
+  }
+  return __uint_as_float(static_cast<uint32_t>(127 - se) << 23);
 }
 
 __device__ __forceinline__ float round_tf32(float x) {

@@ -13,7 +13,7 @@
 //
 //   fc1: acc1 = x_q[tok] @ w1_q[e]; G = (xs[tok] * w1s[e, n]) * acc1;
 //        h = silu(G_gate) * G_up (fp32) -> requant_rows -> h_q (int8), hs
-//   fc2: acc2 = h_q @ w2_q[e];  y = (hs[p] * w2s[e, n]) * acc2 -> combine
+//   fc2: acc2 = h_q @ w2_q[e];  y = (hs[p] * w2s[e, n]) * acc2 -> scaled fp16 -> combine
 //
 // Tiles are 128 x 128 (fc1: 64 gate + 64 up columns), 6 stages of 32 KB, one
 // CTA per SM, the same warp roles as the bf16 kernel.  Operands are bf16
@@ -40,7 +40,8 @@ struct QParams {
   const int32_t* permute_src;
   const float* a_scale;        // fc1: xs [T] (per token); fc2: hs [R] (per permuted row)
   const float* b_scale;        // fc1: w1s [E, 2I]; fc2: w2s [E, H]
-  void* out;                   // raw: int32 acc; else fc1 h fp32 [R, I], fc2 y fp32 [R, H]
+  void* out;                   // raw: int32 acc; else fc1 h fp32 [R, I], fc2 y fp16 [R, H]
+  float* yscale;               // fc2: decode factor per (row, 64 columns)
   int32_t* dev_status;
   int E, k, K, n_tiles, I, H, nchunk, raw;
   uint64_t wait_limit_ns;
@@ -293,10 +294,15 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
                                 : __ldg(p.a_scale + grow);
         const float* cs = p.b_scale + static_cast<int64_t>(e) *
                                           (MODE == MODE_FC1 ? 2 * p.I : p.H);
-        constexpr int NGROUPS = MODE == MODE_FC1 ? 2 : 4;   // 32-column groups
+        // fc1: two groups of 32 gate columns (+ the matching 32 up columns);
+        // fc2: two groups of 64 columns (s0: the first 32, s1: the next 32)
+        constexpr int NGROUPS = 2;
+        constexpr int S1_OFF = MODE == MODE_FC1 ? 64 : 32;   // TMEM column offset of s1
+        constexpr int GW = MODE == MODE_FC1 ? 32 : 64;       // group width in columns
 #pragma unroll 1
         for (int gi = 0; gi < NGROUPS; ++gi) {
-          if (MODE == MODE_FC2 && n * QBN + gi * 32 >= p.H) break;
+          const int col0 = n * (MODE == MODE_FC1 ? 64 : QBN) + gi * GW;
+          if (MODE == MODE_FC2 && col0 >= p.H) break;
           // exact int32 sums over the K chunks of this group's columns
           int32_t s0[32], s1[32];
 #pragma unroll
@@ -304,61 +310,62 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
 #pragma unroll 1
           for (int c = 0; c < nchunk; ++c) {
             uint32_t v[32];
-            tmem_ld32(tbase + c * QBN + gi * 32, v);
+            tmem_ld32(tbase + c * QBN + gi * GW, v);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) s0[i] += __float2int_rn(__uint_as_float(v[i]));
-            if (MODE == MODE_FC1) {
-              tmem_ld32(tbase + c * QBN + 64 + gi * 32, v);
-              tmem_ld_wait();
+            tmem_ld32(tbase + c * QBN + gi * GW + S1_OFF, v);
+            tmem_ld_wait();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) s1[i] += __float2int_rn(__uint_as_float(v[i]));
-            }
+            for (int i = 0; i < 32; ++i) s1[i] += __float2int_rn(__uint_as_float(v[i]));
           }
           if (p.raw) {  // test mode: the int32 accumulators themselves
             if (valid) {
               int32_t* o = static_cast<int32_t*>(p.out);
+              int4* d0;
+              int4* d1;
               if (MODE == MODE_FC1) {
-                int4* dg = reinterpret_cast<int4*>(o + static_cast<int64_t>(grow) * 2 * p.I + n * 64 + gi * 32);
-                int4* du = reinterpret_cast<int4*>(o + static_cast<int64_t>(grow) * 2 * p.I + p.I + n * 64 + gi * 32);
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                  dg[v] = make_int4(s0[4 * v], s0[4 * v + 1], s0[4 * v + 2], s0[4 * v + 3]);
-                  du[v] = make_int4(s1[4 * v], s1[4 * v + 1], s1[4 * v + 2], s1[4 * v + 3]);
-                }
+                d0 = reinterpret_cast<int4*>(o + static_cast<int64_t>(grow) * 2 * p.I + col0);
+                d1 = reinterpret_cast<int4*>(o + static_cast<int64_t>(grow) * 2 * p.I + p.I + col0);
               } else {
-                int4* d = reinterpret_cast<int4*>(o + static_cast<int64_t>(grow) * p.H + n * QBN + gi * 32);
+                d0 = reinterpret_cast<int4*>(o + static_cast<int64_t>(grow) * p.H + col0);
+                d1 = reinterpret_cast<int4*>(o + static_cast<int64_t>(grow) * p.H + col0 + 32);
+              }
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                  d[v] = make_int4(s0[4 * v], s0[4 * v + 1], s0[4 * v + 2], s0[4 * v + 3]);
+              for (int v = 0; v < 8; ++v) {
+                d0[v] = make_int4(s0[4 * v], s0[4 * v + 1], s0[4 * v + 2], s0[4 * v + 3]);
+                d1[v] = make_int4(s1[4 * v], s1[4 * v + 1], s1[4 * v + 2], s1[4 * v + 3]);
               }
             }
             continue;
           }
           // dequant: (row scale * column scale) * acc, in fp32
-          uint32_t outv[32];
+          uint32_t pk[32];
           if (MODE == MODE_FC1) {
-            const int cg = n * 64 + gi * 32;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float g = (rs * __ldg(cs + cg + i)) * static_cast<float>(s0[i]);
-              const float u = (rs * __ldg(cs + p.I + cg + i)) * static_cast<float>(s1[i]);
-              outv[i] = __float_as_uint(silu_f(g) * u);
+              const float g = (rs * __ldg(cs + col0 + i)) * static_cast<float>(s0[i]);
+              const float u = (rs * __ldg(cs + p.I + col0 + i)) * static_cast<float>(s1[i]);
+              pk[i] = __float_as_uint(silu_f(g) * u);
             }
-          } else {
-            const int cg = n * QBN + gi * 32;
+          } else {  // y as fp16 with a power-of-two scale per 64 columns
+            uint32_t y0[32], y1[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              outv[i] = __float_as_uint((rs * __ldg(cs + cg + i)) * static_cast<float>(s0[i]));
+            for (int i = 0; i < 32; ++i) {
+              y0[i] = __float_as_uint((rs * __ldg(cs + col0 + i)) * static_cast<float>(s0[i]));
+              y1[i] = __float_as_uint((rs * __ldg(cs + col0 + 32 + i)) * static_cast<float>(s1[i]));
+            }
+            const float inv = pack_y16(y0, y1, pk);
+            if (valid) p.yscale[static_cast<int64_t>(grow) * (p.H / 64) + col0 / 64] = inv;
           }
           const int out_cols = MODE == MODE_FC1 ? p.I : p.H;
-          const int col0 = MODE == MODE_FC1 ? n * 64 + gi * 32 : n * QBN + gi * 32;
+          constexpr int ESZ = MODE == MODE_FC1 ? 4 : 2;   // h fp32, y fp16
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
 #pragma unroll
           for (int v = 0; v < 8; ++v)
             *reinterpret_cast<uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4)) =
-                make_uint4(outv[4 * v], outv[4 * v + 1], outv[4 * v + 2], outv[4 * v + 3]);
+                make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           if (wrows == 32) {
             fence_proxy_async_smem();
             __syncwarp();
@@ -367,11 +374,11 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
               bulk_commit();
             }
           } else if (valid) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) +
-                                                    static_cast<int64_t>(grow) * out_cols + col0);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(p.out) +
+                                                  (static_cast<int64_t>(grow) * out_cols + col0) * ESZ);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
-              dst[v] = *reinterpret_cast<const float4*>(stage + row_off + ((v ^ (lane & 7)) << 4));
+              dst[v] = *reinterpret_cast<const uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4));
           }
           __syncwarp();
         }
@@ -472,6 +479,7 @@ static cudaError_t launch_q(const QArgs& g, cudaStream_t st) {
   p.a_scale = g.a_scale;
   p.b_scale = g.b_scale;
   p.out = g.out;
+  p.yscale = g.yscale;
   p.dev_status = g.dev_status;
   p.E = s.E;
   p.k = s.k;
@@ -494,7 +502,7 @@ static cudaError_t launch_q(const QArgs& g, cudaStream_t st) {
     ok = encode_2d(&tA, bf, 2, g.a, s.I, R, 64, BM) &&
          encode_3d(&tB, bf, 2, g.b, s.H, s.I, s.E, 64, 64);
     tOut = tB;
-    if (!g.raw) ok = ok && encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.out, s.H, R, 32, 32);
+    if (!g.raw) ok = ok && encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.out, s.H, R, 64, 32);
   }
   if (!ok) return cudaErrorInvalidValue;
   p.nchunk = (p.K / 64 + QCHUNK_KB - 1) / QCHUNK_KB;

@@ -26,7 +26,8 @@ CountsGeom counts_geom(const mc2_shape_t& s);
 // Workspace layout (byte offsets from ws).
 struct WsLayout {
   size_t hist, base;     // int32 [EB * G] each
-  size_t y;              // fp32 [R, H] fc2 rows, expert-major (combine input)
+  size_t y;              // fp16 [R, H] fc2 rows, expert-major, scaled (combine input)
+  size_t yscale;         // fp32 [R, H/64] decode factor of each 64-column group of y
   size_t x_t32, w1_t32, w2_t32;  // fp32 tf32-rounded copies, weights transposed to [E, N, K] (act F32 only)
   size_t h_f32;          // fp32 [R, I] pre-requant SwiGLU output (act I8 only)
   size_t rowmax;         // uint32 [R] row absmax bits (act I8 only)
@@ -54,7 +55,8 @@ struct GemmArgs {
   const int32_t* permute_src;
   const float* a_scale;     // int8: per-token (fc1) or per-row (fc2)
   const float* b_scale;     // int8: per-channel
-  void* out;                // fc1: h [R, I]; fc2: y [R, H] fp32
+  void* out;                // fc1: h [R, I]; fc2: y [R, H] fp16 (scaled)
+  float* yscale;            // fc2: [R, H/64]
   float* out_scale;         // unused by the GEMM itself
   uint32_t* rowmax;         // int8 fc1: row absmax bits
   int32_t* dev_status;
@@ -72,7 +74,8 @@ struct QArgs {
   const int32_t* permute_src;
   const float* a_scale;     // fc1: x scale [T]; fc2: h scale [R]
   const float* b_scale;     // fc1: w1 scale [E, 2I]; fc2: w2 scale [E, H]
-  void* out;                // raw: int32 accumulators; else fc1 h fp32 [R, I], fc2 y fp32 [R, H]
+  void* out;                // raw: int32 accumulators; else fc1 h fp32 [R, I], fc2 y fp16 [R, H]
+  float* yscale;            // fc2 (not raw): [R, H/64]
   int32_t* dev_status;
   int mode;                 // 0 fc1, 1 fc2
   bool raw;
@@ -82,9 +85,10 @@ cudaError_t launch_i8_to_bf16(const int8_t* src, void* dst, size_t n, cudaStream
 cudaError_t launch_requant(const float* h, const int32_t* offsets, const mc2_shape_t& s, int8_t* hq,
                            float* hs, cudaStream_t st);
 
-cudaError_t launch_combine(const mc2_shape_t& s, const float* y, const float* probs,
-                           const int32_t* offsets, const int32_t* unpermute_dst, void* out,
-                           int out_dtype, cudaStream_t st);
+cudaError_t launch_combine(const mc2_shape_t& s, const void* y, const float* yscale,
+                           const float* probs, const int32_t* offsets,
+                           const int32_t* unpermute_dst, void* out, int out_dtype,
+                           cudaStream_t st);
 cudaError_t launch_round_tf32(const float* src, float* dst, size_t n, cudaStream_t st);
 cudaError_t launch_transpose_round_tf32(const float* src, float* dst, int batch, int rows,
                                        int cols, cudaStream_t st);
