@@ -216,6 +216,13 @@ void mc2_set_wait_limit_ns(uint64_t limit_ns);
  * tilings accumulate each output in the same K order.  Host only. */
 void mc2_set_tile_pairing(int32_t mode);
 
+/* Programmatic dependent launch between the kernels of later calls of this
+ * process: 1 (default) lets each kernel's set-up overlap the end of the
+ * previous kernel on the stream (each kernel still waits for its
+ * predecessors' results before reading or writing global memory); 0 launches
+ * them in plain stream order.  Results are identical either way.  Host only. */
+void mc2_set_launch_overlap(int32_t enabled);
+
 /* Number of kernel launches the last successful call on this host thread
  * enqueued. Host only. */
 int32_t mc2_last_launch_count(void);

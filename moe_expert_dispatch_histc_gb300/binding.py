@@ -54,6 +54,7 @@ _SIGS = {
     "mc2_selftest_wait": (ctypes.c_int, [ctypes.c_uint64, _P, _P]),
     "mc2_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "mc2_set_tile_pairing": (None, [ctypes.c_int32]),
+    "mc2_set_launch_overlap": (None, [ctypes.c_int32]),
     "mc2_last_launch_count": (ctypes.c_int32, []),
     "mc2_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -190,6 +191,10 @@ def mc2_set_wait_limit_ns(limit_ns: int) -> None:
 
 def mc2_set_tile_pairing(mode: int) -> None:
     lib().mc2_set_tile_pairing(int(mode))
+
+
+def mc2_set_launch_overlap(enabled: int) -> None:
+    lib().mc2_set_launch_overlap(int(enabled))
 
 
 def mc2_last_launch_count() -> int:

@@ -11,6 +11,7 @@ namespace mc2 {
 
 static std::atomic<uint64_t> g_wait_limit_ns{0};
 static std::atomic<int> g_tile_pairing{0};
+static std::atomic<int> g_launch_overlap{1};
 static thread_local int tl_launches = 0;
 
 uint64_t wait_limit_ns() {
@@ -19,6 +20,8 @@ uint64_t wait_limit_ns() {
 }
 
 int tile_pairing_override() { return g_tile_pairing.load(); }
+
+bool launch_overlap_enabled() { return g_launch_overlap.load() != 0; }
 
 void note_launches(int n) { tl_launches += n; }
 
@@ -330,6 +333,8 @@ mc2_status_t mc2_selftest_wait(uint64_t limit_ns, int32_t* dev_status, void* str
 void mc2_set_wait_limit_ns(uint64_t limit_ns) { g_wait_limit_ns.store(limit_ns); }
 
 void mc2_set_tile_pairing(int32_t mode) { g_tile_pairing.store(mode == 1 || mode == 2 ? mode : 0); }
+
+void mc2_set_launch_overlap(int32_t enabled) { g_launch_overlap.store(enabled ? 1 : 0); }
 
 int32_t mc2_last_launch_count(void) { return tl_launches; }
 

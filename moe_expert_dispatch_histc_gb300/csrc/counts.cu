@@ -20,6 +20,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace mc2 {
 
@@ -61,6 +62,8 @@ __global__ void __launch_bounds__(kCountsWarpsPerBlock * 32)
   int32_t* hist = sh + warp * p.EB;
   for (int b = lane; b < p.EB; b += 32) hist[b] = 0;
   __syncwarp();
+  griddep_wait();
+  griddep_launch_dependents();
   int64_t begin, end;
   warp_range(p, g, begin, end);
   bool bad = false;
@@ -110,6 +113,8 @@ __device__ int64_t block_exclusive_scan(int64_t v, int64_t* warp_sums, int64_t& 
 
 __global__ void __launch_bounds__(1024) scan_counts(CountsParams p) {
   __shared__ int64_t warp_sums[32];
+  griddep_wait();
+  griddep_launch_dependents();
   // exclusive scan of hist in (bin, warp) order; each thread scans a
   // contiguous segment, loading it with independent (unrolled) loads
   const int64_t N = static_cast<int64_t>(p.EB) * p.G;
@@ -152,6 +157,8 @@ __global__ void __launch_bounds__(kCountsWarpsPerBlock * 32)
   const int64_t g = static_cast<int64_t>(blockIdx.x) * kCountsWarpsPerBlock + warp;
   if (g >= p.G) return;
   int32_t* run = sh + warp * p.EB;
+  griddep_wait();
+  griddep_launch_dependents();
   for (int b = lane; b < p.EB; b += 32) run[b] = p.base[static_cast<int64_t>(b) * p.G + g];
   __syncwarp();
   int64_t begin, end;
@@ -212,14 +219,19 @@ cudaError_t launch_counts(const mc2_shape_t& s, const int32_t* sel, int32_t* cnt
   const size_t smem = static_cast<size_t>(kCountsWarpsPerBlock) * geo.EB * sizeof(int32_t);
   const int blocks = static_cast<int>((geo.G + kCountsWarpsPerBlock - 1) / kCountsWarpsPerBlock);
   int launches = 0;
+  cudaError_t err = cudaSuccess;
   if (blocks > 0) {
-    histc_warps<<<blocks, kCountsWarpsPerBlock * 32, smem, st>>>(p);
+    err = launch_kernel(histc_warps, dim3(blocks), dim3(kCountsWarpsPerBlock * 32), smem, st, 1, p);
+    if (err != cudaSuccess) return err;
     ++launches;
   }
-  scan_counts<<<1, 1024, 0, st>>>(p);
+  err = launch_kernel(scan_counts, dim3(1), dim3(1024), 0, st, 1, p);
+  if (err != cudaSuccess) return err;
   ++launches;
   if (blocks > 0) {
-    scatter_warps<<<blocks, kCountsWarpsPerBlock * 32, smem, st>>>(p);
+    err = launch_kernel(scatter_warps, dim3(blocks), dim3(kCountsWarpsPerBlock * 32), smem, st, 1,
+                        p);
+    if (err != cudaSuccess) return err;
     ++launches;
   }
   note_launches(launches);

@@ -99,6 +99,10 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     tmem_alloc(tmem_base_sh, TMEM_COLS);
     tmem_relinquish();
   }
+  // everything above touches only shared memory, TMEM and the parameter
+  // space, so it overlaps the end of the previous kernel in the stream
+  griddep_wait();
+  griddep_launch_dependents();
   if (warp == 2) {  // per-expert tile prefix: ceil(rows_e / BM) * n_tiles
     int run = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
@@ -475,6 +479,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     tmem_alloc_pair(tmem_base_sh, P_TMEM_COLS);
     tmem_relinquish_pair();
   }
+  griddep_wait();
+  griddep_launch_dependents();
   if (warp == 2) {  // per-expert tile prefix: ceil(rows_e / 256) * n_tiles
     int run = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
@@ -813,6 +819,8 @@ __global__ void combine_kernel(const __half* __restrict__ y, const float* __rest
   const int64_t H4 = H / 4;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= T * H4) return;
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t t = idx / H4;
   const int c = static_cast<int>(idx - t * H4) * 4;
   const int32_t nvalid = __ldg(offsets + E);
@@ -842,6 +850,8 @@ __global__ void combine_kernel(const __half* __restrict__ y, const float* __rest
 }
 
 __global__ void round_tf32_kernel(const float* __restrict__ src, float* __restrict__ dst, size_t n) {
+  griddep_wait();
+  griddep_launch_dependents();
   size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (; i < n; i += stride) dst[i] = round_tf32(src[i]);
@@ -855,6 +865,8 @@ __global__ void transpose_round_tf32_kernel(const float* __restrict__ src, float
   const float* s = src + b * rows * static_cast<int64_t>(cols);
   float* d = dst + b * rows * static_cast<int64_t>(cols);
   const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  griddep_wait();
+  griddep_launch_dependents();
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int r = r0 + i, c = c0 + threadIdx.x;
     if (r < rows && c < cols) tile[i][threadIdx.x] = s[static_cast<int64_t>(r) * cols + c];
@@ -940,8 +952,8 @@ static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t tiles_upper = (R / BM + s.E) * static_cast<int64_t>(p.n_tiles);
   const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_upper, 1)));
-  gmm_kernel<MODE, ES><<<grid, Roles<MODE>::kThreads, smem, st>>>(tA, tB, tOut, p);
-  return cudaGetLastError();
+  return launch_kernel(gmm_kernel<MODE, ES>, dim3(grid), dim3(Roles<MODE>::kThreads), smem, st, 1,
+                       tA, tB, tOut, p);
 }
 
 template <int MODE, int ES>
@@ -1017,8 +1029,8 @@ static cudaError_t launch_pair(const GemmArgs& g, cudaStream_t st) {
   const int64_t pair_tiles_upper = (R / (2 * BM) + s.E) * static_cast<int64_t>(p.n_tiles);
   const int grid = 2 * static_cast<int>(std::min<int64_t>(max_clusters,
                                                           std::max<int64_t>(pair_tiles_upper, 1)));
-  cfg.gridDim = dim3(grid, 1, 1);
-  return cudaLaunchKernelEx(&cfg, gmm_pair_kernel<MODE, ES>, tA, tB, tOut, p);
+  return launch_kernel(gmm_pair_kernel<MODE, ES>, dim3(grid), dim3(Roles<MODE>::kThreads), smem,
+                       st, 2, tA, tB, tOut, p);
 }
 
 // Automatic choice, from measurements on GB300 (4096- and 16384-token
@@ -1061,11 +1073,13 @@ cudaError_t launch_combine(const mc2_shape_t& s, const void* y, const float* ysc
   if (n == 0) return cudaSuccess;
   const int threads = 256;
   const int64_t blocks = (n + threads - 1) / threads;
-  combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
-      static_cast<const __half*>(y), yscale, probs, offsets, unpermute_dst, out, s.T, s.H, s.k, s.E,
-      out_dtype == MC2_BF16 ? 1 : 0);
+  const cudaError_t e = launch_kernel(
+      combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st, 1,
+      static_cast<const __half*>(y), yscale, probs, offsets, unpermute_dst, out,
+      static_cast<int64_t>(s.T), static_cast<int>(s.H), static_cast<int>(s.k),
+      static_cast<int>(s.E), out_dtype == MC2_BF16 ? 1 : 0);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_round_tf32(const float* src, float* dst, size_t n, cudaStream_t st) {
@@ -1073,18 +1087,20 @@ cudaError_t launch_round_tf32(const float* src, float* dst, size_t n, cudaStream
   const int threads = 256;
   const size_t want = (n + threads - 1) / threads;
   const unsigned blocks = static_cast<unsigned>(std::min<size_t>(want, 152 * 16));
-  round_tf32_kernel<<<blocks, threads, 0, st>>>(src, dst, n);
+  const cudaError_t e = launch_kernel(round_tf32_kernel, dim3(blocks), dim3(threads), 0, st, 1,
+                                      src, dst, n);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_transpose_round_tf32(const float* src, float* dst, int batch, int rows,
                                        int cols, cudaStream_t st) {
   if (static_cast<int64_t>(batch) * rows * cols == 0) return cudaSuccess;
   dim3 grid((cols + 31) / 32, (rows + 31) / 32, batch);
-  transpose_round_tf32_kernel<<<grid, dim3(32, 8), 0, st>>>(src, dst, rows, cols);
+  const cudaError_t e = launch_kernel(transpose_round_tf32_kernel, grid, dim3(32, 8), 0, st, 1,
+                                      src, dst, rows, cols);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_selftest_wait(uint64_t limit_ns, int32_t* dev_status, cudaStream_t st) {

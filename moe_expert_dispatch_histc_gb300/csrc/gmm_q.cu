@@ -106,6 +106,8 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
     tmem_alloc(tmem_base_sh, TMEM_COLS);
     tmem_relinquish();
   }
+  griddep_wait();
+  griddep_launch_dependents();
   if (warp == 2) {
     int run = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
@@ -401,6 +403,8 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
 // int8 -> bf16 (exact), 16 values per thread step
 __global__ void i8_to_bf16_kernel(const int8_t* __restrict__ src, __nv_bfloat16* __restrict__ dst,
                                   size_t n16) {
+  griddep_wait();
+  griddep_launch_dependents();
   size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (; i < n16; i += stride) {
@@ -423,6 +427,8 @@ __global__ void requant_rows_kernel(const float* __restrict__ h, const int32_t* 
                                     int E, int I, int8_t* __restrict__ hq, float* __restrict__ hs) {
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  griddep_wait();
+  griddep_launch_dependents();
   if (row >= __ldg(offsets + E)) return;
   const float4* hr = reinterpret_cast<const float4*>(h + row * I);
   float m = 0.f;
@@ -451,9 +457,10 @@ cudaError_t launch_i8_to_bf16(const int8_t* src, void* dst, size_t n, cudaStream
   const int threads = 256;
   const unsigned blocks =
       static_cast<unsigned>(std::min<size_t>((n16 + threads - 1) / threads, 152 * 32));
-  i8_to_bf16_kernel<<<blocks, threads, 0, st>>>(src, static_cast<__nv_bfloat16*>(dst), n16);
+  const cudaError_t e = launch_kernel(i8_to_bf16_kernel, dim3(blocks), dim3(threads), 0, st, 1,
+                                      src, static_cast<__nv_bfloat16*>(dst), n16);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_requant(const float* h, const int32_t* offsets, const mc2_shape_t& s, int8_t* hq,
@@ -461,10 +468,11 @@ cudaError_t launch_requant(const float* h, const int32_t* offsets, const mc2_sha
   const int64_t R = static_cast<int64_t>(s.T) * s.k;
   if (R == 0) return cudaSuccess;
   const int warps = 8;
-  requant_rows_kernel<<<static_cast<unsigned>((R + warps - 1) / warps), warps * 32, 0, st>>>(
-      h, offsets, s.E, s.I, hq, hs);
+  const cudaError_t e = launch_kernel(
+      requant_rows_kernel, dim3(static_cast<unsigned>((R + warps - 1) / warps)), dim3(warps * 32), 0,
+      st, 1, h, offsets, static_cast<int>(s.E), static_cast<int>(s.I), hq, hs);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 template <int MODE>
@@ -517,8 +525,8 @@ static cudaError_t launch_q(const QArgs& g, cudaStream_t st) {
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t tiles_upper = (R / BM + s.E) * static_cast<int64_t>(p.n_tiles);
   const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_upper, 1)));
-  gmm_q_kernel<MODE><<<grid, QRoles<MODE>::kThreads, smem, st>>>(tA, tB, tOut, p);
-  return cudaGetLastError();
+  return launch_kernel(gmm_q_kernel<MODE>, dim3(grid), dim3(QRoles<MODE>::kThreads), smem, st, 1,
+                       tA, tB, tOut, p);
 }
 
 cudaError_t launch_gemm_q(const QArgs& g, cudaStream_t st) {

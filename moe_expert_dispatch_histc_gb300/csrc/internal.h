@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "mc2moe.h"
 
 namespace mc2 {
@@ -38,6 +40,38 @@ struct WsLayout {
 WsLayout ws_layout(const mc2_shape_t& s);
 
 uint64_t wait_limit_ns();
+bool launch_overlap_enabled();  // programmatic dependent launch between the block's kernels
+
+// Launch `kernel` on `st` with programmatic stream serialization (so its
+// prologue overlaps the previous kernel's tail; the kernel itself waits with
+// griddepcontrol.wait before touching global memory) and, when cluster_x > 1,
+// thread-block clusters of cluster_x CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, int cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (launch_overlap_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 int tile_pairing_override();  // 0 auto, 1 single CTAs, 2 CTA pairs
 void note_launches(int n);
 void reset_launches();

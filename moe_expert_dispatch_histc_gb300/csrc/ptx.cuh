@@ -30,6 +30,21 @@ __device__ __forceinline__ bool elect_one() {  // lane 0 of a converged warp
 }
 
 // ----------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream finishes;
+// griddep_wait() returns once every prerequisite grid has completed and its
+// memory is visible (a no-op for kernels launched without the attribute).
+// Every kernel of the block waits before its first global-memory access.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ----------------------------------------------------------------------------
 // mbarrier
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

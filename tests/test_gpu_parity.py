@@ -130,6 +130,21 @@ def test_determinism_bitwise(pairing):
     assert torch.equal(b1.h.view(torch.int16), b2.h.view(torch.int16))
 
 
+@pytest.mark.parametrize("wl", [SMALL[1], SMALL[3]], ids=lambda w: w.name)
+def test_launch_overlap_changes_nothing(wl):
+    """Programmatic dependent launch on or off: bitwise the same block."""
+    ensure_built()
+    try:
+        B.mc2_set_launch_overlap(0)
+        _, _, b0 = run_gpu(wl, seed=7)
+    finally:
+        B.mc2_set_launch_overlap(1)
+    _, _, b1 = run_gpu(wl, seed=7)
+    assert torch.equal(b0.out.view(torch.int16), b1.out.view(torch.int16))
+    assert torch.equal(b0.h.view(torch.int16), b1.h.view(torch.int16))
+    assert int(b1.dev_status.item()) == 0
+
+
 # ------------------------------------------------------------------ edge cases
 def _custom(wl, sel, seed=5):
     inp = make_inputs(wl, seed)
