@@ -20,6 +20,9 @@
  *    `stream`, in order.  Inputs are read-only; outputs are fully written.
  *  - Tensors are dense row-major with the shapes given; element types follow
  *    mc2_shape_t.act (activations and weights) and mc2_shape_t.out.
+ *  - Every array pointer is 16-byte aligned and the workspace 256-byte
+ *    aligned (the kernels use 16-byte vector and TMA accesses); a misaligned
+ *    pointer returns MC2_ERR_INVALID_ARG.
  *  - A synchronous return other than MC2_OK means nothing was enqueued.
  *  - Conditions found on the device (an expert id outside [0, E); a bounded
  *    device-side wait that expired) are OR-ed into *dev_status as
@@ -215,6 +218,13 @@ void mc2_set_wait_limit_ns(uint64_t limit_ns);
  * 2 = always CTA pairs.  The choice does not change any result bit: both
  * tilings accumulate each output in the same K order.  Host only. */
 void mc2_set_tile_pairing(int32_t mode);
+
+/* Which counts pass later calls of this process use: 0 (default) one launch
+ * of a thread-block cluster (up to 16 CTAs, per-CTA tables in shared memory)
+ * whenever its tables fit, else three launches over the workspace tables;
+ * 1 always three launches; 2 the same as 0 (the cluster pass when it fits).
+ * Outputs are identical either way.  Host only. */
+void mc2_set_counts_path(int32_t mode);
 
 /* Programmatic dependent launch between the kernels of later calls of this
  * process: 1 (default) lets each kernel's set-up overlap the end of the

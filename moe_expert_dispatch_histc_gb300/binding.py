@@ -55,6 +55,7 @@ _SIGS = {
     "mc2_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "mc2_set_tile_pairing": (None, [ctypes.c_int32]),
     "mc2_set_launch_overlap": (None, [ctypes.c_int32]),
+    "mc2_set_counts_path": (None, [ctypes.c_int32]),
     "mc2_last_launch_count": (ctypes.c_int32, []),
     "mc2_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -195,6 +196,10 @@ def mc2_set_tile_pairing(mode: int) -> None:
 
 def mc2_set_launch_overlap(enabled: int) -> None:
     lib().mc2_set_launch_overlap(int(enabled))
+
+
+def mc2_set_counts_path(mode: int) -> None:
+    lib().mc2_set_counts_path(int(mode))
 
 
 def mc2_last_launch_count() -> int:

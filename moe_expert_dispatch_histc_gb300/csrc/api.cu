@@ -4,6 +4,7 @@
 
 #include <atomic>
 #include <cstring>
+#include <initializer_list>
 
 #include "internal.h"
 
@@ -12,6 +13,7 @@ namespace mc2 {
 static std::atomic<uint64_t> g_wait_limit_ns{0};
 static std::atomic<int> g_tile_pairing{0};
 static std::atomic<int> g_launch_overlap{1};
+static std::atomic<int> g_counts_path{0};
 static thread_local int tl_launches = 0;
 
 uint64_t wait_limit_ns() {
@@ -22,6 +24,8 @@ uint64_t wait_limit_ns() {
 int tile_pairing_override() { return g_tile_pairing.load(); }
 
 bool launch_overlap_enabled() { return g_launch_overlap.load() != 0; }
+
+int counts_path_override() { return g_counts_path.load(); }
 
 void note_launches(int n) { tl_launches += n; }
 
@@ -80,23 +84,36 @@ bool shape_ok(const mc2_shape_t* s) {
 
 mc2_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MC2_OK : MC2_ERR_CUDA; }
 
+// Pointer rule: every array 16-byte aligned (vector and TMA accesses), the
+// workspace 256-byte aligned.  NULL passes (the null rules are separate).
+bool aligned(std::initializer_list<const void*> ps, uintptr_t a = 16) {
+  for (const void* p : ps)
+    if (reinterpret_cast<uintptr_t>(p) & (a - 1)) return false;
+  return true;
+}
+
 mc2_status_t do_counts(const mc2_shape_t* s, const int32_t* sel, int32_t* cnt, int32_t* recv,
                        int32_t* offsets, int32_t* permute_src, int32_t* unpermute_dst, void* ws,
-                       int32_t* dev_status, cudaStream_t st) {
+                       int32_t* dev_status, cudaStream_t st, bool launch = true) {
   if (!cnt || !recv || !offsets || !ws) return MC2_ERR_INVALID_ARG;
   if (s->T > 0 && (!sel || !permute_src || !unpermute_dst)) return MC2_ERR_INVALID_ARG;
+  if (!aligned({sel, cnt, recv, offsets, permute_src, unpermute_dst}) || !aligned({ws}, 256))
+    return MC2_ERR_INVALID_ARG;
+  if (!launch) return MC2_OK;
   return cuda_status(launch_counts(*s, sel, cnt, recv, offsets, permute_src, unpermute_dst,
                                    static_cast<char*>(ws), dev_status, st));
 }
 
 mc2_status_t do_fc1_i8(const mc2_shape_t* s, const void* x, const float* x_scale,
                        const float* w1_scale, const int32_t* offsets, const int32_t* permute_src,
-                       void* ws, void* h, float* h_scale, int32_t* dev_status, cudaStream_t st) {
+                       void* ws, void* h, float* h_scale, int32_t* dev_status, cudaStream_t st, bool launch = true) {
   const bool raw = s->out == MC2_I32;
   if (!offsets || !ws) return MC2_ERR_INVALID_ARG;
   if (raw ? (h_scale != nullptr) : (!x_scale || !w1_scale || !h_scale)) return MC2_ERR_INVALID_ARG;
   if (s->T > 0 && (!x || !permute_src || !h)) return MC2_ERR_INVALID_ARG;
-  if (s->T == 0) return MC2_OK;
+  if (!aligned({x, x_scale, w1_scale, offsets, permute_src, h, h_scale}) || !aligned({ws}, 256))
+    return MC2_ERR_INVALID_ARG;
+  if (!launch || s->T == 0) return MC2_OK;
   const WsLayout L = ws_layout(*s);
   char* w = static_cast<char*>(ws);
   if (launch_i8_to_bf16(static_cast<const int8_t*>(x), w + L.x_b16,
@@ -125,13 +142,16 @@ mc2_status_t do_fc1_i8(const mc2_shape_t* s, const void* x, const float* x_scale
 mc2_status_t do_fc2_i8(const mc2_shape_t* s, const void* h, const float* h_scale,
                        const float* w2_scale, const int32_t* offsets, const int32_t* permute_src,
                        const int32_t* unpermute_dst, const float* probs, void* ws, void* out,
-                       int32_t* dev_status, cudaStream_t st) {
+                       int32_t* dev_status, cudaStream_t st, bool launch = true) {
   const bool raw = s->out == MC2_I32;
   if (!offsets || !ws) return MC2_ERR_INVALID_ARG;
   if (!raw && (!h_scale || !w2_scale)) return MC2_ERR_INVALID_ARG;
   if (s->T > 0 && (!h || !permute_src || !out || (!raw && (!unpermute_dst || !probs))))
     return MC2_ERR_INVALID_ARG;
-  if (s->T == 0) return MC2_OK;
+  if (!aligned({h, h_scale, w2_scale, offsets, permute_src, unpermute_dst, probs, out}) ||
+      !aligned({ws}, 256))
+    return MC2_ERR_INVALID_ARG;
+  if (!launch || s->T == 0) return MC2_OK;
   const WsLayout L = ws_layout(*s);
   char* w = static_cast<char*>(ws);
   const size_t R = static_cast<size_t>(s->T) * s->k;
@@ -160,15 +180,17 @@ mc2_status_t do_fc2_i8(const mc2_shape_t* s, const void* h, const float* h_scale
 
 mc2_status_t do_fc1(const mc2_shape_t* s, const void* x, const float* x_scale, const void* w1,
                     const float* w1_scale, const int32_t* offsets, const int32_t* permute_src,
-                    void* ws, void* h, float* h_scale, int32_t* dev_status, cudaStream_t st) {
+                    void* ws, void* h, float* h_scale, int32_t* dev_status, cudaStream_t st, bool launch = true) {
   if (s->act == MC2_I8) {
     if (s->T > 0 && !w1) return MC2_ERR_INVALID_ARG;
-    return do_fc1_i8(s, x, x_scale, w1_scale, offsets, permute_src, ws, h, h_scale, dev_status, st);
+    return do_fc1_i8(s, x, x_scale, w1_scale, offsets, permute_src, ws, h, h_scale, dev_status, st,
+                     launch);
   }
   if (x_scale || w1_scale || h_scale) return MC2_ERR_INVALID_ARG;
   if (!offsets || !ws) return MC2_ERR_INVALID_ARG;
   if (s->T > 0 && (!x || !w1 || !permute_src || !h)) return MC2_ERR_INVALID_ARG;
-  if (s->T == 0) return MC2_OK;
+  if (!aligned({x, w1, offsets, permute_src, h}) || !aligned({ws}, 256)) return MC2_ERR_INVALID_ARG;
+  if (!launch || s->T == 0) return MC2_OK;
   const WsLayout L = ws_layout(*s);
   char* w = static_cast<char*>(ws);
   GemmArgs g;
@@ -201,17 +223,19 @@ mc2_status_t do_fc1(const mc2_shape_t* s, const void* x, const float* x_scale, c
 mc2_status_t do_fc2(const mc2_shape_t* s, const void* h, const float* h_scale, const void* w2,
                     const float* w2_scale, const int32_t* offsets, const int32_t* permute_src,
                     const int32_t* unpermute_dst, const float* probs, void* ws, void* out,
-                    int32_t* dev_status, cudaStream_t st) {
+                    int32_t* dev_status, cudaStream_t st, bool launch = true) {
   if (s->act == MC2_I8) {
     if (s->T > 0 && !w2) return MC2_ERR_INVALID_ARG;
     return do_fc2_i8(s, h, h_scale, w2_scale, offsets, permute_src, unpermute_dst, probs, ws, out,
-                     dev_status, st);
+                     dev_status, st, launch);
   }
   if (h_scale || w2_scale) return MC2_ERR_INVALID_ARG;
   if (!offsets || !ws) return MC2_ERR_INVALID_ARG;
   if (s->T > 0 && (!h || !w2 || !permute_src || !unpermute_dst || !probs || !out))
     return MC2_ERR_INVALID_ARG;
-  if (s->T == 0) return MC2_OK;
+  if (!aligned({h, w2, offsets, permute_src, unpermute_dst, probs, out}) || !aligned({ws}, 256))
+    return MC2_ERR_INVALID_ARG;
+  if (!launch || s->T == 0) return MC2_OK;
   const WsLayout L = ws_layout(*s);
   char* w = static_cast<char*>(ws);
   void* y = w + L.y;
@@ -298,13 +322,19 @@ mc2_status_t mc2_moe_forward(const mc2_shape_t* s, const void* x, const float* x
   tl_launches = 0;
   if (!shape_ok(s)) return MC2_ERR_INVALID_ARG;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  mc2_status_t r =
-      do_counts(s, sel, cnt, recv, offsets, permute_src, unpermute_dst, ws, dev_status, st);
-  if (r != MC2_OK) return r;
-  r = do_fc1(s, x, x_scale, w1, w1_scale, offsets, permute_src, ws, h, h_scale, dev_status, st);
-  if (r != MC2_OK) return r;
-  return do_fc2(s, h, h_scale, w2, w2_scale, offsets, permute_src, unpermute_dst, probs, ws, out,
-                dev_status, st);
+  // validate all three segments before enqueuing any of them
+  for (const bool launch : {false, true}) {
+    mc2_status_t r = do_counts(s, sel, cnt, recv, offsets, permute_src, unpermute_dst, ws,
+                               dev_status, st, launch);
+    if (r == MC2_OK)
+      r = do_fc1(s, x, x_scale, w1, w1_scale, offsets, permute_src, ws, h, h_scale, dev_status,
+                 st, launch);
+    if (r == MC2_OK)
+      r = do_fc2(s, h, h_scale, w2, w2_scale, offsets, permute_src, unpermute_dst, probs, ws,
+                 out, dev_status, st, launch);
+    if (r != MC2_OK) return r;
+  }
+  return MC2_OK;
 }
 
 mc2_status_t mc2_prepack_weights(const mc2_shape_t* s, const void* w1, const void* w2, void* ws,
@@ -313,6 +343,7 @@ mc2_status_t mc2_prepack_weights(const mc2_shape_t* s, const void* w1, const voi
   if (!shape_ok(s)) return MC2_ERR_INVALID_ARG;
   if (s->act != MC2_I8) return MC2_OK;
   if (!w1 || !w2 || !ws) return MC2_ERR_INVALID_ARG;
+  if (!aligned({w1, w2}) || !aligned({ws}, 256)) return MC2_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(*s);
   char* w = static_cast<char*>(ws);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -335,6 +366,8 @@ void mc2_set_wait_limit_ns(uint64_t limit_ns) { g_wait_limit_ns.store(limit_ns);
 void mc2_set_tile_pairing(int32_t mode) { g_tile_pairing.store(mode == 1 || mode == 2 ? mode : 0); }
 
 void mc2_set_launch_overlap(int32_t enabled) { g_launch_overlap.store(enabled ? 1 : 0); }
+
+void mc2_set_counts_path(int32_t mode) { g_counts_path.store(mode == 1 || mode == 2 ? mode : 0); }
 
 int32_t mc2_last_launch_count(void) { return tl_launches; }
 

@@ -42,6 +42,7 @@ struct Roles {
 };
 
 constexpr size_t SMEM_BYTES_FIXED = 1024 + STAGES * STAGE_BYTES + 4 * OUT_STAGE + 256;
+constexpr int NB1 = BN / 64;  // 64-column blocks of a bf16 B tile
 
 template <int MODE, int ES>
 __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
@@ -158,17 +159,12 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
               tma_load_3d(b_dst, &tmB, &full[s], k0, n * BN, e);
             }
           } else {
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-              int ncol;
-              if (MODE == MODE_FC1) {  // gate half, then up half of the same columns
-                const int half = b / (NB / 2), bb = b % (NB / 2);
-                ncol = half * p.I + n * (BN / 2) + bb * BNB;
-              } else {
-                ncol = n * BN + b * BNB;
-              }
-              tma_load_3d(b_dst + b * B_BLOCK, &tmB, &full[s], ncol, k0, e);
-            }
+            // all NB 64-column blocks in one box: fc1 takes the gate and the
+            // up blocks of the same output columns, fc2 NB adjacent blocks
+            if (MODE == MODE_FC1)
+              tma_load_5d(b_dst, &tmB, &full[s], 0, k0, n * (NB / 2), 0, e);
+            else
+              tma_load_4d(b_dst, &tmB, &full[s], 0, k0, n * NB, e);
           }
         }
         __syncwarp();
@@ -199,7 +195,10 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (lane == 0) ok = mbar_wait(&full[s], ph, ctl);
+        if (lane == 0) {
+          ok = mbar_wait(&full[s], ph, ctl);
+          if (GATHER && ok) fence_proxy_async_smem();  // gathered rows -> async proxy
+        }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
@@ -236,16 +235,16 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     // Thread t copies 16-byte chunk (t % 8) of rows t/8 + 16*i, i = 0..7, of
     // the 128-row A tile: 8 lanes cover one 128-byte row segment, so each
     // warp instruction reads four whole rows.  The chunk lands at its 128B
-    // swizzle position.  MC2_GATHER_DEPTH cp.async groups stay in flight; a
-    // stage is signalled (full[s]) once this thread's copies into it are
-    // complete and made visible to the tensor core's async proxy.
+    // swizzle position.  Each thread's copies into a stage arrive on full[s]
+    // when they land (cp.async.mbarrier.arrive), so the gather runs as far
+    // ahead as the ring has free stages; the MMA thread fences the async
+    // proxy after its wait.
     const int t = threadIdx.x - 6 * 32;
     const int chunk = t & 7, rsub = t >> 3;
     const char* xg = static_cast<const char*>(p.a_ptr);
     const int64_t row_bytes = static_cast<int64_t>(p.K) * ES;
     int s = 0;
     uint32_t ph = 0;
-    int issued = 0, arrived = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       int e, n, row0, rows;
@@ -268,20 +267,11 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           const int r = rsub + 16 * i;
           cp_async16(a_dst + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + kb * 128);
         }
-        cp_async_commit();
-        ++issued;
-        if (issued - arrived == MC2_GATHER_DEPTH) {
-          cp_async_wait<MC2_GATHER_DEPTH - 1>();
-          fence_proxy_async_smem();
-          mbar_arrive(&full[arrived % STAGES]);
-          ++arrived;
-        }
+        cp_async_mbar_arrive_noinc(&full[s]);
         if (++s == STAGES) { s = 0; ph ^= 1; }
       }
     }
     cp_async_wait<0>();
-    fence_proxy_async_smem();
-    for (; arrived < issued; ++arrived) mbar_arrive(&full[arrived % STAGES]);
   } else {
     // ------------------------------------------------------------ epilogue
     // Warp q owns accumulator rows 32q..32q+31 (TMEM lane quarter q).  Each
@@ -546,9 +536,10 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           if constexpr (BKM) {
             tma_load_3d(b_dst, &tmB, &full[s], k0, nbase, e);
           } else {
-#pragma unroll
-            for (int b = 0; b < NBH; ++b)
-              tma_load_3d(b_dst + b * B_BLOCK, &tmB, &full[s], nbase + b * BNB, k0, e);
+            if (MODE == MODE_FC1)
+              tma_load_5d(b_dst, &tmB, &full[s], 0, k0, n * NBH, static_cast<int>(rank), e);
+            else
+              tma_load_4d(b_dst, &tmB, &full[s], 0, k0, nbase / BNB, e);
           }
         }
         __syncwarp();
@@ -581,6 +572,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           if (lane == 0) {
             ok = mbar_wait(&full[s], ph, ctl);
             if (ok) ok = mbar_wait_cluster(&pfull[s], ph, ctl);
+            if (GATHER && ok) fence_proxy_async_smem();  // gathered rows -> async proxy
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
@@ -623,6 +615,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
         for (int kb = 0; kb < kblocks; ++kb) {
           if (lane == 0) {
             ok = mbar_wait(&full[s], ph, ctl);
+            if (GATHER && ok) fence_proxy_async_smem();  // gathered rows -> async proxy
             if (ok) mbar_arrive_remote_relaxed(leader_pfull + s * 8);
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -639,7 +632,6 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     const int64_t row_bytes = static_cast<int64_t>(p.K) * ES;
     int s = 0;
     uint32_t ph = 0;
-    int issued = 0, arrived = 0;
     bool ok = true;
     for (int tile = cluster; tile < total && ok; tile += nclusters) {
       int e, n, prow0, prows;
@@ -668,20 +660,11 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           const int r = rsub + 16 * i;
           cp_async16(a_dst + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + kb * 128);
         }
-        cp_async_commit();
-        ++issued;
-        if (issued - arrived == MC2_PAIR_GATHER_DEPTH) {
-          cp_async_wait<MC2_PAIR_GATHER_DEPTH - 1>();
-          fence_proxy_async_smem();
-          mbar_arrive(&full[arrived % P_STAGES]);
-          ++arrived;
-        }
+        cp_async_mbar_arrive_noinc(&full[s]);
         if (++s == P_STAGES) { s = 0; ph ^= 1; }
       }
     }
     cp_async_wait<0>();
-    fence_proxy_async_smem();
-    for (; arrived < issued; ++arrived) mbar_arrive(&full[arrived % P_STAGES]);
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
@@ -812,40 +795,75 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
 // times its exact power-of-two factor; products rounded to fp32 and summed in
 // ascending j, so the result is bitwise reproducible.
 // ----------------------------------------------------------------------------
+// One thread per 8 output columns of a token.  KC > 0: k == KC is known at
+// compile time, so the k row indices, weights, factors and 16-byte row loads
+// are all issued before the first add (k loads in flight per thread instead
+// of one); KC == 0 is the same sum for any k, one slot at a time.
+template <int KC>
 __global__ void combine_kernel(const __half* __restrict__ y, const float* __restrict__ yscale,
                                const float* __restrict__ probs, const int32_t* __restrict__ offsets,
                                const int32_t* __restrict__ unpermute_dst, void* __restrict__ out,
                                int64_t T, int H, int k, int E, int out_bf16) {
-  const int64_t H4 = H / 4;
+  const int64_t H8 = H / 8;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= T * H4) return;
+  if (idx >= T * H8) return;
   griddep_wait();
   griddep_launch_dependents();
-  const int64_t t = idx / H4;
-  const int c = static_cast<int>(idx - t * H4) * 4;
+  const int64_t t = idx / H8;
+  const int c = static_cast<int>(idx - t * H8) * 8;
   const int32_t nvalid = __ldg(offsets + E);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < k; ++j) {
-    const int64_t flat = t * k + j;
-    const int32_t row = __ldg(unpermute_dst + flat);
-    if (row >= nvalid) continue;
-    const float pj = __ldg(probs + flat);
-    const float f = __ldg(yscale + static_cast<int64_t>(row) * (H / 64) + c / 64);
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(y + static_cast<int64_t>(row) * H + c));
-    const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-    const float2 v23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-    acc.x += __fmul_rn(pj, v01.x * f);
-    acc.y += __fmul_rn(pj, v01.y * f);
-    acc.z += __fmul_rn(pj, v23.x * f);
-    acc.w += __fmul_rn(pj, v23.y * f);
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  auto add = [&](float pj, float f, const uint4& raw) {
+    const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 v = __half22float2(h2[i]);
+      acc[2 * i] += __fmul_rn(pj, v.x * f);
+      acc[2 * i + 1] += __fmul_rn(pj, v.y * f);
+    }
+  };
+  if constexpr (KC > 0) {
+    int32_t row[KC];
+    float pj[KC], f[KC];
+    uint4 raw[KC];
+#pragma unroll
+    for (int j = 0; j < KC; ++j) {
+      row[j] = __ldg(unpermute_dst + t * KC + j);
+      pj[j] = __ldg(probs + t * KC + j);
+    }
+#pragma unroll
+    for (int j = 0; j < KC; ++j) {
+      const bool ok = row[j] < nvalid;
+      const int32_t r = ok ? row[j] : 0;
+      f[j] = ok ? __ldg(yscale + static_cast<int64_t>(r) * (H / 64) + c / 64) : 0.f;
+      raw[j] = ok ? __ldg(reinterpret_cast<const uint4*>(y + static_cast<int64_t>(r) * H + c))
+                  : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < KC; ++j)
+      if (row[j] < nvalid) add(pj[j], f[j], raw[j]);
+  } else {
+    for (int j = 0; j < k; ++j) {
+      const int64_t flat = t * k + j;
+      const int32_t r = __ldg(unpermute_dst + flat);
+      if (r >= nvalid) continue;
+      add(__ldg(probs + flat), __ldg(yscale + static_cast<int64_t>(r) * (H / 64) + c / 64),
+          __ldg(reinterpret_cast<const uint4*>(y + static_cast<int64_t>(r) * H + c)));
+    }
   }
   if (out_bf16) {
-    uint2 w;
-    w.x = pack_bf16x2(acc.x, acc.y);
-    w.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + t * H + c) = w;
+    uint4 w;
+    w.x = pack_bf16x2(acc[0], acc[1]);
+    w.y = pack_bf16x2(acc[2], acc[3]);
+    w.z = pack_bf16x2(acc[4], acc[5]);
+    w.w = pack_bf16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + t * H + c) = w;
   } else {
-    *reinterpret_cast<float4*>(static_cast<float*>(out) + t * H + c) = acc;
+    float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + t * H + c);
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
 }
 
@@ -928,7 +946,7 @@ static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
     p.n_tiles = (s.I + BN / 2 - 1) / (BN / 2);
     p.out_cols = s.I;
     ok = (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.H, 2ull * s.I, s.E, TR::BK, BN / 2)
-                       : encode_3d(&tB, dt, ES, g.b, 2ull * s.I, s.H, s.E, 128 / ES, TR::BK)) &&
+                       : encode_b_blocked(&tB, g.b, s.H, 2ull * s.I, s.E, 2, TR::BK, NB1 / 2, 2)) &&
          encode_2d(&tOut, dt, ES, g.out, s.I, R, 128 / ES, 32);
     tA = tB;  // unused: fc1's A rows are gathered with cp.async
   } else {
@@ -937,7 +955,7 @@ static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
     p.out_cols = s.H;
     ok = encode_2d(&tA, dt, ES, g.a, s.I, R, 128 / ES, BM) &&
          (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.I, s.H, s.E, TR::BK, BN)
-                       : encode_3d(&tB, dt, ES, g.b, s.H, s.I, s.E, 128 / ES, TR::BK)) &&
+                       : encode_b_blocked(&tB, g.b, s.I, s.H, s.E, 1, TR::BK, NB1, 1)) &&
          encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.out, s.H, R, 64, 32);
   }
   if (!ok) return cudaErrorInvalidValue;
@@ -981,7 +999,7 @@ static cudaError_t launch_pair(const GemmArgs& g, cudaStream_t st) {
     p.n_tiles = (s.I + BN / 2 - 1) / (BN / 2);
     p.out_cols = s.I;
     ok = (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.H, 2ull * s.I, s.E, TR::BK, BN / 2)
-                       : encode_3d(&tB, dt, ES, g.b, 2ull * s.I, s.H, s.E, 128 / ES, TR::BK)) &&
+                       : encode_b_blocked(&tB, g.b, s.H, 2ull * s.I, s.E, 2, TR::BK, NB1 / 2, 1)) &&
          encode_2d(&tOut, dt, ES, g.out, s.I, R, 128 / ES, 32);
     tA = tB;  // unused: fc1's A rows are gathered with cp.async
   } else {
@@ -990,7 +1008,7 @@ static cudaError_t launch_pair(const GemmArgs& g, cudaStream_t st) {
     p.out_cols = s.H;
     ok = encode_2d(&tA, dt, ES, g.a, s.I, R, 128 / ES, BM) &&
          (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.I, s.H, s.E, TR::BK, BN / 2)
-                       : encode_3d(&tB, dt, ES, g.b, s.H, s.I, s.E, 128 / ES, TR::BK)) &&
+                       : encode_b_blocked(&tB, g.b, s.I, s.H, s.E, 1, TR::BK, NB1 / 2, 1)) &&
          encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.out, s.H, R, 64, 32);
   }
   if (!ok) return cudaErrorInvalidValue;
@@ -1069,12 +1087,21 @@ cudaError_t launch_combine(const mc2_shape_t& s, const void* y, const float* ysc
                            const float* probs, const int32_t* offsets,
                            const int32_t* unpermute_dst, void* out, int out_dtype,
                            cudaStream_t st) {
-  const int64_t n = static_cast<int64_t>(s.T) * (s.H / 4);
+  const int64_t n = static_cast<int64_t>(s.T) * (s.H / 8);
   if (n == 0) return cudaSuccess;
   const int threads = 256;
   const int64_t blocks = (n + threads - 1) / threads;
+  decltype(&combine_kernel<0>) kern;
+  switch (s.k) {
+    case 1: kern = combine_kernel<1>; break;
+    case 2: kern = combine_kernel<2>; break;
+    case 4: kern = combine_kernel<4>; break;
+    case 6: kern = combine_kernel<6>; break;
+    case 8: kern = combine_kernel<8>; break;
+    default: kern = combine_kernel<0>; break;
+  }
   const cudaError_t e = launch_kernel(
-      combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st, 1,
+      kern, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st, 1,
       static_cast<const __half*>(y), yscale, probs, offsets, unpermute_dst, out,
       static_cast<int64_t>(s.T), static_cast<int>(s.H), static_cast<int>(s.k),
       static_cast<int>(s.E), out_dtype == MC2_BF16 ? 1 : 0);

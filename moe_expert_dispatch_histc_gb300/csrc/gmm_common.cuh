@@ -25,17 +25,6 @@ constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int TMEM_COLS = 512;
 constexpr int OUT_STAGE = 4096;    // epilogue staging per warp: 32 rows x 128 bytes
 
-// cp.async groups a gather thread keeps in flight before it signals the
-// oldest stage.  Stage g is signalled when stage g+depth-1 is issued, which
-// needs the MMA to have released stage g+depth-1-STAGES; the smaller the
-// depth, the earlier the signal relative to the MMA's need for stage g.
-#ifndef MC2_GATHER_DEPTH
-#define MC2_GATHER_DEPTH 2
-#endif
-#ifndef MC2_PAIR_GATHER_DEPTH
-#define MC2_PAIR_GATHER_DEPTH 3
-#endif
-
 struct GemmParams {
   const void* a_ptr;            // fc1: x (rows gathered by the gather warps)
   const int32_t* offsets;
@@ -166,6 +155,37 @@ inline bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, int es, const void
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Row-major bf16 weights [E, K, N] seen as blocks of 64 columns (128 bytes):
+// dims (64, K, N/64 [, halves], E).  With halves = 2 the N columns are two
+// halves of N/2 (fc1's gate and up projections) and the map's block index
+// runs within one half, so one box can take the same 128 output columns of
+// both halves.  A box of (64, bk, nblk [, nhalf], 1) lands in shared memory as
+// [half][block][k row][128 B], each 64 x 128 B block 128-byte swizzled: the
+// MN-major UMMA operand layout, in one TMA instruction instead of one per
+// block.  Requires N % 64 == 0 (N/2 % 64 == 0 with halves).
+inline bool encode_b_blocked(CUtensorMap* m, const void* base, uint64_t K, uint64_t N, uint64_t E,
+                             int halves, uint32_t bk, uint32_t nblk, uint32_t nhalf) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const uint64_t row = N * 2;  // bytes per k row
+  if (halves == 2) {
+    cuuint64_t dims[5] = {64, K, N / 2 / 64, 2, E};
+    cuuint64_t strides[4] = {row, 128, N, K * row};  // half stride: N/2 columns = N bytes
+    cuuint32_t box[5] = {64, bk, nblk, nhalf, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  cuuint64_t dims[4] = {64, K, N / 64, E};
+  cuuint64_t strides[3] = {row, 128, K * row};
+  cuuint32_t box[4] = {64, bk, nblk, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

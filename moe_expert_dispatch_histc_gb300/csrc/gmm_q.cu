@@ -31,7 +31,6 @@ constexpr int QB_STAGE = 16384;                // 64 K rows x 128 columns x 2 B
 constexpr int QSTAGE_BYTES = A_STAGE + QB_STAGE;
 constexpr int QCHUNK_KB = 16;                  // k-blocks (of 64) per exact fp32 chunk: K 1024
 constexpr int QMAX_CHUNKS = 4;                 // K <= 4096
-constexpr int QGATHER_DEPTH = 3;
 constexpr size_t QSMEM_BYTES_FIXED = 1024 + QSTAGES * QSTAGE_BYTES + 4 * OUT_STAGE + 256;
 
 struct QParams {
@@ -188,7 +187,10 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
       tc_fence_after();
       const uint32_t d0 = tmem_base + acc * 256;
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (lane == 0) ok = mbar_wait(&full[s], ph, ctl);
+        if (lane == 0) {
+          ok = mbar_wait(&full[s], ph, ctl);
+          if (GATHER && ok) fence_proxy_async_smem();  // gathered rows -> async proxy
+        }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
@@ -230,7 +232,6 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
     const int64_t row_bytes = static_cast<int64_t>(p.K) * 2;
     int s = 0;
     uint32_t ph = 0;
-    int issued = 0, arrived = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       int e, n, row0, rows;
@@ -253,20 +254,11 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
           const int r = rsub + 16 * i;
           cp_async16(a_dst + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + kb * 128);
         }
-        cp_async_commit();
-        ++issued;
-        if (issued - arrived == QGATHER_DEPTH) {
-          cp_async_wait<QGATHER_DEPTH - 1>();
-          fence_proxy_async_smem();
-          mbar_arrive(&full[arrived % QSTAGES]);
-          ++arrived;
-        }
+        cp_async_mbar_arrive_noinc(&full[s]);
         if (++s == QSTAGES) { s = 0; ph ^= 1; }
       }
     }
     cp_async_wait<0>();
-    fence_proxy_async_smem();
-    for (; arrived < issued; ++arrived) mbar_arrive(&full[arrived % QSTAGES]);
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;

@@ -89,6 +89,34 @@ def test_null_pointers_are_rejected_before_any_launch():
     assert B.mc2_selftest_wait(1000, None, stream=0, check=False) == B.MC2_ERR_INVALID_ARG
 
 
+def test_misaligned_pointers_are_rejected():
+    s = _shape()
+    fake = 1 << 40
+    odd = fake + 8          # 8-byte aligned only
+    assert B.mc2_moe_counts(s, odd, fake, fake, fake, fake, fake, fake, None, stream=0,
+                            check=False) == B.MC2_ERR_INVALID_ARG
+    assert B.mc2_moe_counts(s, fake, fake, fake, fake, fake, fake, fake + 16, None, stream=0,
+                            check=False) == B.MC2_ERR_INVALID_ARG     # ws needs 256 bytes
+    assert B.mc2_alltoallv_gmm(s, odd, None, fake, None, fake, fake, fake, fake, None,
+                               stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+    assert B.mc2_gmm_alltoallv(s, fake, None, fake, None, fake, fake, fake, fake, fake, odd,
+                               stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+
+
+def test_forward_validates_every_segment_before_enqueuing():
+    """A bad fc1 or fc2 argument is reported before the counts are launched
+    (with no GPU here, a launch would have failed with MC2_ERR_CUDA)."""
+    s = _shape()
+    fake = 1 << 40
+    args = dict(x=fake, x_scale=None, sel=fake, probs=fake, w1=fake, w1_scale=None, w2=fake,
+                w2_scale=None, cnt=fake, recv=fake, offsets=fake, permute_src=fake,
+                unpermute_dst=fake, h=fake, h_scale=None, out=fake, ws=fake)
+    for bad in (dict(x=None), dict(w2=None), dict(out=fake + 4), dict(h_scale=fake)):
+        a = {**args, **bad}
+        assert B.mc2_moe_forward(s, *a.values(), None, stream=0,
+                                 check=False) == B.MC2_ERR_INVALID_ARG, bad
+
+
 def test_prepack_is_a_noop_for_float_paths_and_checks_int8_args():
     fake = 1 << 40
     assert B.mc2_prepack_weights(_shape(), None, None, None, stream=0, check=False) == B.MC2_OK

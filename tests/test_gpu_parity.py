@@ -52,20 +52,61 @@ def test_selftest_wait_times_out_and_reports():
     assert int(st.item()) & B.MC2_DEV_TIMEOUT
 
 
-@pytest.mark.parametrize("name", ["tiny", "uniform", "skew", "int8", "decode"])
-def test_counts_bit_exact(name):
-    wl = WORKLOADS[name]
+@pytest.fixture(params=[1, 2], ids=["three_launches", "one_cluster"])
+def counts_path(request):
+    """Force one of the two counts passes for the test."""
     ensure_built()
-    inp = make_inputs(wl.scaled(act="bf16") if wl.act == "i8" else wl, 0)
-    wlc = wl.scaled(act="bf16") if wl.act == "i8" else wl
-    d_sel = torch.from_numpy(inp["sel"]).cuda()
+    B.mc2_set_counts_path(request.param)
+    yield request.param
+    B.mc2_set_counts_path(0)
+
+
+def _run_counts(wl, sel):
     from moe_expert_dispatch_histc_gb300 import block as blk
-    b = blk.alloc_buffers(wlc)
-    B.mc2_moe_counts(blk.shape_of(wlc), d_sel, b.cnt, b.recv, b.offsets, b.permute_src,
+    d_sel = torch.from_numpy(np.ascontiguousarray(sel.astype(np.int32))).cuda()
+    b = blk.alloc_buffers(wl)
+    B.mc2_moe_counts(blk.shape_of(wl), d_sel, b.cnt, b.recv, b.offsets, b.permute_src,
                      b.unpermute_dst, b.ws, b.dev_status)
     torch.cuda.synchronize()
+    return b
+
+
+@pytest.mark.parametrize("name", ["tiny", "uniform", "skew", "int8", "decode"])
+def test_counts_bit_exact(name, counts_path):
+    wl = WORKLOADS[name]
+    wlc = wl.scaled(act="bf16") if wl.act == "i8" else wl
+    inp = make_inputs(wlc, 0)
+    b = _run_counts(wlc, inp["sel"])
     _counts_exact(wlc, inp, b)
     assert int(b.dev_status.item()) == 0
+
+
+COUNTS_SHAPES = [
+    Workload("w1_ragged", 1000, 64, 64, 16, 3, 1, "bf16"),        # one rank, ragged last chunk
+    Workload("many_ranks", 1024, 64, 64, 1024, 2, 1024, "bf16"),  # W = E = 1024: three launches only
+    Workload("big_e", 2048, 64, 64, 1024, 8, 8, "bf16"),          # E = 1024 tables in shared memory
+    Workload("long_chunks", 65536, 64, 64, 8, 4, 2, "bf16"),      # 16 CTAs, 512-entry chunks
+]
+
+
+@pytest.mark.parametrize("wl", COUNTS_SHAPES, ids=lambda w: w.name)
+def test_counts_shapes_bit_exact(wl, counts_path):
+    inp = make_inputs(wl, 3)
+    b = _run_counts(wl, inp["sel"])
+    _counts_exact(wl, inp, b)
+    assert int(b.dev_status.item()) == 0
+
+
+def test_counts_invalid_ids_every_value(counts_path):
+    """-2, -1, E and a large id are all invalid: counted nowhere, sorted last."""
+    wl = Workload("bad_counts", 512, 64, 64, 16, 4, 4, "bf16")
+    inp = make_inputs(wl, 4)
+    sel = inp["sel"].copy()
+    sel[0, 0], sel[5, 1], sel[200, 3], sel[511, 2], sel[300, 0] = -2, -1, 16, 1 << 30, -(1 << 31)
+    inp["sel"] = sel
+    b = _run_counts(wl, sel)
+    _counts_exact(wl, inp, b)
+    assert int(b.dev_status.item()) & B.MC2_DEV_BAD_EXPERT_ID
 
 
 SMALL = [
