@@ -181,13 +181,12 @@ def _config(wl, l2):
             "parallelism": "replicas" if int(os.environ.get("WORLD_SIZE", "1")) > 1 else "1gpu"}
 
 
-def e2e_pipelined(wl, d, b, stream, steps):
+def e2e_pipelined(wl, d, b, stream, steps, run):
     """Milliseconds of `steps` pipelined end-to-end steps (see run_cuda), and
     the bytes each step copies to and from the host."""
     import dataclasses
 
     import torch
-    from moe_expert_dispatch_histc_gb300 import block as blk
 
     names = [n for n in ("x", "xs", "sel", "probs") if d.get(n) is not None]
     host = {n: d[n].cpu().pin_memory() for n in names}
@@ -212,7 +211,7 @@ def e2e_pipelined(wl, d, b, stream, steps):
             stream.wait_event(ev_d2h[k])       # step i-2's output is back on the host
         dd = dict(d)
         dd.update(dev[k])
-        blk.run_block(wl, dd, dataclasses.replace(b, out=outs[k]), stream=stream)
+        run(dd, dataclasses.replace(b, out=outs[k]))
         ev_comp[k].record(stream)
         s_d2h.wait_event(ev_comp[k])
         with torch.cuda.stream(s_d2h):
@@ -266,31 +265,56 @@ def run_cuda(args):
     t_prepack = time.perf_counter() - t_prepack
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")  # 256 MB > L2
 
-    def step():
+    unfused = args.path == "unfused"
+    xp = None
+    if unfused:
+        if wl.act != "bf16":
+            raise SystemExit("--path unfused: bf16 workloads only")
+        xp = torch.empty(wl.R, wl.H, dtype=torch.bfloat16, device="cuda")
+
+    def seg_counts():
         B.mc2_moe_counts(shape, d["sel"], b.cnt, b.recv, b.offsets, b.permute_src,
                          b.unpermute_dst, b.ws, b.dev_status, stream=stream)
-        n = B.mc2_last_launch_count()
-        ev[1].record(stream)
-        B.mc2_alltoallv_gmm(shape, d["x"], d["xs"], d["w1"], d["w1s"], b.offsets, b.permute_src,
-                            b.ws, b.h, b.h_scale, b.dev_status, stream=stream)
-        n += B.mc2_last_launch_count()
-        ev[2].record(stream)
+
+    def seg_permute():
+        B.mc2_permute_rows(shape, d["x"], b.permute_src, xp, stream=stream)
+
+    def seg_fc1():
+        if unfused:
+            B.mc2_gmm_swiglu(shape, xp, d["w1"], b.offsets, b.h, b.dev_status, stream=stream)
+        else:
+            B.mc2_alltoallv_gmm(shape, d["x"], d["xs"], d["w1"], d["w1s"], b.offsets,
+                                b.permute_src, b.ws, b.h, b.h_scale, b.dev_status, stream=stream)
+
+    def seg_fc2():
         B.mc2_gmm_alltoallv(shape, b.h, b.h_scale, d["w2"], d["w2s"], b.offsets, b.permute_src,
                             b.unpermute_dst, d["probs"], b.ws, b.out, b.dev_status, stream=stream)
-        n += B.mc2_last_launch_count()
+
+    segments = [("counts", seg_counts)] + ([("permute", seg_permute)] if unfused else []) + \
+        [("fc1_swiglu", seg_fc1), ("fc2_combine", seg_fc2)]
+    nseg = len(segments)
+
+    def step():
+        n = 0
+        for i, (_, fn) in enumerate(segments):
+            fn()
+            n += B.mc2_last_launch_count()
+            if i + 1 < nseg:
+                ev[i + 1].record(stream)
         return n
 
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(nseg + 1)]
     for _ in range(args.warmup):
         flush.zero_()
         ev[0].record(stream)
         step()
-        ev[3].record(stream)
+        ev[nseg].record(stream)
     torch.cuda.synchronize()
     if int(b.dev_status.item()) != 0:
         raise RuntimeError(f"device status {int(b.dev_status.item())} after warm-up")
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nseg + 1)]
+              for _ in range(args.steps)]
     clocks = ClockSampler(local)
     if world > 1:
         dist.barrier()
@@ -303,13 +327,14 @@ def run_cuda(args):
         ev = events[i]
         ev[0].record(stream)
         launches += step()
-        ev[3].record(stream)
+        ev[nseg].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
-    seg = np.array([[e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])]
-                    for e in events])  # ms: counts, fc1, fc2+combine
+    seg = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(nseg)]
+                    for e in events])  # ms per segment, in the order of `segments`
+    segi = {name: i for i, (name, _) in enumerate(segments)}
     total_ms = float(seg.sum())
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
@@ -325,7 +350,11 @@ def run_cuda(args):
     # first copy to the last read-back.  No flush: the weights a step streams
     # (w1 + w2) are larger than L2.
     e2e_steps = max(3, args.steps // 4)
-    e2e_ms, bi, bo = e2e_pipelined(wl, d, b, stream, e2e_steps)
+    if unfused:
+        e2e_run = lambda dd, bb: blk.run_unfused(wl, dd, bb, xp, stream=stream)  # noqa: E731
+    else:
+        e2e_run = lambda dd, bb: blk.run_block(wl, dd, bb, stream=stream)  # noqa: E731
+    e2e_ms, bi, bo = e2e_pipelined(wl, d, b, stream, e2e_steps, e2e_run)
     if world > 1:
         t = torch.tensor([e2e_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -336,8 +365,8 @@ def run_cuda(args):
         dist.barrier() if world > 1 else None
         return
     peaks, src = _peaks()
-    fc1_ms = float(seg[:, 1].mean())
-    fc2_ms = float(seg[:, 2].mean())
+    fc1_ms = float(seg[:, segi["fc1_swiglu"]].mean())
+    fc2_ms = float(seg[:, segi["fc2_combine"]].mean())
     fc1_flops = 2 * wl.R * wl.H * 2 * wl.I
     achieved = fc1_flops / (fc1_ms / 1e3) / 1e12
     peak = float(peaks["bf16_tflops"])
@@ -348,20 +377,25 @@ def run_cuda(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": _config(wl, l2="flushed (256 MB write) between steps"),
         "tflops": tflops, "tflops_frac_of_peak": tflops / peak,
-        "segments_ms": {"counts": float(seg[:, 0].mean()), "fc1_swiglu": fc1_ms,
-                        "fc2_combine": fc2_ms},
-        "roofline": {"kernel": "gmm_kernel<fc1> (permute gather + fc1 + SwiGLU)",
+        "segments_ms": {name: float(seg[:, i].mean()) for name, i in segi.items()},
+        "roofline": {"kernel": ("gmm_kernel<fc1 rows> (fc1 + SwiGLU on materialised rows)"
+                                if unfused else
+                                "gmm_kernel<fc1> (permute gather + fc1 + SwiGLU)"),
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": f"{src} bf16_tflops (burst)",
-                     "traffic": _ncu_traffic("gmm_fc1", wl.name)},
+                     "traffic": None if unfused else _ncu_traffic("gmm_fc1", wl.name)},
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "steps": e2e_steps,
-                "mode": "mc2_moe_forward per step; the next step's host->device copies and the "
+                "mode": ("counts, mc2_permute_rows, mc2_gmm_swiglu, mc2_gmm_alltoallv per step"
+                         if unfused else "mc2_moe_forward per step") +
+                        "; the next step's host->device copies and the "
                         "previous step's device->host read-back overlap the compute (two "
                         "buffer sets, three streams); no L2 flush (w1 + w2 exceed L2)"},
         "gpu_launches": launches,
         "clocks": clk,
     }
+    if unfused:
+        line["config"]["path"] = "unfused: materialised permute + plain grouped fc1"
     if wl.act == "i8":
         line["weight_prepack_ms"] = t_prepack * 1e3
         line["dtype"] = "int8 (exact, on bf16 tensor cores)"
@@ -381,6 +415,9 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--workload", default="uniform", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="fused", choices=["fused", "unfused"],
+                    help="unfused: the non-fused baseline (materialised permute, plain grouped "
+                         "fc1), bf16 workloads only")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -174,6 +174,30 @@ mc2_status_t mc2_moe_counts_static(const mc2_shape_t* s, const int32_t* sel, int
                                    int32_t* unpermute_dst, int32_t* dev_status, void* stream);
 
 /*
+ * The non-fused baseline of the same block: the data flow of the "alltoall"
+ * dispatcher that MC2 replaces ("NPU Training Operators - MC2", sections
+ * "Execution path" and "Migration checks": permute, then the plain grouped
+ * matmul).  mc2_moe_counts, then mc2_permute_rows, then mc2_gmm_swiglu, then
+ * mc2_gmm_alltoallv computes exactly what mc2_moe_forward computes (h and out
+ * are bitwise equal), with the permuted token rows materialised in between
+ * instead of gathered inside fc1.  It exists to measure what that fusion
+ * buys.  bf16 only (act = out = MC2_BF16; other types: MC2_ERR_UNSUPPORTED).
+ *
+ * mc2_permute_rows -- xp[p, :] = x[permute_src[p] / k, :] for every p < T*k.
+ *   x [T, H] and xp [T*k, H] bf16 [dev]; permute_src [T*k] int32 [dev] from
+ *   mc2_moe_counts (every entry a valid flat index).
+ * mc2_gmm_swiglu -- for each expert e and each row p in [offsets[e],
+ *   offsets[e+1]): h[p, :] = SwiGLU(xp[p, :] @ w1[e]); rows from offsets[E]
+ *   on (invalid ids) are not written.  xp [T*k, H], w1 [E, H, 2I], h [T*k, I]
+ *   bf16 [dev]; offsets [E+1] int32 [dev].  dev_status as above (may be NULL).
+ * Pointer and shape rules as for the other entry points.
+ */
+mc2_status_t mc2_permute_rows(const mc2_shape_t* s, const void* x, const int32_t* permute_src,
+                              void* xp, void* stream);
+mc2_status_t mc2_gmm_swiglu(const mc2_shape_t* s, const void* xp, const void* w1,
+                            const int32_t* offsets, void* h, int32_t* dev_status, void* stream);
+
+/*
  * mc2_prepack_weights -- int8 path only (a no-op returning MC2_OK for other
  * activation types): expands the int8 weights w1 [E, H, 2I] and w2 [E, I, H]
  * into bf16 copies held in `ws`.  Every int8 value is exact in bf16; the

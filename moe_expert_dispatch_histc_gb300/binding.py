@@ -50,6 +50,8 @@ _SIGS = {
     "mc2_alltoallv_gmm": (ctypes.c_int, [_SP] + [_P] * 11),
     "mc2_gmm_alltoallv": (ctypes.c_int, [_SP] + [_P] * 12),
     "mc2_moe_forward": (ctypes.c_int, [_SP] + [_P] * 19),
+    "mc2_permute_rows": (ctypes.c_int, [_SP] + [_P] * 4),
+    "mc2_gmm_swiglu": (ctypes.c_int, [_SP] + [_P] * 6),
     "mc2_prepack_weights": (ctypes.c_int, [_SP] + [_P] * 4),
     "mc2_selftest_wait": (ctypes.c_int, [ctypes.c_uint64, _P, _P]),
     "mc2_set_wait_limit_ns": (None, [ctypes.c_uint64]),
@@ -157,6 +159,22 @@ def mc2_gmm_alltoallv(shape, h, h_scale, w2, w2_scale, offsets, permute_src, unp
                                  _p(ws), _p(out), _p(dev_status), _stream(stream))
     if check:
         _check("mc2_gmm_alltoallv", st)
+    return st
+
+
+def mc2_permute_rows(shape, x, permute_src, xp, stream=None, check=True):
+    st = lib().mc2_permute_rows(ctypes.byref(shape), _p(x), _p(permute_src), _p(xp),
+                                _stream(stream))
+    if check:
+        _check("mc2_permute_rows", st)
+    return st
+
+
+def mc2_gmm_swiglu(shape, xp, w1, offsets, h, dev_status=None, stream=None, check=True):
+    st = lib().mc2_gmm_swiglu(ctypes.byref(shape), _p(xp), _p(w1), _p(offsets), _p(h),
+                              _p(dev_status), _stream(stream))
+    if check:
+        _check("mc2_gmm_swiglu", st)
     return st
 
 

@@ -110,3 +110,15 @@ def run_segments(wl: Workload, d: dict, b: BlockBuffers, stream=None, out: str |
         return
     B.mc2_gmm_alltoallv(shape, b.h, b.h_scale, d["w2"], d["w2s"], b.offsets, b.permute_src,
                         b.unpermute_dst, d["probs"], b.ws, b.out, b.dev_status, stream=stream)
+
+
+def run_unfused(wl: Workload, d: dict, b: BlockBuffers, xp: torch.Tensor, stream=None):
+    """The non-fused baseline: counts, materialised permute into xp [T*k, H],
+    plain grouped fc1 + SwiGLU, then fc2 + combine (bf16 only)."""
+    shape = shape_of(wl)
+    B.mc2_moe_counts(shape, d["sel"], b.cnt, b.recv, b.offsets, b.permute_src, b.unpermute_dst,
+                     b.ws, b.dev_status, stream=stream)
+    B.mc2_permute_rows(shape, d["x"], b.permute_src, xp, stream=stream)
+    B.mc2_gmm_swiglu(shape, xp, d["w1"], b.offsets, b.h, b.dev_status, stream=stream)
+    B.mc2_gmm_alltoallv(shape, b.h, None, d["w2"], None, b.offsets, b.permute_src, b.unpermute_dst,
+                        d["probs"], b.ws, b.out, b.dev_status, stream=stream)

@@ -200,7 +200,7 @@ mc2_status_t do_fc1(const mc2_shape_t* s, const void* x, const float* x_scale, c
   g.permute_src = permute_src;
   g.out = h;
   g.dev_status = dev_status;
-  g.mode = 0;
+  g.mode = MODE_FC1;
   if (s->act == MC2_F32) {
     float* xr = reinterpret_cast<float*>(w + L.x_t32);
     float* w1r = reinterpret_cast<float*>(w + L.w1_t32);
@@ -249,7 +249,7 @@ mc2_status_t do_fc2(const mc2_shape_t* s, const void* h, const float* h_scale, c
   g.out = y;
   g.yscale = yscale;
   g.dev_status = dev_status;
-  g.mode = 1;
+  g.mode = MODE_FC2;
   if (s->act == MC2_F32) {
     float* w2r = reinterpret_cast<float*>(w + L.w2_t32);
     // [E, I, H] -> [E, H, I]
@@ -335,6 +335,37 @@ mc2_status_t mc2_moe_forward(const mc2_shape_t* s, const void* x, const float* x
     if (r != MC2_OK) return r;
   }
   return MC2_OK;
+}
+
+mc2_status_t mc2_permute_rows(const mc2_shape_t* s, const void* x, const int32_t* permute_src,
+                              void* xp, void* stream) {
+  tl_launches = 0;
+  if (!shape_ok(s)) return MC2_ERR_INVALID_ARG;
+  if (s->T > 0 && (!x || !permute_src || !xp)) return MC2_ERR_INVALID_ARG;
+  if (!aligned({x, permute_src, xp})) return MC2_ERR_INVALID_ARG;
+  if (s->act != MC2_BF16) return MC2_ERR_UNSUPPORTED;
+  return cuda_status(launch_permute_rows(*s, x, permute_src, xp, static_cast<cudaStream_t>(stream)));
+}
+
+mc2_status_t mc2_gmm_swiglu(const mc2_shape_t* s, const void* xp, const void* w1,
+                            const int32_t* offsets, void* h, int32_t* dev_status, void* stream) {
+  tl_launches = 0;
+  if (!shape_ok(s)) return MC2_ERR_INVALID_ARG;
+  if (!offsets) return MC2_ERR_INVALID_ARG;
+  if (s->T > 0 && (!xp || !w1 || !h)) return MC2_ERR_INVALID_ARG;
+  if (!aligned({xp, w1, offsets, h})) return MC2_ERR_INVALID_ARG;
+  if (s->act != MC2_BF16) return MC2_ERR_UNSUPPORTED;
+  GemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  g.s = s;
+  g.a = xp;
+  g.b = w1;
+  g.offsets = offsets;
+  g.out = h;
+  g.dev_status = dev_status;
+  g.mode = MODE_FC1_ROWS;
+  g.a_elem_bytes = 2;
+  return cuda_status(launch_gemm(g, static_cast<cudaStream_t>(stream)));
 }
 
 mc2_status_t mc2_prepack_weights(const mc2_shape_t* s, const void* w1, const void* w2, void* ws,

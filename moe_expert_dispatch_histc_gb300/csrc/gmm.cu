@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           if constexpr (BKM) {
             // K-major B: N rows of 128 bytes of K; fc1 loads the gate rows
             // and the up rows of the same output columns as two boxes
-            if (MODE == MODE_FC1) {
+            if (MODE != MODE_FC2) {
               tma_load_3d(b_dst, &tmB, &full[s], k0, n * (BN / 2), e);
               tma_load_3d(b_dst + (BN / 2) * 128, &tmB, &full[s], k0, p.I + n * (BN / 2), e);
             } else {
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           } else {
             // all NB 64-column blocks in one box: fc1 takes the gate and the
             // up blocks of the same output columns, fc2 NB adjacent blocks
-            if (MODE == MODE_FC1)
+            if (MODE != MODE_FC2)
               tma_load_5d(b_dst, &tmB, &full[s], 0, k0, n * (NB / 2), 0, e);
             else
               tma_load_4d(b_dst, &tmB, &full[s], 0, k0, n * NB, e);
@@ -295,16 +295,16 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       const int wrows = min(32, rows - q * 32);       // valid rows of this warp
       const int grow0 = row0 + q * 32;                 // first global row of this warp
       if (wrows > 0) {
-        constexpr int GROUP_COLS = 128 / (MODE == MODE_FC1 ? ES : 2);  // output cols per 128 B
-        constexpr int NGROUPS = (MODE == MODE_FC1 ? BN / 2 : BN) / GROUP_COLS;
+        constexpr int GROUP_COLS = 128 / (MODE != MODE_FC2 ? ES : 2);  // output cols per 128 B
+        constexpr int NGROUPS = (MODE != MODE_FC2 ? BN / 2 : BN) / GROUP_COLS;
 #pragma unroll 1
         for (int gi = 0; gi < NGROUPS; ++gi) {
-          const int col0 = n * (MODE == MODE_FC1 ? BN / 2 : BN) + gi * GROUP_COLS;
+          const int col0 = n * (MODE != MODE_FC2 ? BN / 2 : BN) + gi * GROUP_COLS;
           if (col0 >= p.out_cols) break;
           // the previous store out of this warp's staging buffer has read it
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
-          if (MODE == MODE_FC1 && ES == 2) {
+          if (MODE != MODE_FC2 && ES == 2) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               uint32_t g[32], u[32];
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
                   make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           } else {
             uint32_t v32[32];
-            if (MODE == MODE_FC1) {  // fp32 h, tf32-rounded for the fc2 tensor-core pass
+            if (MODE != MODE_FC2) {  // fp32 h, tf32-rounded for the fc2 tensor-core pass
               uint32_t g[32];
               tmem_ld32(tbase + gi * 32, g);
               tmem_ld32(tbase + BN / 2 + gi * 32, v32);
@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           } else if (lane < wrows) {  // tail rows: plain stores of this lane's row
             char* dst = static_cast<char*>(p.out) +
                         (static_cast<int64_t>(grow0 + lane) * p.out_cols + col0) *
-                            (MODE == MODE_FC1 ? ES : 2);
+                            (MODE != MODE_FC2 ? ES : 2);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               reinterpret_cast<uint4*>(dst)[v] =
@@ -531,12 +531,12 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           if (!GATHER) tma_load_2d(sA + s * A_STAGE, &tmA, &full[s], k0, row0);
           // this CTA's 128 columns of B: fc1 gate (even) or up (odd) half;
           // fc2 the first or second 128 of the 256-column tile
-          const int nbase = MODE == MODE_FC1 ? static_cast<int>(rank) * p.I + n * (BN / 2)
+          const int nbase = MODE != MODE_FC2 ? static_cast<int>(rank) * p.I + n * (BN / 2)
                                              : n * BN + static_cast<int>(rank) * (BN / 2);
           if constexpr (BKM) {
             tma_load_3d(b_dst, &tmB, &full[s], k0, nbase, e);
           } else {
-            if (MODE == MODE_FC1)
+            if (MODE != MODE_FC2)
               tma_load_5d(b_dst, &tmB, &full[s], 0, k0, n * NBH, static_cast<int>(rank), e);
             else
               tma_load_4d(b_dst, &tmB, &full[s], 0, k0, nbase / BNB, e);
@@ -690,15 +690,15 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       const int wrows = min(32, rows - q * 32);
       const int grow0 = row0 + q * 32;
       if (wrows > 0) {
-        constexpr int GROUP_COLS = 128 / (MODE == MODE_FC1 ? ES : 2);
-        constexpr int NGROUPS = (MODE == MODE_FC1 ? BN / 2 : BN) / GROUP_COLS;
+        constexpr int GROUP_COLS = 128 / (MODE != MODE_FC2 ? ES : 2);
+        constexpr int NGROUPS = (MODE != MODE_FC2 ? BN / 2 : BN) / GROUP_COLS;
 #pragma unroll 1
         for (int gi = 0; gi < NGROUPS; ++gi) {
-          const int col0 = n * (MODE == MODE_FC1 ? BN / 2 : BN) + gi * GROUP_COLS;
+          const int col0 = n * (MODE != MODE_FC2 ? BN / 2 : BN) + gi * GROUP_COLS;
           if (col0 >= p.out_cols) break;
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
-          if (MODE == MODE_FC1 && ES == 2) {
+          if (MODE != MODE_FC2 && ES == 2) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               uint32_t g[32], u[32];
@@ -733,7 +733,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
                   make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           } else {
             uint32_t v32[32];
-            if (MODE == MODE_FC1) {
+            if (MODE != MODE_FC2) {
               uint32_t g[32];
               tmem_ld32(tbase + gi * 32, g);
               tmem_ld32(tbase + BN / 2 + gi * 32, v32);
@@ -761,7 +761,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           } else if (lane < wrows) {
             char* dst = static_cast<char*>(p.out) +
                         (static_cast<int64_t>(grow0 + lane) * p.out_cols + col0) *
-                            (MODE == MODE_FC1 ? ES : 2);
+                            (MODE != MODE_FC2 ? ES : 2);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               reinterpret_cast<uint4*>(dst)[v] =
@@ -941,14 +941,17 @@ static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
   p.I = s.I;
   p.wait_limit_ns = wait_limit_ns();
   bool ok;
-  if (MODE == MODE_FC1) {
+  if (MODE != MODE_FC2) {
     p.K = s.H;
     p.n_tiles = (s.I + BN / 2 - 1) / (BN / 2);
     p.out_cols = s.I;
     ok = (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.H, 2ull * s.I, s.E, TR::BK, BN / 2)
                        : encode_b_blocked(&tB, g.b, s.H, 2ull * s.I, s.E, 2, TR::BK, NB1 / 2, 2)) &&
          encode_2d(&tOut, dt, ES, g.out, s.I, R, 128 / ES, 32);
-    tA = tB;  // unused: fc1's A rows are gathered with cp.async
+    if (MODE == MODE_FC1_ROWS)  // already permuted rows [R, H]: plain TMA tiles
+      ok = ok && encode_2d(&tA, dt, ES, g.a, s.H, R, 128 / ES, BM);
+    else
+      tA = tB;  // unused: fc1's A rows are gathered with cp.async
   } else {
     p.K = s.I;
     p.n_tiles = (s.H + BN - 1) / BN;
@@ -994,14 +997,17 @@ static cudaError_t launch_pair(const GemmArgs& g, cudaStream_t st) {
   p.I = s.I;
   p.wait_limit_ns = wait_limit_ns();
   bool ok;
-  if (MODE == MODE_FC1) {
+  if (MODE != MODE_FC2) {
     p.K = s.H;
     p.n_tiles = (s.I + BN / 2 - 1) / (BN / 2);
     p.out_cols = s.I;
     ok = (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.H, 2ull * s.I, s.E, TR::BK, BN / 2)
                        : encode_b_blocked(&tB, g.b, s.H, 2ull * s.I, s.E, 2, TR::BK, NB1 / 2, 1)) &&
          encode_2d(&tOut, dt, ES, g.out, s.I, R, 128 / ES, 32);
-    tA = tB;  // unused: fc1's A rows are gathered with cp.async
+    if (MODE == MODE_FC1_ROWS)  // already permuted rows [R, H]: plain TMA tiles
+      ok = ok && encode_2d(&tA, dt, ES, g.a, s.H, R, 128 / ES, BM);
+    else
+      tA = tB;  // unused: fc1's A rows are gathered with cp.async
   } else {
     p.K = s.I;
     p.n_tiles = (s.H + BN - 1) / BN;
@@ -1073,6 +1079,9 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
       e = g.a_elem_bytes == 2 ? launch_pair<MODE_FC1, 2>(g, st) : launch_pair<MODE_FC1, 4>(g, st);
     else
       e = g.a_elem_bytes == 2 ? launch_one<MODE_FC1, 2>(g, st) : launch_one<MODE_FC1, 4>(g, st);
+  } else if (g.mode == MODE_FC1_ROWS) {  // bf16 only
+    if (g.a_elem_bytes != 2) return cudaErrorInvalidValue;
+    e = pairs ? launch_pair<MODE_FC1_ROWS, 2>(g, st) : launch_one<MODE_FC1_ROWS, 2>(g, st);
   } else {
     if (pairs)
       e = g.a_elem_bytes == 2 ? launch_pair<MODE_FC2, 2>(g, st) : launch_pair<MODE_FC2, 4>(g, st);
@@ -1105,6 +1114,34 @@ cudaError_t launch_combine(const mc2_shape_t& s, const void* y, const float* ysc
       static_cast<const __half*>(y), yscale, probs, offsets, unpermute_dst, out,
       static_cast<int64_t>(s.T), static_cast<int>(s.H), static_cast<int>(s.k),
       static_cast<int>(s.E), out_dtype == MC2_BF16 ? 1 : 0);
+  note_launches(1);
+  return e;
+}
+
+// Materialised permute of the non-fused path: xp[p, :] = x[permute_src[p] / k, :]
+// for every permuted row (16 bytes per thread).
+__global__ void permute_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src,
+                                    int k, int64_t R, int H8, uint4* __restrict__ xp) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= R * H8) return;
+  const int64_t p = i / H8;
+  const int c = static_cast<int>(i - p * H8);
+  xp[i] = __ldg(x + static_cast<int64_t>(__ldg(src + p) / k) * H8 + c);
+}
+
+cudaError_t launch_permute_rows(const mc2_shape_t& s, const void* x, const int32_t* permute_src,
+                                void* xp, cudaStream_t st) {
+  const int64_t R = static_cast<int64_t>(s.T) * s.k;
+  const int H8 = s.H / 8;  // bf16: 8 per 16 bytes
+  if (R == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (R * H8 + threads - 1) / threads;
+  const cudaError_t e = launch_kernel(permute_rows_kernel, dim3(static_cast<unsigned>(blocks)),
+                                      dim3(threads), 0, st, 1, static_cast<const uint4*>(x),
+                                      permute_src, static_cast<int>(s.k), R, H8,
+                                      static_cast<uint4*>(xp));
   note_launches(1);
   return e;
 }

@@ -14,7 +14,6 @@
 
 namespace mc2 {
 
-enum { MODE_FC1 = 0, MODE_FC2 = 1 };
 
 constexpr int BM = 128;            // rows per tile (UMMA M)
 constexpr int BN = 256;            // accumulator columns per tile (UMMA N)

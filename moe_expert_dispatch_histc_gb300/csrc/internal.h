@@ -25,6 +25,12 @@ struct CountsGeom {
 };
 CountsGeom counts_geom(const mc2_shape_t& s);
 
+// Grouped-GEMM modes.  MODE_FC1: fc1 + SwiGLU with the permute folded in
+// (token rows gathered); MODE_FC2: fc2 -> scaled fp16 rows; MODE_FC1_ROWS:
+// fc1 + SwiGLU on rows that are already permuted (the non-fused baseline
+// path; plain TMA A tiles).
+enum { MODE_FC1 = 0, MODE_FC2 = 1, MODE_FC1_ROWS = 2 };
+
 // Workspace layout (byte offsets from ws).
 struct WsLayout {
   size_t hist, base;     // int32 [EB * G] each
@@ -99,6 +105,8 @@ struct GemmArgs {
   int mode;                 // see gmm.cu
 };
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st);
+cudaError_t launch_permute_rows(const mc2_shape_t& s, const void* x, const int32_t* permute_src,
+                                void* xp, cudaStream_t st);
 
 // int8 path (bf16 tensor cores holding int8 values, exact int32 sums)
 struct QArgs {

@@ -117,6 +117,24 @@ def test_forward_validates_every_segment_before_enqueuing():
                                  check=False) == B.MC2_ERR_INVALID_ARG, bad
 
 
+def test_baseline_path_argument_rules():
+    fake = 1 << 40
+    s = _shape()
+    assert B.mc2_permute_rows(s, fake, fake, None, stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+    assert B.mc2_permute_rows(s, fake + 8, fake, fake, stream=0,
+                              check=False) == B.MC2_ERR_INVALID_ARG
+    assert B.mc2_gmm_swiglu(s, fake, fake, None, fake, None, stream=0,
+                            check=False) == B.MC2_ERR_INVALID_ARG
+    assert B.mc2_gmm_swiglu(_shape(E=9), fake, fake, fake, fake, None, stream=0,
+                            check=False) == B.MC2_ERR_INVALID_ARG
+    for act in ("f32", "i8"):  # the baseline path is bf16 only
+        sa = _shape(act=act)
+        assert B.mc2_permute_rows(sa, fake, fake, fake, stream=0,
+                                  check=False) == B.MC2_ERR_UNSUPPORTED
+        assert B.mc2_gmm_swiglu(sa, fake, fake, fake, fake, None, stream=0,
+                                check=False) == B.MC2_ERR_UNSUPPORTED
+
+
 def test_prepack_is_a_noop_for_float_paths_and_checks_int8_args():
     fake = 1 << 40
     assert B.mc2_prepack_weights(_shape(), None, None, None, stream=0, check=False) == B.MC2_OK

@@ -186,6 +186,39 @@ def test_launch_overlap_changes_nothing(wl):
     assert int(b1.dev_status.item()) == 0
 
 
+def _unfused(wl, seed, out=None):
+    from moe_expert_dispatch_histc_gb300 import block as blk
+    inp = make_inputs(wl, seed)
+    d = blk.inputs_to_device(inp, wl)
+    b = blk.alloc_buffers(wl)
+    xp = torch.empty(wl.T * wl.k, wl.H, dtype=torch.bfloat16, device="cuda")
+    blk.run_unfused(wl, d, b, xp)
+    torch.cuda.synchronize()
+    return inp, d, b, xp
+
+
+@pytest.mark.parametrize("wl", [w for w in SMALL if w.act == "bf16"], ids=lambda w: w.name)
+def test_unfused_baseline_equals_fused_block(wl):
+    """Materialised permute + plain grouped fc1, then fc2 + combine: the same
+    h and out bits as the fused block, and xp[p] = x[permute_src[p] / k]."""
+    inp, d, b, xp = _unfused(wl, 10)
+    _, _, bf = run_gpu(wl, seed=10)
+    src = to_np(b.permute_src)
+    x = torch.from_numpy(inp["x"].view(np.int16)).cuda()
+    assert torch.equal(xp.view(torch.int16), x[torch.from_numpy(src // wl.k).cuda().long()])
+    assert torch.equal(b.h.view(torch.int16), bf.h.view(torch.int16))
+    assert torch.equal(b.out.view(torch.int16), bf.out.view(torch.int16))
+    assert int(b.dev_status.item()) == 0
+
+
+def test_unfused_baseline_full_size_uniform():
+    wl = WORKLOADS["uniform"]
+    _, _, b, _ = _unfused(wl, 0)
+    _, _, bf = run_gpu(wl, seed=0)
+    assert torch.equal(b.out.view(torch.int16), bf.out.view(torch.int16))
+    assert int(b.dev_status.item()) == 0
+
+
 # ------------------------------------------------------------------ edge cases
 def _custom(wl, sel, seed=5):
     inp = make_inputs(wl, seed)
