@@ -407,6 +407,107 @@ def run_cuda(args):
         dist.barrier()
 
 
+MMRS = {"W": 8, "m": 4096, "k": 1024, "n": 4096}   # TP over 8 ranks of a K=8192 projection
+
+
+def run_mmrs(args):
+    """Quantised matmul + reduce-scatter over W logical ranks (one C call per
+    step: int8 -> bf16 copies, the exact int8 grouped GEMM with one group per
+    rank, and the rank-ordered dequant + sum).  Metric: int8 tera-ops/s of
+    the whole operation (2*m*W*k*n per call)."""
+    import torch
+    from moe_expert_dispatch_histc_gb300 import binding as B
+    from moe_expert_dispatch_histc_gb300.build import build
+    build()
+    B.lib()
+    W, m, k, n = MMRS["W"], MMRS["m"], MMRS["k"], MMRS["n"]
+    rng = np.random.default_rng(0)
+    x1 = rng.integers(-127, 128, (W, m, k)).astype(np.int8)
+    x2 = rng.integers(-127, 128, (W, k, n)).astype(np.int8)
+    x1s = rng.uniform(1e-3, 1e-2, (W, m)).astype(np.float32)
+    x2s = rng.uniform(1e-3, 1e-2, (W, n)).astype(np.float32)
+    s = B.MmrsShape(m, k, n, W)
+    ws = torch.empty(B.mc2_mm_reduce_scatter_workspace_bytes(s), dtype=torch.uint8, device="cuda")
+    out = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d = [torch.from_numpy(a).cuda() for a in (x1, x1s, x2, x2s)]
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
+
+    def call():
+        B.mc2_mm_reduce_scatter_i8(s, d[0], d[1], d[2], d[3], out, ws, st, stream=stream)
+        return B.mc2_last_launch_count()
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.2)
+    evs, launches = [], 0
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launches += call()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())}")
+    ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    ops = 2.0 * m * W * k * n
+    value = ops / (ms / 1e3) / 1e12
+    # end to end: inputs from pinned host memory, output back, every call
+    h = [t.cpu().pin_memory() for t in d]
+    h_out = torch.empty(m, n, dtype=torch.bfloat16).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, args.steps // 4)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for dst, src in zip(d, h):
+            dst.copy_(src, non_blocking=True)
+        call()
+        h_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    bi = sum(t.numel() * t.element_size() for t in h)
+    # CPU oracle on a bounded sample: the first rows of every rank's block
+    from oracle import mc2_oracle as orc
+    ms_rows = 8 * W
+    t0 = time.perf_counter()
+    orc.mm_reduce_scatter(x1[:, :ms_rows], x1s[:, :ms_rows], x2, x2s)
+    cpu_s = time.perf_counter() - t0
+    cpu_val = 2.0 * ms_rows * W * k * n / cpu_s / 1e12
+    peaks, src = _peaks()
+    peak = float(peaks["bf16_tflops"])
+    line = {
+        "metric": "int8 matmul + reduce-scatter over logical ranks, tera-ops/s (1 GPU)",
+        "value": value, "unit": "TOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8 (exact, on bf16 tensor cores)", "data": "synthetic",
+        "config": {"workload": f"mm_reduce_scatter W{W} m{m} k{k} n{n}", **MMRS,
+                   "l2": "flushed (256 MB write) between steps"},
+        "roofline": {"kernel": "the whole call (int8->bf16 copies, gmm_q_kernel, reduce)",
+                     "bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
+                     "frac": value / peak,
+                     "peak_source": f"{src} bf16_tflops (burst); int8 runs at the bf16 rate",
+                     "traffic": None},
+        "e2e": {"value": ops / (e2e_ms / 1e3) / 1e12, "unit": "TOP/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": m * n * 2, "steps": e2e_steps,
+                "mode": "inputs copied in, call, output copied back, serially per step"},
+        "cpu_baseline": {"value": cpu_val, "unit": "TOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"first {ms_rows} rows of each of the {W} ranks (int64 "
+                                   f"numpy matmul), {cpu_s:.1f} s"},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -418,9 +519,19 @@ def main():
     ap.add_argument("--path", default="fused", choices=["fused", "unfused"],
                     help="unfused: the non-fused baseline (materialised permute, plain grouped "
                          "fc1), bf16 workloads only")
+    ap.add_argument("--op", default="block", choices=["block", "mm_reduce_scatter"],
+                    help="mm_reduce_scatter: the quantised matmul + reduce-scatter over "
+                         "logical ranks (a separate line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.op == "mm_reduce_scatter":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "--op mm_reduce_scatter has "
+                              "its CPU oracle in the cpu_baseline of the cuda line"}))
+            return
+        run_mmrs(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

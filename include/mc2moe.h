@@ -198,6 +198,41 @@ mc2_status_t mc2_gmm_swiglu(const mc2_shape_t* s, const void* xp, const void* w1
                             const int32_t* offsets, void* h, int32_t* dev_status, void* stream);
 
 /*
+ * Quantised matmul + reduce-scatter over W logical tensor-parallel ranks, the
+ * operation of "torch_npu.npu_mm_reduce_scatter_base" (Ascend op-plugin docs,
+ * sections "Function description" and "Parameters") in its quantised form:
+ * rank r holds x1_r [m, k] int8 with per-token scales x1_scale_r [m] (fp32)
+ * and x2_r [k, n] int8 with per-channel scales x2_scale_r [n] (fp32); the
+ * reduce op is a sum, no bias, bf16 output:
+ *   total = sum over r of (x1_scale_r * x2_scale_r) * (x1_r @ x2_r)
+ * and rank r's result is rows [r*m/W, (r+1)*m/W) of total.
+ *
+ * Inputs [dev], stacked over ranks: x1 [W, m, k], x1_scale [W, m], x2 [W, k,
+ * n], x2_scale [W, n].  Output out [m, n] bf16 [dev]: all ranks' results,
+ * rank r's block at rows r*m/W.  Each rank's x1_r @ x2_r is summed exactly
+ * (int32); the products (x1_scale * x2_scale) * float(acc) are summed in fp32
+ * in rank order, then rounded once to bf16.
+ * Rules: W >= 1, m >= 0, m % W == 0 (the pages: m divisible by world_size),
+ * k and n multiples of 64, 64 <= k <= 4096 (the pages allow k up to 65535;
+ * here K is summed in exact chunks of 1024 in at most four accumulators),
+ * n >= 64; W*m < 2^31.  ws: mc2_mm_reduce_scatter_workspace_bytes(s) bytes
+ * [dev], 256-byte aligned (bf16 copies of x1 and x2 and the int32 partial
+ * products of every rank).  Errors and dev_status as for the block.
+ */
+typedef struct {
+  int32_t m;  /* rows of each rank's x1 */
+  int32_t k;  /* each rank's reduction length */
+  int32_t n;  /* columns */
+  int32_t W;  /* logical ranks (world_size) */
+} mc2_mmrs_shape_t;
+
+size_t mc2_mm_reduce_scatter_workspace_bytes(const mc2_mmrs_shape_t* s);
+mc2_status_t mc2_mm_reduce_scatter_i8(const mc2_mmrs_shape_t* s, const int8_t* x1,
+                                      const float* x1_scale, const int8_t* x2,
+                                      const float* x2_scale, void* out, void* ws,
+                                      int32_t* dev_status, void* stream);
+
+/*
  * mc2_prepack_weights -- int8 path only (a no-op returning MC2_OK for other
  * activation types): expands the int8 weights w1 [E, H, 2I] and w2 [E, I, H]
  * into bf16 copies held in `ws`.  Every int8 value is exact in bf16; the

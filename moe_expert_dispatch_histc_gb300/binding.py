@@ -51,6 +51,8 @@ _SIGS = {
     "mc2_gmm_alltoallv": (ctypes.c_int, [_SP] + [_P] * 12),
     "mc2_moe_forward": (ctypes.c_int, [_SP] + [_P] * 19),
     "mc2_permute_rows": (ctypes.c_int, [_SP] + [_P] * 4),
+    "mc2_mm_reduce_scatter_workspace_bytes": (ctypes.c_size_t, [ctypes.c_void_p]),
+    "mc2_mm_reduce_scatter_i8": (ctypes.c_int, [ctypes.c_void_p] + [_P] * 8),
     "mc2_gmm_swiglu": (ctypes.c_int, [_SP] + [_P] * 6),
     "mc2_prepack_weights": (ctypes.c_int, [_SP] + [_P] * 4),
     "mc2_selftest_wait": (ctypes.c_int, [ctypes.c_uint64, _P, _P]),
@@ -159,6 +161,26 @@ def mc2_gmm_alltoallv(shape, h, h_scale, w2, w2_scale, offsets, permute_src, unp
                                  _p(ws), _p(out), _p(dev_status), _stream(stream))
     if check:
         _check("mc2_gmm_alltoallv", st)
+    return st
+
+
+class MmrsShape(ctypes.Structure):
+    """mc2_mmrs_shape_t: quantised matmul + reduce-scatter over W logical ranks."""
+    _fields_ = [("m", ctypes.c_int32), ("k", ctypes.c_int32), ("n", ctypes.c_int32),
+                ("W", ctypes.c_int32)]
+
+
+def mc2_mm_reduce_scatter_workspace_bytes(shape) -> int:
+    return int(lib().mc2_mm_reduce_scatter_workspace_bytes(ctypes.byref(shape)))
+
+
+def mc2_mm_reduce_scatter_i8(shape, x1, x1_scale, x2, x2_scale, out, ws, dev_status=None,
+                             stream=None, check=True):
+    st = lib().mc2_mm_reduce_scatter_i8(ctypes.byref(shape), _p(x1), _p(x1_scale), _p(x2),
+                                        _p(x2_scale), _p(out), _p(ws), _p(dev_status),
+                                        _stream(stream))
+    if check:
+        _check("mc2_mm_reduce_scatter_i8", st)
     return st
 
 

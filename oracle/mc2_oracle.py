@@ -31,7 +31,9 @@ Sources (page title, then section):
       "Function description" (功能说明): quantised output
       (x1_scale * x2_scale) * (x1 @ x2 + bias); "Parameters" (参数说明):
       x1_scale (m, 1) fp32 per token, x2_scale (1, n) fp32 per channel,
-      output bf16 by default, non-zero bias unsupported.
+      output bf16 by default, non-zero bias unsupported; the op itself is
+      output = reducescatter(...) over world_size ranks with reduce_op 'sum',
+      and m must be divisible by world_size.
 
 Readings where the pages are silent (each also listed in the design notes):
   * ids outside [0, E) are invalid [MIG]; they are left out of every count
@@ -60,7 +62,8 @@ __all__ = [
     "histc", "round_to_bf16", "round_to_f32", "silu", "swiglu",
     "rank_counts", "send_recv_counts", "permute", "unpermute",
     "expert_offsets", "grouped_matmul", "block_forward", "ep_mc2_forward_emulated",
-    "brute_force_token", "quant_block_forward", "requant_rows", "ORACLE_UNPINNED",
+    "brute_force_token", "quant_block_forward", "requant_rows", "mm_reduce_scatter",
+    "ORACLE_UNPINNED",
 ]
 
 # Functions with no pin independent of this file (see tests/test_oracle_pins.py).
@@ -358,6 +361,26 @@ def quant_block_forward(xq, xs, w1q, w1s, w2q, w2s, sel, probs, E, W, hq_overrid
     out = unpermute(y, sorted_indices, probs, valid_rows=nvalid)
     return dict(cnt=num_global, offsets=offsets, permute_src=sorted_indices,
                 acc1=acc1, h=h, hq=hq, hs=hs, acc2=acc2, y=y, out=out)
+
+
+def mm_reduce_scatter(x1q, x1s, x2q, x2s):
+    """Quantised matmul + reduce-scatter over W ranks [RSQ].
+    x1q [W, m, k] int8, x1s [W, m], x2q [W, k, n] int8, x2s [W, n].
+    Each rank's partial is (x1_scale * x2_scale) * (x1 @ x2) with the product
+    exact in int64; the reduce is the sum over ranks (float64 here); rank r
+    receives rows [r*m/W, (r+1)*m/W) of the sum.
+    Returns (acc [W, m, n] int64, total [m, n] float64, per_rank [W, m/W, n])."""
+    W, m, _ = x1q.shape
+    n = x2q.shape[2]
+    assert m % W == 0
+    acc = np.zeros((W, m, n), dtype=np.int64)
+    total = np.zeros((m, n))
+    for r in range(W):
+        acc[r] = x1q[r].astype(np.int64) @ x2q[r].astype(np.int64)
+        scale = x1s[r].astype(np.float64)[:, None] * x2s[r].astype(np.float64)[None, :]
+        total += scale * acc[r]
+    per_rank = total.reshape(W, m // W, n)
+    return acc, total, per_rank
 
 
 def bf16_tolerance_ok(got: np.ndarray, ref: np.ndarray, max_rel=1e-2, mean_rel=2e-3):

@@ -135,6 +135,22 @@ def test_baseline_path_argument_rules():
                                 check=False) == B.MC2_ERR_UNSUPPORTED
 
 
+def test_mm_reduce_scatter_rules():
+    ok = B.MmrsShape(64, 256, 128, 2)
+    assert B.mc2_mm_reduce_scatter_workspace_bytes(ok) >= 2 * 64 * 128 * 4
+    for bad in (B.MmrsShape(63, 256, 128, 2), B.MmrsShape(64, 200, 128, 2),
+                B.MmrsShape(64, 256, 100, 2), B.MmrsShape(64, 4160, 128, 2),
+                B.MmrsShape(64, 256, 128, 0), B.MmrsShape(-2, 256, 128, 2)):
+        assert B.mc2_mm_reduce_scatter_workspace_bytes(bad) == 0
+        assert B.mc2_mm_reduce_scatter_i8(bad, None, None, None, None, None, None, None,
+                                          stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+    fake = 1 << 40
+    assert B.mc2_mm_reduce_scatter_i8(ok, fake, fake, fake, fake, fake, fake + 16, None,
+                                      stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+    assert B.mc2_mm_reduce_scatter_i8(ok, None, fake, fake, fake, fake, fake, None,
+                                      stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+
+
 def test_prepack_is_a_noop_for_float_paths_and_checks_int8_args():
     fake = 1 << 40
     assert B.mc2_prepack_weights(_shape(), None, None, None, stream=0, check=False) == B.MC2_OK

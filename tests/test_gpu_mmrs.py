@@ -1,0 +1,76 @@
+"""Quantised matmul + reduce-scatter over logical ranks on the GPU, against
+the CPU oracle: every rank's int32 partial product bit-exact (read from the
+workspace), the bf16 result within the block's tolerance rule."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import mc2_oracle as orc
+from moe_expert_dispatch_histc_gb300 import binding as B
+
+from gpu_util import ensure_built
+
+pytestmark = pytest.mark.gpu
+
+
+def _align(v, a=256):
+    return (v + a - 1) // a * a
+
+
+def _run(W, m, k, n, seed=0, worst=False):
+    ensure_built()
+    rng = np.random.default_rng(seed)
+    if worst:   # every product at the int8 extreme with one sign: |acc| = k * 127^2 per rank
+        x1 = np.full((W, m, k), 127, np.int8)
+        x2 = np.full((W, k, n), -127, np.int8)
+    else:
+        x1 = rng.integers(-127, 128, (W, m, k)).astype(np.int8)
+        x2 = rng.integers(-127, 128, (W, k, n)).astype(np.int8)
+    x1s = rng.uniform(1e-3, 1e-2, (W, m)).astype(np.float32)
+    x2s = rng.uniform(1e-3, 1e-2, (W, n)).astype(np.float32)
+    s = B.MmrsShape(m, k, n, W)
+    nbytes = B.mc2_mm_reduce_scatter_workspace_bytes(s)
+    assert nbytes > 0
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d = [torch.from_numpy(a).cuda() for a in (x1, x1s, x2, x2s)]
+    B.mc2_mm_reduce_scatter_i8(s, d[0], d[1], d[2], d[3], out, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    acc, total, per_rank = orc.mm_reduce_scatter(x1, x1s, x2, x2s)
+    # workspace: bf16 x1 [W*m, k], bf16 x2 [W, k, n], int32 partials [W*m, n]
+    off = _align(W * m * k * 2) + _align(W * k * n * 2)
+    got_acc = ws[off:off + W * m * n * 4].view(torch.int32).view(W, m, n).cpu().numpy()
+    assert np.array_equal(got_acc, acc), "int32 partial products differ"
+    got = out.float().cpu().numpy()
+    ok, a, b = orc.bf16_tolerance_ok(got, total)
+    assert ok, (a, b)
+    for r in range(W):   # each rank's reduce-scatter block
+        blk = got[r * (m // W):(r + 1) * (m // W)]
+        assert np.array_equal(blk, got.reshape(W, m // W, n)[r])
+    return got, total
+
+
+@pytest.mark.parametrize("W,m,k,n", [(1, 64, 256, 128), (2, 64, 256, 128), (4, 256, 1024, 320),
+                                     (8, 136, 512, 192), (3, 300, 1088, 64)])
+def test_mm_reduce_scatter_parity(W, m, k, n):
+    _run(W, m, k, n, seed=W * 7 + k)
+
+
+def test_mm_reduce_scatter_worst_case_accumulators():
+    """k = 4096 with every product -127*127: |acc| = 66 M > 2^24 per rank, still
+    exact in int32 (four exact 1024-long chunks)."""
+    _run(2, 128, 4096, 128, worst=True)
+
+
+def test_mm_reduce_scatter_empty_and_rejected():
+    ensure_built()
+    s = B.MmrsShape(0, 256, 128, 2)
+    ws = torch.empty(B.mc2_mm_reduce_scatter_workspace_bytes(s), dtype=torch.uint8, device="cuda")
+    x2 = torch.zeros(2, 256, 128, dtype=torch.int8, device="cuda")
+    x2s = torch.ones(2, 128, device="cuda")
+    assert B.mc2_mm_reduce_scatter_i8(s, None, None, x2, x2s, None, ws, None) == B.MC2_OK
+    bad = B.MmrsShape(6, 256, 128, 4)   # m not divisible by W
+    assert B.mc2_mm_reduce_scatter_i8(bad, x2, x2s, x2, x2s, x2, ws, None,
+                                      check=False) == B.MC2_ERR_INVALID_ARG

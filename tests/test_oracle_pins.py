@@ -296,6 +296,68 @@ def test_requant_rows_properties():
     assert np.all(err <= hs[:, None] * (0.5 + 1e-5))
 
 
+# ---------------------------------------------------- quantised matmul + reduce-scatter
+def _mmrs_inputs(W, m, k, n, seed):
+    rng = np.random.default_rng(seed)
+    x1 = rng.integers(-127, 128, (W, m, k)).astype(np.int8)
+    x2 = rng.integers(-127, 128, (W, k, n)).astype(np.int8)
+    x1s = rng.uniform(1e-3, 1e-2, (W, m)).astype(np.float32)
+    x2s = rng.uniform(1e-3, 1e-2, (W, n)).astype(np.float32)
+    return x1, x1s, x2, x2s
+
+
+def test_mm_reduce_scatter_by_brute_force():
+    """Element by element: sum over ranks and over k of
+    x1_scale * x2_scale * x1 * x2, in plain Python integers and floats."""
+    W, m, k, n = 3, 6, 5, 6
+    x1, x1s, x2, x2s = _mmrs_inputs(W, m, k, n, 0)
+    acc, total, per_rank = orc.mm_reduce_scatter(x1, x1s, x2, x2s)
+    for i in range(m):
+        for c in range(n):
+            want = 0.0
+            for r in range(W):
+                a = sum(int(x1[r, i, q]) * int(x2[r, q, c]) for q in range(k))
+                assert acc[r, i, c] == a
+                want += float(x1s[r, i]) * float(x2s[r, c]) * a
+            assert math.isclose(total[i, c], want, rel_tol=1e-12, abs_tol=1e-15)
+    # rank r receives rows [r*m/W, (r+1)*m/W)
+    for r in range(W):
+        assert np.array_equal(per_rank[r], total[r * (m // W):(r + 1) * (m // W)])
+
+
+def test_mm_reduce_scatter_one_rank_is_a_dequantised_matmul():
+    x1, x1s, x2, x2s = _mmrs_inputs(1, 16, 64, 8, 1)
+    _, total, per_rank = orc.mm_reduce_scatter(x1, x1s, x2, x2s)
+    ref = torch.from_numpy(x1[0].astype(np.float64)) @ torch.from_numpy(x2[0].astype(np.float64))
+    ref = (torch.from_numpy(x1s[0].astype(np.float64))[:, None] *
+           torch.from_numpy(x2s[0].astype(np.float64))[None, :]) * ref
+    assert np.allclose(total, ref.numpy(), rtol=1e-13, atol=0)
+    assert per_rank.shape == (1, 16, 8)
+
+
+def test_mm_reduce_scatter_shared_scales_is_one_long_matmul():
+    """With the same scales on every rank, the sum over ranks of x1_r @ x2_r is
+    one matmul over the concatenated reduction axis (block matrix product)."""
+    W, m, k, n = 4, 8, 32, 6
+    x1, x1s, x2, x2s = _mmrs_inputs(W, m, k, n, 2)
+    x1s[:] = x1s[0]
+    x2s[:] = x2s[0]
+    _, total, _ = orc.mm_reduce_scatter(x1, x1s, x2, x2s)
+    a = np.concatenate(list(x1), axis=1).astype(np.float64)          # [m, W*k]
+    b = np.concatenate(list(x2), axis=0).astype(np.float64)          # [W*k, n]
+    ref = (x1s[0].astype(np.float64)[:, None] * x2s[0].astype(np.float64)[None, :]) * (a @ b)
+    assert np.allclose(total, ref, rtol=1e-13, atol=0)
+
+
+def test_mm_reduce_scatter_sum_is_independent_of_rank_order():
+    W, m, k, n = 4, 8, 16, 5
+    x1, x1s, x2, x2s = _mmrs_inputs(W, m, k, n, 3)
+    perm = np.array([2, 0, 3, 1])
+    _, t0, _ = orc.mm_reduce_scatter(x1, x1s, x2, x2s)
+    _, t1, _ = orc.mm_reduce_scatter(x1[perm], x1s[perm], x2[perm], x2s[perm])
+    assert np.allclose(t0, t1, rtol=1e-13, atol=0)
+
+
 def test_tolerance_rule():
     ref = np.array([1.0, -2.0, 4.0])
     assert orc.bf16_tolerance_ok(ref + 1e-4, ref)[0]
@@ -312,6 +374,33 @@ def _mut_swap_gate_up(gu):
 def _mut_sign(g):
     g = np.asarray(g, dtype=np.float64)
     return g / (1.0 + np.exp(g))
+
+
+@pytest.mark.parametrize("mutation", ["drop_channel_scale", "first_rank_only",
+                                      "scatter_columns"])
+def test_planted_reduce_scatter_mistakes_are_caught(monkeypatch, mutation):
+    real = orc.mm_reduce_scatter
+
+    def bad(x1q, x1s, x2q, x2s):
+        W, m, _ = x1q.shape
+        if mutation == "drop_channel_scale":
+            return real(x1q, x1s, x2q, np.ones_like(x2s))
+        if mutation == "first_rank_only":
+            acc, total, _ = real(x1q[:1], x1s[:1], x2q[:1], x2s[:1])
+            return acc, total, total.reshape(W, m // W, -1) if m % W == 0 else None
+        acc, total, _ = real(x1q, x1s, x2q, x2s)       # scatter_columns
+        return acc, total, np.stack(np.split(total, W, axis=1)) if total.shape[1] % W == 0 \
+            else total.reshape(W, m // W, -1)
+    monkeypatch.setattr(orc, "mm_reduce_scatter", bad)
+    failures = 0
+    for fn in (test_mm_reduce_scatter_by_brute_force,
+               test_mm_reduce_scatter_one_rank_is_a_dequantised_matmul,
+               test_mm_reduce_scatter_shared_scales_is_one_long_matmul):
+        try:
+            fn()
+        except (AssertionError, ValueError, IndexError):
+            failures += 1
+    assert failures > 0, f"no pin caught the planted mistake {mutation}"
 
 
 @pytest.mark.parametrize("mutation", ["swap_gate_up", "silu_sign", "transposed_recv",
