@@ -63,7 +63,7 @@ __all__ = [
     "rank_counts", "send_recv_counts", "permute", "unpermute",
     "expert_offsets", "grouped_matmul", "block_forward", "ep_mc2_forward_emulated",
     "brute_force_token", "quant_block_forward", "requant_rows", "mm_reduce_scatter",
-    "ORACLE_UNPINNED",
+    "silu_grad", "block_backward", "ORACLE_UNPINNED",
 ]
 
 # Functions with no pin independent of this file (see tests/test_oracle_pins.py).
@@ -293,6 +293,84 @@ def ep_mc2_forward_emulated(x, w1, w2, sel, probs, E, W, h_dtype=None):
         out[s * Tl:(s + 1) * Tl] = unpermute(back, perm_idx[s],
                                              probs[s * Tl:(s + 1) * Tl], valid_rows=nvalid)  # step 10
     return out
+
+
+# ---------------------------------------------------------------------------
+# Backward of the block [EP]: the gradient of sum(out * dout) with respect to
+# x, w1, w2 and probs, taken step by step back through steps 10 .. 6.
+# (The pages name the fused operators AllToAllGroupedMatmul /
+# GroupedMatmulAllToAll; their backward is the chain rule of the same flow.)
+# ---------------------------------------------------------------------------
+def silu_grad(a: np.ndarray) -> np.ndarray:
+    """d silu(a) / da = s(a) * (1 + a * (1 - s(a))), s the logistic function."""
+    a = np.asarray(a, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        s = 1.0 / (1.0 + np.exp(-a))
+    return s * (1.0 + a * (1.0 - s))
+
+
+def block_backward(x, w1, w2, sel, probs, dout, E, W, h_dtype=None):
+    """Gradients of L = sum(block_forward(...).out * dout).
+
+    Reading: h enters fc2 as materialised (rounded to h_dtype); its rounding
+    passes gradients through unchanged (derivative 1), so dh flows back into
+    the SwiGLU at the unrounded pre-activation G.  Ids outside [0, E) take no
+    part in the block and get no gradient (their dprobs is 0).
+
+    step 10  out[t] = sum_j probs[t, j] * Y[p(t, j)]
+             -> dY[p] = probs[t, j] * dout[t];  dprobs[t, j] = Y[p] . dout[t]
+    step 9   Y_e = h_e @ w2[e]   -> dh_e = dY_e @ w2[e]^T;  dw2[e] = h_e^T @ dY_e
+    step 8   h = silu(a) * b     -> da = dh * b * silu'(a);  db = dh * silu(a)
+    step 7   G_e = Xp_e @ w1[e]  -> dXp_e = dG_e @ w1[e]^T;  dw1[e] = Xp_e^T @ dG_e
+    step 6   Xp[p] = x[t(p)]     -> dx[t] = sum over valid slots of dXp[p(t, j)]
+
+    Returns a dict with dx [T, H], dw1 [E, H, 2I], dw2 [E, I, H], dprobs [T, k]
+    and the intermediates (g, h, y, dy, dh, dg, dxp) in permuted-row order."""
+    T, k = sel.shape
+    x = np.asarray(x, dtype=np.float64).reshape(T, -1)
+    H = x.shape[1]
+    I = w2.shape[1]
+    num_global = rank_counts(sel, E, W)
+    offsets = expert_offsets(num_global)
+    permuted, src = permute(x, sel, E)
+    nvalid = int(offsets[-1])
+    tot = num_global.sum(axis=0)
+    xp = permuted[:nvalid]
+    g = grouped_matmul(xp, w1, tot)
+    h = _ROUND[h_dtype](swiglu(g))
+    y = grouped_matmul(h, w2, tot)
+    tok, slot = src[:nvalid] // k, src[:nvalid] % k
+    dout = np.asarray(dout, dtype=np.float64)
+    p_rows = probs.astype(np.float64)[tok, slot]
+    dy = p_rows[:, None] * dout[tok]                                    # step 10
+    dprobs = np.zeros((T, k))
+    dprobs[tok, slot] = np.einsum("ph,ph->p", y, dout[tok])
+    dh = np.zeros((nvalid, I))
+    dw2 = np.zeros((E, I, H))
+    dg = np.zeros((nvalid, 2 * I))
+    dxp = np.zeros((nvalid, H))
+    dw1 = np.zeros((E, H, 2 * I))
+    for e in range(E):
+        a0, a1 = int(offsets[e]), int(offsets[e + 1])
+        if a0 == a1:
+            continue
+        dh[a0:a1] = dy[a0:a1] @ w2[e].T                                 # step 9
+        dw2[e] = h[a0:a1].T @ dy[a0:a1]
+    gate, up = g[:, :I], g[:, I:]
+    dg[:, :I] = dh * up * silu_grad(gate)                               # step 8
+    dg[:, I:] = dh * silu(gate)
+    for e in range(E):
+        a0, a1 = int(offsets[e]), int(offsets[e + 1])
+        if a0 == a1:
+            continue
+        dxp[a0:a1] = dg[a0:a1] @ w1[e].T                                # step 7
+        dw1[e] = xp[a0:a1].T @ dg[a0:a1]
+    dx = np.zeros((T, H))
+    for j in range(k):                                                  # step 6
+        m = slot == j
+        np.add.at(dx, tok[m], dxp[m])
+    return dict(dx=dx, dw1=dw1, dw2=dw2, dprobs=dprobs, g=g, h=h, y=y, dy=dy, dh=dh,
+                dg=dg, dxp=dxp, offsets=offsets, permute_src=src)
 
 
 def brute_force_token(x_t, w1, w2, sel_t, probs_t, E, h_dtype=None):

@@ -296,6 +296,116 @@ def test_requant_rows_properties():
     assert np.all(err <= hs[:, None] * (0.5 + 1e-5))
 
 
+# ---------------------------------------------------------------- backward
+def _bwd_case(T, H, I, E, k, W, seed):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, H))
+    w1 = rng.standard_normal((E, H, 2 * I)) * 0.3
+    w2 = rng.standard_normal((E, I, H)) * 0.3
+    sel = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    probs = rng.uniform(0.1, 1.0, (T, k)).astype(np.float32)
+    dout = rng.standard_normal((T, H))
+    return x, w1, w2, sel, probs, dout
+
+
+def _torch_token_forward(x, w1, w2, sel, probs, E):
+    """The block written per token with torch ops (no permutation, no groups):
+    out[t] = sum over valid slots of probs[t, j] * SwiGLU(x[t] @ w1[e]) @ w2[e]."""
+    T, k = sel.shape
+    I = w2.shape[1]
+    rows = []
+    for t in range(T):
+        acc = torch.zeros(x.shape[1], dtype=torch.float64)
+        for j in range(k):
+            e = int(sel[t, j])
+            if not 0 <= e < E:
+                continue
+            g = x[t] @ w1[e]
+            acc = acc + probs[t, j] * ((torch.nn.functional.silu(g[:I]) * g[I:]) @ w2[e])
+        rows.append(acc)
+    return torch.stack(rows)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_backward_matches_torch_autograd(seed):
+    T, H, I, E, k, W = 6, 8, 4, 4, 2, 2
+    x, w1, w2, sel, probs, dout = _bwd_case(T, H, I, E, k, W, seed)
+    sel[2, 1] = 9  # one invalid slot: no gradient through it
+    r = orc.block_backward(x, w1, w2, sel, probs, dout, E, W)
+    tx, tw1, tw2 = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (x, w1, w2))
+    tp = torch.tensor(probs.astype(np.float64), requires_grad=True)
+    out = _torch_token_forward(tx, tw1, tw2, sel, tp, E)
+    (out * torch.from_numpy(dout)).sum().backward()
+    for name, t in (("dx", tx), ("dw1", tw1), ("dw2", tw2), ("dprobs", tp)):
+        assert np.allclose(r[name], t.grad.numpy(), rtol=1e-10, atol=1e-12), name
+    assert r["dprobs"][2, 1] == 0.0
+
+
+def test_backward_by_finite_differences():
+    T, H, I, E, k, W = 4, 6, 3, 3, 2, 1
+    x, w1, w2, sel, probs, dout = _bwd_case(T, H, I, E, k, W, 5)
+    r = orc.block_backward(x, w1, w2, sel, probs, dout, E, W)
+
+    def loss(x_, w1_, w2_, p_):
+        return float((orc.block_forward(x_, w1_, w2_, sel, p_, E, W)["out"] * dout).sum())
+    eps = 1e-6
+    rng = np.random.default_rng(6)
+    for name, arr in (("dx", x), ("dw1", w1), ("dw2", w2), ("dprobs", probs)):
+        for _ in range(3):
+            idx = tuple(int(rng.integers(0, n)) for n in arr.shape)
+            args = [x, w1, w2, probs.astype(np.float64)]
+            pos = {"dx": 0, "dw1": 1, "dw2": 2, "dprobs": 3}[name]
+            plus, minus = [a.copy() for a in args], [a.copy() for a in args]
+            plus[pos][idx] += eps
+            minus[pos][idx] -= eps
+            fd = (loss(*plus) - loss(*minus)) / (2 * eps)
+            assert math.isclose(r[name][idx], fd, rel_tol=1e-5, abs_tol=1e-7), (name, idx)
+
+
+def test_backward_prob_gradient_identity():
+    """out is linear in probs: sum_j probs[t, j] * dprobs[t, j] = out[t] . dout[t]."""
+    x, w1, w2, sel, probs, dout = _bwd_case(8, 8, 4, 4, 3, 2, 7)
+    r = orc.block_backward(x, w1, w2, sel, probs, dout, 4, 2)
+    out = orc.block_forward(x, w1, w2, sel, probs, 4, 2)["out"]
+    lhs = (probs.astype(np.float64) * r["dprobs"]).sum(axis=1)
+    assert np.allclose(lhs, (out * dout).sum(axis=1), rtol=1e-12, atol=1e-12)
+
+
+def test_silu_grad_pins():
+    a = torch.linspace(-30, 30, 241, dtype=torch.float64, requires_grad=True)
+    torch.nn.functional.silu(a).sum().backward()
+    assert np.allclose(orc.silu_grad(a.detach().numpy()), a.grad.numpy(), rtol=1e-12, atol=1e-14)
+    assert orc.silu_grad(np.array([0.0]))[0] == 0.5
+
+
+@pytest.mark.parametrize("mutation", ["silu_grad_sign", "no_prob_in_dy", "transposed_dw2"])
+def test_planted_backward_mistakes_are_caught(monkeypatch, mutation):
+    if mutation == "silu_grad_sign":
+        real = orc.silu_grad
+        monkeypatch.setattr(orc, "silu_grad", lambda a: real(-np.asarray(a)))
+    elif mutation == "no_prob_in_dy":
+        real = orc.block_backward
+
+        def bad(x, w1, w2, sel, probs, dout, E, W, h_dtype=None):
+            return real(x, w1, w2, sel, np.ones_like(probs), dout, E, W, h_dtype)
+        monkeypatch.setattr(orc, "block_backward", bad)
+    else:
+        real = orc.block_backward
+
+        def bad(x, w1, w2, sel, probs, dout, E, W, h_dtype=None):
+            r = real(x, w1, w2, sel, probs, dout, E, W, h_dtype)
+            r["dw2"] = r["dw2"][:, ::-1, :]
+            return r
+        monkeypatch.setattr(orc, "block_backward", bad)
+    failures = 0
+    for fn in (lambda: test_backward_matches_torch_autograd(0), test_backward_by_finite_differences):
+        try:
+            fn()
+        except (AssertionError, ValueError, IndexError):
+            failures += 1
+    assert failures > 0, f"no pin caught the planted mistake {mutation}"
+
+
 # ---------------------------------------------------- quantised matmul + reduce-scatter
 def _mmrs_inputs(W, m, k, n, seed):
     rng = np.random.default_rng(seed)
