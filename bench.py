@@ -407,6 +407,125 @@ def run_cuda(args):
         dist.barrier()
 
 
+def run_backward(args):
+    """Backward of the block (bf16): one mc2_moe_backward per step (G recomputed,
+    both dgrads, SwiGLU backward, the unpermute-sum of dx, both weight
+    gradients), with the counts and the transposed weights prepared once.
+    Metric: tokens/s of the backward; roofline on the call's tensor work
+    (16*R*H*I flops, of which 4*R*H*I recompute G)."""
+    import torch
+    from moe_expert_dispatch_histc_gb300 import binding as B, block as blk
+    from moe_expert_dispatch_histc_gb300.build import build
+    build()
+    B.lib()
+    wl = WORKLOADS[args.workload]
+    if wl.act != "bf16":
+        raise SystemExit("--op backward: bf16 workloads only")
+    inp = make_inputs(wl, 0)
+    d = blk.inputs_to_device(inp, wl)
+    b = blk.alloc_buffers(wl)
+    shape = blk.shape_of(wl)
+    stream = torch.cuda.current_stream()
+    B.mc2_moe_counts(shape, d["sel"], b.cnt, b.recv, b.offsets, b.permute_src, b.unpermute_dst,
+                     b.ws, b.dev_status, stream=stream)
+    w1t = torch.empty(wl.E, 2 * wl.I, wl.H, dtype=torch.bfloat16, device="cuda")
+    w2t = torch.empty(wl.E, wl.H, wl.I, dtype=torch.bfloat16, device="cuda")
+    B.mc2_transpose_weights(shape, d["w1"], d["w2"], w1t, w2t, stream=stream)
+    rng = np.random.default_rng(1)
+    dout_np = rng.standard_normal((wl.T, wl.H)).astype(np.float32)
+    dout = torch.from_numpy(dout_np).cuda().to(torch.bfloat16)
+    ws = torch.empty(B.mc2_backward_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    dx = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device="cuda")
+    dw1 = torch.empty(wl.E, wl.H, 2 * wl.I, device="cuda")
+    dw2 = torch.empty(wl.E, wl.I, wl.H, device="cuda")
+    dprobs = torch.empty(wl.T, wl.k, device="cuda")
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
+
+    def call():
+        B.mc2_moe_backward(shape, d["x"], d["probs"], d["w1"], w1t, w2t, dout, b.offsets,
+                           b.permute_src, b.unpermute_dst, dx, dw1, dw2, dprobs, ws,
+                           b.dev_status, stream=stream)
+        return B.mc2_last_launch_count()
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.2)
+    evs, launches = [], 0
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        launches += call()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if int(b.dev_status.item()) != 0:
+        raise RuntimeError(f"device status {int(b.dev_status.item())}")
+    ms = float(np.mean([a.elapsed_time(c) for a, c in evs]))
+    value = wl.T / (ms / 1e3)
+    flops = 16.0 * wl.R * wl.H * wl.I
+    peaks, src = _peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (ms / 1e3) / 1e12
+    # end to end: x, ids, probs and dout in from pinned host memory; dx, dprobs,
+    # dw1, dw2 back, every step (counts included: the ids arrive with the step)
+    host = {n: d[n].cpu().pin_memory() for n in ("x", "sel", "probs")}
+    h_dout = dout.cpu().pin_memory()
+    outs = [dx, dprobs, dw1, dw2]
+    h_outs = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    e2e_steps = max(3, args.steps // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for n, h in host.items():
+            d[n].copy_(h, non_blocking=True)
+        dout.copy_(h_dout, non_blocking=True)
+        B.mc2_moe_counts(shape, d["sel"], b.cnt, b.recv, b.offsets, b.permute_src,
+                         b.unpermute_dst, b.ws, b.dev_status, stream=stream)
+        call()
+        for h, o in zip(h_outs, outs):
+            h.copy_(o, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    bi = sum(h.numel() * h.element_size() for h in host.values()) + h_dout.numel() * 2
+    bo = sum(h.numel() * h.element_size() for h in h_outs)
+    # CPU oracle on a bounded sample of the same workload
+    from oracle import mc2_oracle as orc
+    x64, w1, w2 = (as_f64(inp[n], wl.act) for n in ("x", "w1", "w2"))
+    Ts = min(wl.T, max(wl.W, (512 // wl.W) * wl.W))
+    t0 = time.perf_counter()
+    orc.block_backward(x64[:Ts], w1, w2, inp["sel"][:Ts], inp["probs"][:Ts],
+                       dout_np[:Ts].astype(np.float64), wl.E, wl.W, h_dtype="bf16")
+    cpu_s = time.perf_counter() - t0
+    line = {
+        "metric": "MoE expert-block backward tokens/s (1 GPU)", "value": value, "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {**_config(wl, l2="flushed (256 MB write) between steps"), "op": "backward"},
+        "tflops": achieved,
+        "roofline": {"kernel": "the whole backward call (10 launches; 16*R*H*I flops incl. the "
+                               "G recompute)", "bound": "tensor", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"{src} bf16_tflops (burst)", "traffic": None},
+        "e2e": {"value": wl.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo, "steps": e2e_steps,
+                "mode": "inputs and dout in, counts + backward, dx/dprobs/dw1/dw2 out, serially"},
+        "cpu_baseline": {"value": Ts / cpu_s, "unit": "tokens/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"first {Ts} of {wl.T} tokens, all experts (numpy float64 "
+                                   f"chain rule), {cpu_s:.1f} s"},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 MMRS = {"W": 8, "m": 4096, "k": 1024, "n": 4096}   # TP over 8 ranks of a K=8192 projection
 
 
@@ -519,12 +638,19 @@ def main():
     ap.add_argument("--path", default="fused", choices=["fused", "unfused"],
                     help="unfused: the non-fused baseline (materialised permute, plain grouped "
                          "fc1), bf16 workloads only")
-    ap.add_argument("--op", default="block", choices=["block", "mm_reduce_scatter"],
+    ap.add_argument("--op", default="block", choices=["block", "backward", "mm_reduce_scatter"],
                     help="mm_reduce_scatter: the quantised matmul + reduce-scatter over "
                          "logical ranks (a separate line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.op == "backward":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "--op backward has its CPU "
+                              "oracle in the cpu_baseline of the cuda line"}))
+            return
+        run_backward(args)
+        return
     if args.op == "mm_reduce_scatter":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "--op mm_reduce_scatter has "

@@ -198,6 +198,34 @@ mc2_status_t mc2_gmm_swiglu(const mc2_shape_t* s, const void* xp, const void* w1
                             const int32_t* offsets, void* h, int32_t* dev_status, void* stream);
 
 /*
+ * Backward of the block (bf16): the gradients of L = sum(out * dout) with
+ * respect to x, w1, w2 and probs, by the chain rule back through the steps of
+ * "NPU Training Operators - MC2", section "Execution path" (10 back to 6; the
+ * fused AllToAllGroupedMatmul / GroupedMatmulAllToAll operators of the pages
+ * wrap forward and backward).  Ids outside [0, E) get no gradient (their
+ * dprobs is 0).  The forward's h passes through its bf16 rounding with
+ * derivative 1; G = x[t] @ w1[e] is recomputed in bf16.
+ *
+ * mc2_transpose_weights -- w1t [E, 2I, H] = w1 transposed per expert, w2t
+ *   [E, H, I] = w2 transposed, bf16 [dev]; once whenever the weights change.
+ * mc2_moe_backward -- inputs: x [T, H] bf16, probs [T, k] fp32, w1 [E, H, 2I],
+ *   w1t, w2t (from mc2_transpose_weights), dout [T, H] bf16, and offsets,
+ *   permute_src, unpermute_dst of mc2_moe_counts for the same ids.  Outputs:
+ *   dx [T, H] bf16, dw1 [E, H, 2I] fp32, dw2 [E, I, H] fp32 (zero for experts
+ *   without rows), dprobs [T, k] fp32.  ws: mc2_backward_workspace_bytes(s)
+ *   bytes [dev], 256-byte aligned.  act = out = MC2_BF16 only (else
+ *   MC2_ERR_UNSUPPORTED).  Pointer rules, errors and dev_status as above.
+ */
+size_t mc2_backward_workspace_bytes(const mc2_shape_t* s);
+mc2_status_t mc2_transpose_weights(const mc2_shape_t* s, const void* w1, const void* w2,
+                                   void* w1t, void* w2t, void* stream);
+mc2_status_t mc2_moe_backward(const mc2_shape_t* s, const void* x, const float* probs,
+                              const void* w1, const void* w1t, const void* w2t, const void* dout,
+                              const int32_t* offsets, const int32_t* permute_src,
+                              const int32_t* unpermute_dst, void* dx, float* dw1, float* dw2,
+                              float* dprobs, void* ws, int32_t* dev_status, void* stream);
+
+/*
  * Quantised matmul + reduce-scatter over W logical tensor-parallel ranks, the
  * operation of "torch_npu.npu_mm_reduce_scatter_base" (Ascend op-plugin docs,
  * sections "Function description" and "Parameters") in its quantised form:

@@ -37,7 +37,7 @@ namespace mc2 {
 
 template <int MODE>
 struct Roles {
-  static constexpr int kGatherWarps = MODE == MODE_FC1 ? 4 : 0;
+  static constexpr int kGatherWarps = MODE == MODE_FC1 || MODE == MODE_FC1_PRE ? 4 : 0;
   static constexpr int kThreads = (6 + kGatherWarps) * 32;
 };
 
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
   constexpr int KK_B = (32 / ES) * 128;      // B bytes per UMMA K step
   constexpr bool BKM = TR::B_KMAJOR;
   constexpr uint32_t IDESC = instr_desc(TR::FMT, false, !BKM, BM, BN);
-  constexpr bool GATHER = MODE == MODE_FC1;
+  constexpr bool GATHER = MODE == MODE_FC1 || MODE == MODE_FC1_PRE;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -304,6 +304,49 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           // the previous store out of this warp's staging buffer has read it
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
+          if constexpr (MODE == MODE_FC1_PRE) {
+            // gate then up columns of G [R, 2I], bf16, as they leave the MMA
+#pragma unroll 1
+            for (int part = 0; part < 2; ++part) {
+              if (part) {
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+              }
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                uint32_t v[32];
+                tmem_ld32(tbase + part * (BN / 2) + gi * 64 + half * 32, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                  const int ch = half * 4 + w;
+                  *reinterpret_cast<uint4*>(stage + row_off + ((ch ^ (lane & 7)) << 4)) =
+                      make_uint4(pack_bf16x2(__uint_as_float(v[8 * w]), __uint_as_float(v[8 * w + 1])),
+                                 pack_bf16x2(__uint_as_float(v[8 * w + 2]), __uint_as_float(v[8 * w + 3])),
+                                 pack_bf16x2(__uint_as_float(v[8 * w + 4]), __uint_as_float(v[8 * w + 5])),
+                                 pack_bf16x2(__uint_as_float(v[8 * w + 6]), __uint_as_float(v[8 * w + 7])));
+                }
+              }
+              const int gcol = part * p.out_cols + col0;
+              if (wrows == 32) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                  tma_store_2d(&tmOut, stage, gcol, grow0);
+                  bulk_commit();
+                }
+              } else if (lane < wrows) {
+                uint4* dst = reinterpret_cast<uint4*>(
+                    static_cast<__nv_bfloat16*>(p.out) +
+                    static_cast<int64_t>(grow0 + lane) * 2 * p.out_cols + gcol);
+#pragma unroll
+                for (int w = 0; w < 8; ++w)
+                  dst[w] = *reinterpret_cast<const uint4*>(stage + row_off + ((w ^ (lane & 7)) << 4));
+              }
+              __syncwarp();
+            }
+            continue;
+          }
           if (MODE != MODE_FC2 && ES == 2) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -421,7 +464,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
   constexpr int KK_B = (32 / ES) * 128;
   constexpr bool BKM = TR::B_KMAJOR;
   constexpr uint32_t IDESC = instr_desc(TR::FMT, false, !BKM, 2 * BM, BN);
-  constexpr bool GATHER = MODE == MODE_FC1;
+  constexpr bool GATHER = MODE == MODE_FC1 || MODE == MODE_FC1_PRE;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -947,7 +990,7 @@ static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
     p.out_cols = s.I;
     ok = (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.H, 2ull * s.I, s.E, TR::BK, BN / 2)
                        : encode_b_blocked(&tB, g.b, s.H, 2ull * s.I, s.E, 2, TR::BK, NB1 / 2, 2)) &&
-         encode_2d(&tOut, dt, ES, g.out, s.I, R, 128 / ES, 32);
+         encode_2d(&tOut, dt, ES, g.out, MODE == MODE_FC1_PRE ? 2ull * s.I : s.I, R, 128 / ES, 32);
     if (MODE == MODE_FC1_ROWS)  // already permuted rows [R, H]: plain TMA tiles
       ok = ok && encode_2d(&tA, dt, ES, g.a, s.H, R, 128 / ES, BM);
     else
@@ -1079,6 +1122,9 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
       e = g.a_elem_bytes == 2 ? launch_pair<MODE_FC1, 2>(g, st) : launch_pair<MODE_FC1, 4>(g, st);
     else
       e = g.a_elem_bytes == 2 ? launch_one<MODE_FC1, 2>(g, st) : launch_one<MODE_FC1, 4>(g, st);
+  } else if (g.mode == MODE_FC1_PRE) {  // bf16, single CTAs
+    if (g.a_elem_bytes != 2) return cudaErrorInvalidValue;
+    e = launch_one<MODE_FC1_PRE, 2>(g, st);
   } else if (g.mode == MODE_FC1_ROWS) {  // bf16 only
     if (g.a_elem_bytes != 2) return cudaErrorInvalidValue;
     e = pairs ? launch_pair<MODE_FC1_ROWS, 2>(g, st) : launch_one<MODE_FC1_ROWS, 2>(g, st);

@@ -28,8 +28,9 @@ CountsGeom counts_geom(const mc2_shape_t& s);
 // Grouped-GEMM modes.  MODE_FC1: fc1 + SwiGLU with the permute folded in
 // (token rows gathered); MODE_FC2: fc2 -> scaled fp16 rows; MODE_FC1_ROWS:
 // fc1 + SwiGLU on rows that are already permuted (the non-fused baseline
-// path; plain TMA A tiles).
-enum { MODE_FC1 = 0, MODE_FC2 = 1, MODE_FC1_ROWS = 2 };
+// path; plain TMA A tiles); MODE_FC1_PRE: fc1 with the permute folded in,
+// writing the pre-activation gate|up rows G [R, 2I] in bf16 (the backward).
+enum { MODE_FC1 = 0, MODE_FC2 = 1, MODE_FC1_ROWS = 2, MODE_FC1_PRE = 3 };
 
 // Workspace layout (byte offsets from ws).
 struct WsLayout {
@@ -107,6 +108,10 @@ struct GemmArgs {
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st);
 cudaError_t launch_permute_rows(const mc2_shape_t& s, const void* x, const int32_t* permute_src,
                                 void* xp, cudaStream_t st);
+// dW [E, M, N] fp32 = per expert A_e^T @ B_e over its permuted rows; A [R, M],
+// B [R, N] bf16 (wgrad.cu).
+cudaError_t launch_wgrad(const void* a, const void* b, const int32_t* offsets, int64_t R, int E,
+                         int M, int N, float* dw, int32_t* dev_status, cudaStream_t st);
 
 // int8 path (bf16 tensor cores holding int8 values, exact int32 sums)
 struct QArgs {

@@ -1,0 +1,93 @@
+"""Backward of the block on the GPU against the CPU oracle (float64 chain rule
+of the forward, pinned by torch autograd and finite differences).
+
+Tolerance: the GPU path rounds G, dG, probs*h and the transposed weights to
+bf16 (relative 2^-9 each) and keeps the gathered gradient rows as scaled
+fp16 (2^-11) before the next matmul, so its gradients carry a few bf16 ulps:
+max|err| <= 2e-2 * max|ref| and sum|err| / sum|ref| <= 1e-2 per output
+(dx, dw1, dw2, dprobs)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import mc2_oracle as orc
+from moe_expert_dispatch_histc_gb300 import binding as B, block as blk
+from moe_expert_dispatch_histc_gb300.workloads import (Workload, as_f64, bf16_bits_to_f32,
+                                                       f32_to_bf16_bits, make_inputs)
+
+from gpu_util import ensure_built, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _tol(got, ref, what, max_rel=2e-2, mean_rel=1e-2):
+    ok, a, m = orc.bf16_tolerance_ok(got, ref, max_rel=max_rel, mean_rel=mean_rel)
+    assert ok, f"{what}: max|err|/max|ref| = {a:.3e}, mean rel = {m:.3e}"
+    return a, m
+
+
+def run_backward(wl, seed=0, sel=None):
+    ensure_built()
+    inp = make_inputs(wl, seed)
+    if sel is not None:
+        inp["sel"] = np.ascontiguousarray(sel.astype(np.int32))
+    rng = np.random.default_rng(seed + 100)
+    dout_bits = f32_to_bf16_bits(rng.standard_normal((wl.T, wl.H)).astype(np.float32))
+    d = blk.inputs_to_device(inp, wl)
+    b = blk.alloc_buffers(wl)
+    shape = blk.shape_of(wl)
+    B.mc2_moe_counts(shape, d["sel"], b.cnt, b.recv, b.offsets, b.permute_src, b.unpermute_dst,
+                     b.ws, b.dev_status)
+    w1t = torch.empty(wl.E, 2 * wl.I, wl.H, dtype=torch.bfloat16, device="cuda")
+    w2t = torch.empty(wl.E, wl.H, wl.I, dtype=torch.bfloat16, device="cuda")
+    B.mc2_transpose_weights(shape, d["w1"], d["w2"], w1t, w2t)
+    dout = torch.from_numpy(dout_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    ws = torch.empty(B.mc2_backward_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    dx = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device="cuda")
+    dw1 = torch.empty(wl.E, wl.H, 2 * wl.I, dtype=torch.float32, device="cuda")
+    dw2 = torch.empty(wl.E, wl.I, wl.H, dtype=torch.float32, device="cuda")
+    dprobs = torch.empty(wl.T, wl.k, dtype=torch.float32, device="cuda")
+    B.mc2_moe_backward(shape, d["x"], d["probs"], d["w1"], w1t, w2t, dout, b.offsets, b.permute_src,
+                       b.unpermute_dst, dx, dw1, dw2, dprobs, ws, b.dev_status)
+    torch.cuda.synchronize()
+    # transposes are exact copies
+    assert torch.equal(w1t.view(torch.int16), d["w1"].transpose(1, 2).contiguous().view(torch.int16))
+    assert torch.equal(w2t.view(torch.int16), d["w2"].transpose(1, 2).contiguous().view(torch.int16))
+    x, w1, w2 = (as_f64(inp[n], wl.act) for n in ("x", "w1", "w2"))
+    ref = orc.block_backward(x, w1, w2, inp["sel"], inp["probs"],
+                             bf16_bits_to_f32(dout_bits).astype(np.float64), wl.E, wl.W,
+                             h_dtype="bf16")
+    got = dict(dx=to_np(dx), dw1=to_np(dw1), dw2=to_np(dw2), dprobs=to_np(dprobs))
+    return got, ref, int(b.dev_status.item())
+
+
+BWD = [
+    Workload("bwd_small", 256, 256, 128, 8, 2, 2, "bf16"),
+    Workload("bwd_ragged", 384, 320, 192, 6, 3, 3, "bf16"),       # partial tiles in M and N
+    Workload("bwd_many_experts", 512, 512, 256, 32, 4, 4, "bf16"),
+    Workload("bwd_multi_tile", 2048, 1024, 512, 16, 4, 4, "bf16"),  # ~512 rows per expert
+]
+
+
+@pytest.mark.parametrize("wl", BWD, ids=lambda w: w.name)
+def test_backward_parity(wl):
+    got, ref, status = run_backward(wl, seed=1)
+    assert status == 0
+    for name in ("dx", "dw1", "dw2", "dprobs"):
+        _tol(got[name], ref[name], name)
+
+
+def test_backward_invalid_ids_and_empty_experts():
+    """Invalid slots get dprobs 0 and no gradient; experts without rows get zero
+    weight gradients."""
+    wl = Workload("bwd_sparse", 256, 256, 128, 8, 2, 2, "bf16")
+    rng = np.random.default_rng(3)
+    sel = np.stack([rng.choice([1, 5], 2, replace=False) for _ in range(wl.T)]).astype(np.int32)
+    sel[7, 0], sel[100, 1] = -1, 8
+    got, ref, status = run_backward(wl, seed=3, sel=sel)
+    assert status & B.MC2_DEV_BAD_EXPERT_ID
+    assert got["dprobs"][7, 0] == 0.0 and got["dprobs"][100, 1] == 0.0
+    for e in (0, 2, 3, 4, 6, 7):
+        assert not got["dw1"][e].any() and not got["dw2"][e].any()
+    for name in ("dx", "dw1", "dw2", "dprobs"):
+        _tol(got[name], ref[name], name)
