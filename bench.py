@@ -175,6 +175,23 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(value: float, world: int, device="cuda") -> float:
+    """The job's time of a region timed on every rank: the slowest rank's."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput of weak-scaled replicas: every rank's tokens over
+    the slowest rank's time."""
+    return tokens_per_rank * world * steps / (max_ms / 1e3)
+
+
 def _config(wl, l2):
     return {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
             "W": wl.W, "act": wl.act, "routing": wl.routing, "l2": l2,
@@ -336,11 +353,8 @@ def run_cuda(args):
                     for e in events])  # ms per segment, in the order of `segments`
     segi = {name: i for i, (name, _) in enumerate(segments)}
     total_ms = float(seg.sum())
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = wl.T * world * args.steps / (total_ms / 1e3)
+    total_ms = max_over_ranks(total_ms, world)
+    value = job_tokens_per_s(wl.T, world, args.steps, total_ms)
 
     # e2e: every step copies its inputs (x, ids, probs; int8 also the token
     # scales) from pinned host memory and reads its output back to pinned host
@@ -355,11 +369,8 @@ def run_cuda(args):
     else:
         e2e_run = lambda dd, bb: blk.run_block(wl, dd, bb, stream=stream)  # noqa: E731
     e2e_ms, bi, bo = e2e_pipelined(wl, d, b, stream, e2e_steps, e2e_run)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_val = wl.T * world * e2e_steps / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    e2e_val = job_tokens_per_s(wl.T, world, e2e_steps, e2e_ms)
 
     if rank != 0:
         dist.barrier() if world > 1 else None
