@@ -419,11 +419,12 @@ def run_cuda(args):
 
 
 def run_backward(args):
-    """Backward of the block (bf16): one mc2_moe_backward per step (G recomputed,
-    both dgrads, SwiGLU backward, the unpermute-sum of dx, both weight
-    gradients), with the counts and the transposed weights prepared once.
+    """Backward of the block (bf16): one mc2_moe_backward per step (both
+    dgrads, SwiGLU backward, the unpermute-sum of dx, both weight gradients;
+    G as the training forward kept it, or recomputed with --recompute-g), with
+    the counts, the kept G and the transposed weights prepared once.
     Metric: tokens/s of the backward; roofline on the call's tensor work
-    (16*R*H*I flops, of which 4*R*H*I recompute G)."""
+    (12*R*H*I flops, 16*R*H*I with the recompute)."""
     import torch
     from moe_expert_dispatch_histc_gb300 import binding as B, block as blk
     from moe_expert_dispatch_histc_gb300.build import build
@@ -446,6 +447,12 @@ def run_backward(args):
     dout_np = rng.standard_normal((wl.T, wl.H)).astype(np.float32)
     dout = torch.from_numpy(dout_np).cuda().to(torch.bfloat16)
     ws = torch.empty(B.mc2_backward_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    g_kept = None
+    if not args.recompute_g:   # the training forward keeps G; done once, outside the timing
+        g_kept = torch.empty(wl.R, 2 * wl.I, dtype=torch.bfloat16, device="cuda")
+        h_tmp = torch.empty(wl.R, wl.I, dtype=torch.bfloat16, device="cuda")
+        B.mc2_alltoallv_gmm_keep(shape, d["x"], d["w1"], b.offsets, b.permute_src, h_tmp, g_kept,
+                                 b.dev_status, stream=stream)
     dx = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device="cuda")
     dw1 = torch.empty(wl.E, wl.H, 2 * wl.I, device="cuda")
     dw2 = torch.empty(wl.E, wl.I, wl.H, device="cuda")
@@ -455,7 +462,7 @@ def run_backward(args):
     def call():
         B.mc2_moe_backward(shape, d["x"], d["probs"], d["w1"], w1t, w2t, dout, b.offsets,
                            b.permute_src, b.unpermute_dst, dx, dw1, dw2, dprobs, ws,
-                           b.dev_status, stream=stream)
+                           b.dev_status, stream=stream, g=g_kept)
         return B.mc2_last_launch_count()
     for _ in range(args.warmup):
         flush.zero_()
@@ -478,7 +485,7 @@ def run_backward(args):
         raise RuntimeError(f"device status {int(b.dev_status.item())}")
     ms = float(np.mean([a.elapsed_time(c) for a, c in evs]))
     value = wl.T / (ms / 1e3)
-    flops = 16.0 * wl.R * wl.H * wl.I
+    flops = (12.0 if g_kept is not None else 16.0) * wl.R * wl.H * wl.I
     peaks, src = _peaks()
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (ms / 1e3) / 1e12
@@ -518,10 +525,12 @@ def run_backward(args):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {**_config(wl, l2="flushed (256 MB write) between steps"), "op": "backward"},
+        "config": {**_config(wl, l2="flushed (256 MB write) between steps"), "op": "backward",
+                   "G": "recomputed" if g_kept is None else "kept by mc2_alltoallv_gmm_keep"},
         "tflops": achieved,
-        "roofline": {"kernel": "the whole backward call (10 launches; 16*R*H*I flops incl. the "
-                               "G recompute)", "bound": "tensor", "achieved": achieved,
+        "roofline": {"kernel": "the whole backward call (12*R*H*I flops of gradients, "
+                               "+4*R*H*I when G is recomputed)", "bound": "tensor",
+                     "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": f"{src} bf16_tflops (burst)", "traffic": None},
         "e2e": {"value": wl.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
@@ -649,6 +658,8 @@ def main():
     ap.add_argument("--path", default="fused", choices=["fused", "unfused"],
                     help="unfused: the non-fused baseline (materialised permute, plain grouped "
                          "fc1), bf16 workloads only")
+    ap.add_argument("--recompute-g", action="store_true",
+                    help="--op backward: recompute G instead of taking the training forward's")
     ap.add_argument("--op", default="block", choices=["block", "backward", "mm_reduce_scatter"],
                     help="mm_reduce_scatter: the quantised matmul + reduce-scatter over "
                          "logical ranks (a separate line)")

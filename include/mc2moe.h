@@ -208,7 +208,14 @@ mc2_status_t mc2_gmm_swiglu(const mc2_shape_t* s, const void* xp, const void* w1
  *
  * mc2_transpose_weights -- w1t [E, 2I, H] = w1 transposed per expert, w2t
  *   [E, H, I] = w2 transposed, bf16 [dev]; once whenever the weights change.
+ * mc2_alltoallv_gmm_keep -- the training form of mc2_alltoallv_gmm (bf16):
+ *   also keeps the pre-activation rows g [T*k, 2I] bf16 [dev] (gate | up of
+ *   every valid permuted row) for the backward; h [T*k, I] is then
+ *   bf16(silu(gate) * up) of those bf16 rows.  Same rules as
+ *   mc2_alltoallv_gmm otherwise.
  * mc2_moe_backward -- inputs: x [T, H] bf16, probs [T, k] fp32, w1 [E, H, 2I],
+ *   g (the rows kept by mc2_alltoallv_gmm_keep, or NULL: then they are
+ *   recomputed from x and w1, bitwise the same),
  *   w1t, w2t (from mc2_transpose_weights), dout [T, H] bf16, and offsets,
  *   permute_src, unpermute_dst of mc2_moe_counts for the same ids.  Outputs:
  *   dx [T, H] bf16, dw1 [E, H, 2I] fp32, dw2 [E, I, H] fp32 (zero for experts
@@ -217,10 +224,14 @@ mc2_status_t mc2_gmm_swiglu(const mc2_shape_t* s, const void* xp, const void* w1
  *   MC2_ERR_UNSUPPORTED).  Pointer rules, errors and dev_status as above.
  */
 size_t mc2_backward_workspace_bytes(const mc2_shape_t* s);
+mc2_status_t mc2_alltoallv_gmm_keep(const mc2_shape_t* s, const void* x, const void* w1,
+                                    const int32_t* offsets, const int32_t* permute_src, void* h,
+                                    void* g, int32_t* dev_status, void* stream);
 mc2_status_t mc2_transpose_weights(const mc2_shape_t* s, const void* w1, const void* w2,
                                    void* w1t, void* w2t, void* stream);
 mc2_status_t mc2_moe_backward(const mc2_shape_t* s, const void* x, const float* probs,
-                              const void* w1, const void* w1t, const void* w2t, const void* dout,
+                              const void* w1, const void* g, const void* w1t, const void* w2t,
+                              const void* dout,
                               const int32_t* offsets, const int32_t* permute_src,
                               const int32_t* unpermute_dst, void* dx, float* dw1, float* dw2,
                               float* dprobs, void* ws, int32_t* dev_status, void* stream);

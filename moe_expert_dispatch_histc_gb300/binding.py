@@ -53,7 +53,8 @@ _SIGS = {
     "mc2_permute_rows": (ctypes.c_int, [_SP] + [_P] * 4),
     "mc2_backward_workspace_bytes": (ctypes.c_size_t, [_SP]),
     "mc2_transpose_weights": (ctypes.c_int, [_SP] + [_P] * 5),
-    "mc2_moe_backward": (ctypes.c_int, [_SP] + [_P] * 16),
+    "mc2_moe_backward": (ctypes.c_int, [_SP] + [_P] * 17),
+    "mc2_alltoallv_gmm_keep": (ctypes.c_int, [_SP] + [_P] * 8),
     "mc2_mm_reduce_scatter_workspace_bytes": (ctypes.c_size_t, [ctypes.c_void_p]),
     "mc2_mm_reduce_scatter_i8": (ctypes.c_int, [ctypes.c_void_p] + [_P] * 8),
     "mc2_gmm_swiglu": (ctypes.c_int, [_SP] + [_P] * 6),
@@ -179,9 +180,20 @@ def mc2_transpose_weights(shape, w1, w2, w1t, w2t, stream=None, check=True):
     return st
 
 
+def mc2_alltoallv_gmm_keep(shape, x, w1, offsets, permute_src, h, g, dev_status=None,
+                           stream=None, check=True):
+    st = lib().mc2_alltoallv_gmm_keep(ctypes.byref(shape), _p(x), _p(w1), _p(offsets),
+                                      _p(permute_src), _p(h), _p(g), _p(dev_status),
+                                      _stream(stream))
+    if check:
+        _check("mc2_alltoallv_gmm_keep", st)
+    return st
+
+
 def mc2_moe_backward(shape, x, probs, w1, w1t, w2t, dout, offsets, permute_src, unpermute_dst,
-                     dx, dw1, dw2, dprobs, ws, dev_status=None, stream=None, check=True):
-    st = lib().mc2_moe_backward(ctypes.byref(shape), _p(x), _p(probs), _p(w1), _p(w1t), _p(w2t),
+                     dx, dw1, dw2, dprobs, ws, dev_status=None, stream=None, check=True, g=None):
+    st = lib().mc2_moe_backward(ctypes.byref(shape), _p(x), _p(probs), _p(w1), _p(g), _p(w1t),
+                                _p(w2t),
                                 _p(dout), _p(offsets), _p(permute_src), _p(unpermute_dst),
                                 _p(dx), _p(dw1), _p(dw2), _p(dprobs), _p(ws), _p(dev_status),
                                 _stream(stream))

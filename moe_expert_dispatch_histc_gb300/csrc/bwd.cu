@@ -82,6 +82,32 @@ __global__ void fill_f32_kernel(float* __restrict__ p, int64_t n, float v) {
 
 __device__ __forceinline__ float sigmoid_f(float a) { return 1.0f / (1.0f + expf(-a)); }
 
+// Training forward: h[p] = bf16(silu(gate) * up) from the kept pre-activation
+// rows G [R, 2I] (bf16), rows p < offsets[E]; 8 columns per thread.
+__global__ void swiglu_fwd_kernel(const __nv_bfloat16* __restrict__ G,
+                                  const int32_t* __restrict__ offsets, int E, int I,
+                                  __nv_bfloat16* __restrict__ h) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int I8 = I / 8;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t p = idx / I8;
+  if (p >= __ldg(offsets + E)) return;
+  const int c = static_cast<int>(idx - p * I8) * 8;
+  const uint4 ga = __ldg(reinterpret_cast<const uint4*>(G + p * 2 * I + c));
+  const uint4 ua = __ldg(reinterpret_cast<const uint4*>(G + p * 2 * I + I + c));
+  const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&ga);
+  const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(&ua);
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 gv = __bfloat1622float2(g2[i]);
+    const float2 uv = __bfloat1622float2(u2[i]);
+    o[i] = pack_bf16x2(silu_f(gv.x) * uv.x, silu_f(gv.y) * uv.y);
+  }
+  *reinterpret_cast<uint4*>(h + p * I + c) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // One warp per permuted row p.  Valid rows: dG, probs * h and dprobs of the
 // row's (token, slot).  Rows of invalid ids: dprobs of their slot = 0, and
 // zero dG and probs * h rows (the weight-gradient GEMM may read them as the
@@ -195,8 +221,44 @@ extern "C" mc2_status_t mc2_transpose_weights(const mc2_shape_t* s, const void* 
   return e == cudaSuccess ? MC2_OK : MC2_ERR_CUDA;
 }
 
+extern "C" mc2_status_t mc2_alltoallv_gmm_keep(const mc2_shape_t* s, const void* x,
+                                               const void* w1, const int32_t* offsets,
+                                               const int32_t* permute_src, void* h, void* g,
+                                               int32_t* dev_status, void* stream) {
+  reset_launches();
+  if (mc2_check_shape(s) != MC2_OK) return MC2_ERR_INVALID_ARG;
+  if (!bwd_shape_ok(s)) return MC2_ERR_UNSUPPORTED;
+  if (!offsets) return MC2_ERR_INVALID_ARG;
+  if (s->T > 0 && (!x || !w1 || !permute_src || !h || !g)) return MC2_ERR_INVALID_ARG;
+  if (!al({x, w1, offsets, permute_src, h, g})) return MC2_ERR_INVALID_ARG;
+  const int64_t R = static_cast<int64_t>(s->T) * s->k;
+  if (R == 0) return MC2_OK;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.s = s;
+  a.a = x;
+  a.b = w1;
+  a.offsets = offsets;
+  a.permute_src = permute_src;
+  a.out = g;
+  a.dev_status = dev_status;
+  a.mode = MODE_FC1_PRE;
+  a.a_elem_bytes = 2;
+  cudaError_t e = launch_gemm(a, st);
+  if (e == cudaSuccess) {
+    const int64_t n = R * (s->I / 8);
+    e = launch_kernel(swiglu_fwd_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0,
+                      st, 1, static_cast<const __nv_bfloat16*>(g), offsets, static_cast<int>(s->E),
+                      static_cast<int>(s->I), static_cast<__nv_bfloat16*>(h));
+    if (e == cudaSuccess) note_launches(1);
+  }
+  return e == cudaSuccess ? MC2_OK : MC2_ERR_CUDA;
+}
+
 extern "C" mc2_status_t mc2_moe_backward(const mc2_shape_t* s, const void* x, const float* probs,
-                                         const void* w1, const void* w1t, const void* w2t,
+                                         const void* w1, const void* g_kept, const void* w1t,
+                                         const void* w2t,
                                          const void* dout, const int32_t* offsets,
                                          const int32_t* permute_src,
                                          const int32_t* unpermute_dst, void* dx, float* dw1,
@@ -208,8 +270,8 @@ extern "C" mc2_status_t mc2_moe_backward(const mc2_shape_t* s, const void* x, co
   if (!offsets || !ws || !w1 || !w1t || !w2t || !dw1 || !dw2) return MC2_ERR_INVALID_ARG;
   if (s->T > 0 && (!x || !probs || !dout || !permute_src || !unpermute_dst || !dx || !dprobs))
     return MC2_ERR_INVALID_ARG;
-  if (!al({x, probs, w1, w1t, w2t, dout, offsets, permute_src, unpermute_dst, dx, dw1, dw2,
-           dprobs}) ||
+  if (!al({x, probs, w1, g_kept, w1t, w2t, dout, offsets, permute_src, unpermute_dst, dx, dw1,
+           dw2, dprobs}) ||
       !al({ws}, 256))
     return MC2_ERR_INVALID_ARG;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -217,7 +279,7 @@ extern "C" mc2_status_t mc2_moe_backward(const mc2_shape_t* s, const void* x, co
   const BwdLayout L = bwd_layout(*s);
   char* w = static_cast<char*>(ws);
   auto* xp = w + L.xp;
-  auto* G = w + L.g;
+  const void* G = g_kept ? g_kept : static_cast<const void*>(w + L.g);
   auto* D = w + L.d;
   auto* dhu = w + L.dhu;
   auto* dhs = reinterpret_cast<float*>(w + L.dhs);
@@ -228,19 +290,22 @@ extern "C" mc2_status_t mc2_moe_backward(const mc2_shape_t* s, const void* x, co
   auto* ones = reinterpret_cast<float*>(w + L.ones);
   cudaError_t e = cudaSuccess;
   if (R > 0) {
-    // recompute G (pre-activation gate | up) with the fc1 kernel; permuted rows of x and dout
-    GemmArgs g;
-    std::memset(&g, 0, sizeof(g));
-    g.s = s;
-    g.a = x;
-    g.b = w1;
-    g.offsets = offsets;
-    g.permute_src = permute_src;
-    g.out = G;
-    g.dev_status = dev_status;
-    g.mode = MODE_FC1_PRE;
-    g.a_elem_bytes = 2;
-    e = launch_gemm(g, st);
+    // G (pre-activation gate | up): kept by the training forward, else recomputed
+    // with the fc1 kernel; then the permuted rows of x and dout
+    if (!g_kept) {
+      GemmArgs g;
+      std::memset(&g, 0, sizeof(g));
+      g.s = s;
+      g.a = x;
+      g.b = w1;
+      g.offsets = offsets;
+      g.permute_src = permute_src;
+      g.out = w + L.g;
+      g.dev_status = dev_status;
+      g.mode = MODE_FC1_PRE;
+      g.a_elem_bytes = 2;
+      e = launch_gemm(g, st);
+    }
     if (e == cudaSuccess) e = launch_permute_rows(*s, x, permute_src, xp, st);
     if (e == cudaSuccess) e = launch_permute_rows(*s, dout, permute_src, D, st);
     // dhu = D @ w2^T: the fc2 kernel with K = H, N = I on w2t [E, H, I]

@@ -26,7 +26,7 @@ def _tol(got, ref, what, max_rel=2e-2, mean_rel=1e-2):
     return a, m
 
 
-def run_backward(wl, seed=0, sel=None):
+def run_backward(wl, seed=0, sel=None, keep_g=False):
     ensure_built()
     inp = make_inputs(wl, seed)
     if sel is not None:
@@ -42,13 +42,19 @@ def run_backward(wl, seed=0, sel=None):
     w2t = torch.empty(wl.E, wl.H, wl.I, dtype=torch.bfloat16, device="cuda")
     B.mc2_transpose_weights(shape, d["w1"], d["w2"], w1t, w2t)
     dout = torch.from_numpy(dout_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    g = None
+    if keep_g:   # the training forward keeps the pre-activation rows
+        g = torch.empty(wl.T * wl.k, 2 * wl.I, dtype=torch.bfloat16, device="cuda")
+        h = torch.empty(wl.T * wl.k, wl.I, dtype=torch.bfloat16, device="cuda")
+        B.mc2_alltoallv_gmm_keep(shape, d["x"], d["w1"], b.offsets, b.permute_src, h, g,
+                                 b.dev_status)
     ws = torch.empty(B.mc2_backward_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
     dx = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device="cuda")
     dw1 = torch.empty(wl.E, wl.H, 2 * wl.I, dtype=torch.float32, device="cuda")
     dw2 = torch.empty(wl.E, wl.I, wl.H, dtype=torch.float32, device="cuda")
     dprobs = torch.empty(wl.T, wl.k, dtype=torch.float32, device="cuda")
     B.mc2_moe_backward(shape, d["x"], d["probs"], d["w1"], w1t, w2t, dout, b.offsets, b.permute_src,
-                       b.unpermute_dst, dx, dw1, dw2, dprobs, ws, b.dev_status)
+                       b.unpermute_dst, dx, dw1, dw2, dprobs, ws, b.dev_status, g=g)
     torch.cuda.synchronize()
     # transposes are exact copies
     assert torch.equal(w1t.view(torch.int16), d["w1"].transpose(1, 2).contiguous().view(torch.int16))
@@ -91,3 +97,38 @@ def test_backward_invalid_ids_and_empty_experts():
         assert not got["dw1"][e].any() and not got["dw2"][e].any()
     for name in ("dx", "dw1", "dw2", "dprobs"):
         _tol(got[name], ref[name], name)
+
+
+def test_backward_with_kept_pre_activation_is_bitwise_the_recompute():
+    wl = BWD[3]
+    got_r, _, st_r = run_backward(wl, seed=4)
+    got_k, _, st_k = run_backward(wl, seed=4, keep_g=True)
+    assert st_r == 0 and st_k == 0
+    for name in ("dx", "dw1", "dw2", "dprobs"):
+        assert np.array_equal(got_r[name], got_k[name]), name
+
+
+def test_training_forward_h_against_the_oracle():
+    """mc2_alltoallv_gmm_keep: h from the kept bf16 pre-activation, within the
+    block's forward tolerance of the oracle's h; g = the oracle's G rows."""
+    ensure_built()
+    wl = BWD[3]
+    inp = make_inputs(wl, 5)
+    d = blk.inputs_to_device(inp, wl)
+    b = blk.alloc_buffers(wl)
+    shape = blk.shape_of(wl)
+    B.mc2_moe_counts(shape, d["sel"], b.cnt, b.recv, b.offsets, b.permute_src, b.unpermute_dst,
+                     b.ws, b.dev_status)
+    g = torch.empty(wl.T * wl.k, 2 * wl.I, dtype=torch.bfloat16, device="cuda")
+    h = torch.empty(wl.T * wl.k, wl.I, dtype=torch.bfloat16, device="cuda")
+    B.mc2_alltoallv_gmm_keep(shape, d["x"], d["w1"], b.offsets, b.permute_src, h, g, b.dev_status)
+    torch.cuda.synchronize()
+    x, w1, w2 = (as_f64(inp[n], wl.act) for n in ("x", "w1", "w2"))
+    ref = orc.block_backward(x, w1, w2, inp["sel"], inp["probs"], np.zeros((wl.T, wl.H)), wl.E,
+                             wl.W, h_dtype="bf16")
+    nvalid = ref["g"].shape[0]
+    ok, a, m = orc.bf16_tolerance_ok(to_np(g)[:nvalid], ref["g"])
+    assert ok, (a, m)
+    ok, a, m = orc.bf16_tolerance_ok(to_np(h)[:nvalid], ref["h"])
+    assert ok, (a, m)
+    assert int(b.dev_status.item()) == 0
