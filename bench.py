@@ -379,9 +379,23 @@ def run_cuda(args):
     fc1_ms = float(seg[:, segi["fc1_swiglu"]].mean())
     fc2_ms = float(seg[:, segi["fc2_combine"]].mean())
     fc1_flops = 2 * wl.R * wl.H * 2 * wl.I
-    achieved = fc1_flops / (fc1_ms / 1e3) / 1e12
     peak = float(peaks["bf16_tflops"])
     tflops = wl.flops / ((fc1_ms + fc2_ms) / 1e3) / 1e12
+    # fc1's algorithmic bytes: the weights of experts that got rows, x, h
+    offs = b.offsets.cpu().numpy().astype(np.int64)
+    touched = int((np.diff(offs) > 0).sum())
+    esz = {"f32": 4, "bf16": 2, "i8": 1}[wl.act]
+    fc1_bytes = touched * wl.H * 2 * wl.I * esz + wl.T * wl.H * esz + \
+        int(offs[-1]) * wl.I * (4 if wl.act == "f32" else 2)
+    hbm = float(peaks["hbm_gbs"])
+    if fc1_flops / fc1_bytes < peak * 1e12 / (hbm * 1e9):   # below the ridge: bound by HBM
+        roof = {"bound": "hbm", "achieved": fc1_bytes / (fc1_ms / 1e3) / 1e9, "peak": hbm,
+                "unit": "GB/s", "peak_source": f"{src} hbm_gbs"}
+    else:
+        roof = {"bound": "tensor", "achieved": fc1_flops / (fc1_ms / 1e3) / 1e12, "peak": peak,
+                "unit": "TFLOP/s", "peak_source": f"{src} bf16_tflops (burst)"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["algorithmic"] = {"flops": fc1_flops, "bytes": fc1_bytes}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
@@ -392,8 +406,7 @@ def run_cuda(args):
         "roofline": {"kernel": ("gmm_kernel<fc1 rows> (fc1 + SwiGLU on materialised rows)"
                                 if unfused else
                                 "gmm_kernel<fc1> (permute gather + fc1 + SwiGLU)"),
-                     "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "peak_source": f"{src} bf16_tflops (burst)",
+                     **roof,
                      "traffic": None if unfused else _ncu_traffic("gmm_fc1", wl.name)},
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "steps": e2e_steps,
