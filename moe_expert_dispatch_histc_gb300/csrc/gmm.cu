@@ -7,10 +7,15 @@
 //        the permute is a row gather straight into the swizzled A tile
 //        (cp.async by four gather warps); SwiGLU runs on the fp32
 //        accumulator in TMEM; h tiles leave through TMA stores.
-//   fc2 (combine segment):   y[p, :] = h[p, :] @ w2[e]   (fp32, expert-major)
-//        then combine_kernel: out[t] = sum_j probs[t, j] * y[unpermute_dst[t*k+j]]
+//   fc2 (combine segment):   y[p, :] = h[p, :] @ w2[e]   (expert-major rows)
+//        stored as fp16 times a power-of-two factor per 64 columns, then
+//        combine_kernel: out[t] = sum_j probs[t, j] * y[unpermute_dst[t*k+j]]
 //        in ascending j -- every y row is written once, so the sum has a
 //        fixed order and the result is bitwise reproducible.
+//   Two more fc1 modes: MODE_FC1_ROWS takes already permuted rows through
+//   TMA (the non-fused baseline path); MODE_FC1_PRE writes the
+//   pre-activation gate | up rows instead of h (the backward's G).  The fc2
+//   kernel also serves the backward's two dgrads (on transposed weights).
 //
 // One persistent kernel per segment, one CTA per SM:
 //   warp 0      TMA producer of the B (weight) tiles (and of fc2's A tiles)
@@ -28,7 +33,11 @@
 //
 // Why a cp.async gather and not TMA tile::gather4: on GB300 the gather4
 // version of fc1 took 537 us on the 4096-token workload against 237 us for
-// this one (and 183 us when x is pre-permuted), with bit-identical h.
+// an early form of this one (190 us now; 175 us on pre-permuted rows, which
+// cost a 41 us permute pass first), with bit-identical h.
+//
+// Below the single-CTA kernel: a CTA-pair variant (tcgen05 cta_group::2,
+// 256-row tiles), used for fc2 when experts average >= 256 rows.
 #include <algorithm>
 
 #include "gmm_common.cuh"
