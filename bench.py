@@ -571,15 +571,19 @@ MMRS = {"W": 8, "m": 4096, "k": 1024, "n": 4096}   # TP over 8 ranks of a K=8192
 
 def run_mmrs(args):
     """Quantised matmul + reduce-scatter over W logical ranks (one C call per
-    step: int8 -> bf16 copies, the exact int8 grouped GEMM with one group per
-    rank, and the rank-ordered dequant + sum).  Metric: int8 tera-ops/s of
-    the whole operation (2*m*W*k*n per call)."""
+    step: int8 -> bf16 copies, then the fused CTA-pair kernel that folds every
+    rank's dequantised product into an on-chip sum; --path twopass: the exact
+    int8 grouped GEMM with one group per rank writing int32 partials, then the
+    rank-ordered dequant + sum).  Metric: int8 tera-ops/s of the whole
+    operation (2*m*W*k*n per call)."""
     import torch
     from moe_expert_dispatch_histc_gb300 import binding as B
     from moe_expert_dispatch_histc_gb300.build import build
     build()
     B.lib()
     W, m, k, n = MMRS["W"], MMRS["m"], MMRS["k"], MMRS["n"]
+    twopass = args.path == "twopass"
+    B.mc2_set_mmrs_path(1 if twopass else 0)
     rng = np.random.default_rng(0)
     x1 = rng.integers(-127, 128, (W, m, k)).astype(np.int8)
     x2 = rng.integers(-127, 128, (W, k, n)).astype(np.int8)
@@ -648,8 +652,11 @@ def run_mmrs(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8 (exact, on bf16 tensor cores)", "data": "synthetic",
         "config": {"workload": f"mm_reduce_scatter W{W} m{m} k{k} n{n}", **MMRS,
+                   "path": "twopass" if twopass else "fused",
                    "l2": "flushed (256 MB write) between steps"},
-        "roofline": {"kernel": "the whole call (int8->bf16 copies, gmm_q_kernel, reduce)",
+        "roofline": {"kernel": "the whole call (int8->bf16 copies, " +
+                               ("gmm_q_kernel, mmrs_reduce_kernel)" if twopass
+                                else "mmrs_fused_kernel)"),
                      "bound": "tensor", "achieved": value, "peak": peak, "unit": "TFLOP/s",
                      "frac": value / peak,
                      "peak_source": f"{src} bf16_tflops (burst); int8 runs at the bf16 rate",
@@ -675,9 +682,10 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--workload", default="uniform", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", default="fused", choices=["fused", "unfused"],
+    ap.add_argument("--path", default="fused", choices=["fused", "unfused", "twopass"],
                     help="unfused: the non-fused baseline (materialised permute, plain grouped "
-                         "fc1), bf16 workloads only")
+                         "fc1), bf16 workloads only; twopass (--op mm_reduce_scatter): int32 "
+                         "partials through memory, then a reduce kernel")
     ap.add_argument("--recompute-g", action="store_true",
                     help="--op backward: recompute G instead of taking the training forward's")
     ap.add_argument("--op", default="block", choices=["block", "backward", "mm_reduce_scatter"],
@@ -686,6 +694,10 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.path == "twopass" and args.op != "mm_reduce_scatter":
+        ap.error("--path twopass goes with --op mm_reduce_scatter")
+    if args.op == "mm_reduce_scatter" and args.path == "unfused":
+        ap.error("--op mm_reduce_scatter takes --path fused or twopass")
     if args.op == "backward":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "--op backward has its CPU "

@@ -255,8 +255,9 @@ mc2_status_t mc2_moe_backward(const mc2_shape_t* s, const void* x, const float* 
  * k and n multiples of 64, 64 <= k <= 4096 (the pages allow k up to 65535;
  * here K is summed in exact chunks of 1024 in at most four accumulators),
  * n >= 64; W*m < 2^31.  ws: mc2_mm_reduce_scatter_workspace_bytes(s) bytes
- * [dev], 256-byte aligned (bf16 copies of x1 and x2 and the int32 partial
- * products of every rank).  Errors and dev_status as for the block.
+ * [dev], 256-byte aligned (bf16 copies of x1 and x2, then room for the int32
+ * partial products of every rank, which only the two-pass form of
+ * mc2_set_mmrs_path writes).  Errors and dev_status as for the block.
  */
 typedef struct {
   int32_t m;  /* rows of each rank's x1 */
@@ -323,6 +324,16 @@ void mc2_set_tile_pairing(int32_t mode);
  * 1 always three launches; 2 the same as 0 (the cluster pass when it fits).
  * Outputs are identical either way.  Host only. */
 void mc2_set_counts_path(int32_t mode);
+
+/* Which form later mc2_mm_reduce_scatter_i8 calls of this process take:
+ * 0 (default) fused, one CTA-pair kernel after the int8 -> bf16 copies that
+ * folds every rank's dequantised product into an on-chip fp32 sum; 1 two
+ * passes, the int32 partial product of every rank written to the workspace
+ * (as [W, m, n] int32, after the two bf16 copies, each region 256-byte
+ * aligned), then a reduce kernel.  Both fold rank r in as
+ * fma(x1_scale * x2_scale, float(acc), sum), r ascending: the outputs are
+ * identical bit for bit.  Host only. */
+void mc2_set_mmrs_path(int32_t mode);
 
 /* Programmatic dependent launch between the kernels of later calls of this
  * process: 1 (default) lets each kernel's set-up overlap the end of the

@@ -64,6 +64,7 @@ _SIGS = {
     "mc2_set_tile_pairing": (None, [ctypes.c_int32]),
     "mc2_set_launch_overlap": (None, [ctypes.c_int32]),
     "mc2_set_counts_path": (None, [ctypes.c_int32]),
+    "mc2_set_mmrs_path": (None, [ctypes.c_int32]),
     "mc2_last_launch_count": (ctypes.c_int32, []),
     "mc2_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -278,6 +279,10 @@ def mc2_set_launch_overlap(enabled: int) -> None:
 
 def mc2_set_counts_path(mode: int) -> None:
     lib().mc2_set_counts_path(int(mode))
+
+
+def mc2_set_mmrs_path(mode: int) -> None:
+    lib().mc2_set_mmrs_path(int(mode))
 
 
 def mc2_last_launch_count() -> int:

@@ -14,6 +14,7 @@ static std::atomic<uint64_t> g_wait_limit_ns{0};
 static std::atomic<int> g_tile_pairing{0};
 static std::atomic<int> g_launch_overlap{1};
 static std::atomic<int> g_counts_path{0};
+static std::atomic<int> g_mmrs_path{0};
 static thread_local int tl_launches = 0;
 
 uint64_t wait_limit_ns() {
@@ -26,6 +27,8 @@ int tile_pairing_override() { return g_tile_pairing.load(); }
 bool launch_overlap_enabled() { return g_launch_overlap.load() != 0; }
 
 int counts_path_override() { return g_counts_path.load(); }
+
+int mmrs_path_override() { return g_mmrs_path.load(); }
 
 void note_launches(int n) { tl_launches += n; }
 
@@ -399,6 +402,8 @@ void mc2_set_tile_pairing(int32_t mode) { g_tile_pairing.store(mode == 1 || mode
 void mc2_set_launch_overlap(int32_t enabled) { g_launch_overlap.store(enabled ? 1 : 0); }
 
 void mc2_set_counts_path(int32_t mode) { g_counts_path.store(mode == 1 || mode == 2 ? mode : 0); }
+
+void mc2_set_mmrs_path(int32_t mode) { g_mmrs_path.store(mode == 1 ? 1 : 0); }
 
 int32_t mc2_last_launch_count(void) { return tl_launches; }
 

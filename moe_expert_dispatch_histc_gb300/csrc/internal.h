@@ -49,6 +49,7 @@ WsLayout ws_layout(const mc2_shape_t& s);
 uint64_t wait_limit_ns();
 bool launch_overlap_enabled();  // programmatic dependent launch between the block's kernels
 int counts_path_override();     // 0 auto, 1 three launches, 2 one cluster launch when it fits
+int mmrs_path_override();       // 0 fused (default), 1 two passes through int32 partials
 
 // Launch `kernel` on `st` with programmatic stream serialization (so its
 // prologue overlaps the previous kernel's tail; the kernel itself waits with

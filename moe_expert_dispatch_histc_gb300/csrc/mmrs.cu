@@ -8,20 +8,24 @@
 //           (x1_r' @ x2_r')                              (reduce op: sum)
 //
 // On one GPU the W ranks are logical, so the reduce-scatter is a sum over the
-// rank index and a row split.  Two passes:
-//   1. the exact int8 grouped GEMM of the MoE block (gmm_q.cu, raw int32
-//      accumulators; int8 values held as bf16, K summed in exact chunks) with
-//      one group per rank: rows r*m .. r*m+m-1 of the stacked x1 against x2_r;
-//   2. mmrs_reduce_kernel: per output element, the dequantised partials
-//      (x1_scale * x2_scale) * float(acc) summed in fp32 in rank order, one
-//      rounding to bf16.
+// rank index and a row split.  The int8 values run exactly on the bf16 tensor
+// cores (int8 -> bf16 copies first; K summed in exact fp32 chunks of 1024, as
+// in gmm_q.cu).  Two forms give the same bits:
+//   fused (default): mmrs_fused_kernel, one CTA-pair kernel per call that
+//     keeps every output tile's rank sum on chip (below);
+//   two passes: the exact int8 grouped GEMM of the MoE block (gmm_q.cu, raw
+//     int32 accumulators, one group per rank: rows r*m .. r*m+m-1 of the
+//     stacked x1 against x2_r) writes every rank's partial product to the
+//     workspace, then mmrs_reduce_kernel sums the dequantised partials.
+// Both fold rank r in as fma(x1_scale * x2_scale, float(acc), sum) in fp32,
+// r ascending, and round once to bf16.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 
-#include "internal.h"
-#include "ptx.cuh"
+#include "gmm_common.cuh"
 
 namespace mc2 {
 namespace {
@@ -61,7 +65,8 @@ __global__ void mmrs_offsets_kernel(int32_t* offsets, int W, int m) {
   for (int r = threadIdx.x; r <= W; r += blockDim.x) offsets[r] = r * m;
 }
 
-// out[i, c..c+7] = bf16( sum_r (xs[r, i] * ws[r, c]) * float(acc[r*m + i, c]) ), r ascending
+// out[i, c..c+7] = bf16( sum_r (xs[r, i] * ws[r, c]) * float(acc[r*m + i, c]) ), r ascending,
+// each rank folded in with one fma
 __global__ void mmrs_reduce_kernel(const int32_t* __restrict__ acc, const float* __restrict__ xs,
                                    const float* __restrict__ ws, int W, int m, int n,
                                    __nv_bfloat16* __restrict__ out) {
@@ -81,14 +86,14 @@ __global__ void mmrs_reduce_kernel(const int32_t* __restrict__ acc, const float*
     const int4 a0 = __ldg(a), a1 = __ldg(a + 1);
     const float4* w = reinterpret_cast<const float4*>(ws + static_cast<int64_t>(r) * n + c);
     const float4 w0 = __ldg(w), w1 = __ldg(w + 1);
-    s[0] += (xr * w0.x) * static_cast<float>(a0.x);
-    s[1] += (xr * w0.y) * static_cast<float>(a0.y);
-    s[2] += (xr * w0.z) * static_cast<float>(a0.z);
-    s[3] += (xr * w0.w) * static_cast<float>(a0.w);
-    s[4] += (xr * w1.x) * static_cast<float>(a1.x);
-    s[5] += (xr * w1.y) * static_cast<float>(a1.y);
-    s[6] += (xr * w1.z) * static_cast<float>(a1.z);
-    s[7] += (xr * w1.w) * static_cast<float>(a1.w);
+    s[0] = __fmaf_rn(xr * w0.x, static_cast<float>(a0.x), s[0]);
+    s[1] = __fmaf_rn(xr * w0.y, static_cast<float>(a0.y), s[1]);
+    s[2] = __fmaf_rn(xr * w0.z, static_cast<float>(a0.z), s[2]);
+    s[3] = __fmaf_rn(xr * w0.w, static_cast<float>(a0.w), s[3]);
+    s[4] = __fmaf_rn(xr * w1.x, static_cast<float>(a1.x), s[4]);
+    s[5] = __fmaf_rn(xr * w1.y, static_cast<float>(a1.y), s[5]);
+    s[6] = __fmaf_rn(xr * w1.z, static_cast<float>(a1.z), s[6]);
+    s[7] = __fmaf_rn(xr * w1.w, static_cast<float>(a1.w), s[7]);
   }
   uint4 o;
   __nv_bfloat162 b;
@@ -101,6 +106,366 @@ __global__ void mmrs_reduce_kernel(const int32_t* __restrict__ acc, const float*
   b = __floats2bfloat162_rn(s[6], s[7]);
   o.w = *reinterpret_cast<uint32_t*>(&b);
   *reinterpret_cast<uint4*>(out + i * n + c) = o;
+}
+
+// ----------------------------------------------------------------------------
+// Fused form: one CTA-pair kernel (tcgen05 cta_group::2, UMMA M = 256, N = 128).
+// A cluster owns an output tile of 256 rows x 128 columns (each CTA 128 rows).
+// For every rank r in ascending order it accumulates x1_r @ x2_r into TMEM
+// (K in exact chunks of 1024, one accumulator region each), and the epilogue
+// warps fold (x1_scale_r * x2_scale_r) * acc_r into an fp32 running sum held
+// in registers: one row and 128 columns per thread.  Two TMEM accumulator sets
+// (K <= 2048) let rank r+1's MMAs run while rank r is folded in.  After the
+// last rank the sum is rounded to bf16 and stored with TMA: the int32
+// partials never leave the SM, and the arithmetic is that of the two-pass
+// form, so both give the same bits.
+// ----------------------------------------------------------------------------
+constexpr int F_BN = 128;                    // UMMA N: output columns per tile
+constexpr int F_STAGES = 8;
+constexpr int F_A_STAGE = 128 * 128;         // 128 rows x 64 K values x 2 B
+constexpr int F_B_STAGE = 64 * 128;          // 64 K rows x this CTA's 64 columns x 2 B
+constexpr int F_STAGE_BYTES = F_A_STAGE + F_B_STAGE;
+constexpr int F_OUT_STAGE = 32 * 128;        // per epilogue warp: 32 rows x 64 bf16
+constexpr int F_CHUNK_KB = 16;               // k-blocks of 64 per exact fp32 chunk (K 1024)
+constexpr int F_THREADS = 6 * 32;            // producer, MMA / relay, four epilogue warps
+constexpr uint32_t F_TMEM_COLS = 512;
+constexpr size_t F_SMEM_BYTES = 1024 + F_STAGES * F_STAGE_BYTES + 4 * F_OUT_STAGE + 256;
+
+struct FParams {
+  const float* xs;       // x1_scale [W, m]
+  const float* ws;       // x2_scale [W, n]
+  int32_t* dev_status;
+  int W, m, n, K, n_tiles, total, nchunk;
+  uint64_t wait_limit_ns;
+};
+
+__global__ void __launch_bounds__(F_THREADS, 1)
+    mmrs_fused_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmOut, const FParams p) {
+  constexpr int BK = 64;
+  constexpr int KK_B = 16 * 128;             // B bytes per UMMA K step (16 K rows)
+  constexpr uint32_t IDESC = instr_desc(1, false, true, 256, F_BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + F_STAGES * F_A_STAGE;
+  uint8_t* sOut = sB + F_STAGES * F_B_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * F_OUT_STAGE);
+  uint64_t* pfull = full + F_STAGES;         // even CTA: the odd CTA's stage landed
+  uint64_t* empty = pfull + F_STAGES;
+  uint64_t* tfull = empty + F_STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_sh = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  const int nchunk = p.nchunk;
+  const int bufs = nchunk <= 2 ? 2 : 1;      // accumulator sets that fit in 512 columns
+  const uint32_t acc_cols = static_cast<uint32_t>(nchunk * F_BN);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < F_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&pfull[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2 * 4);  // one arrival per epilogue warp of both CTAs
+    }
+    mbar_init(mma_done, 1);
+    *abort_sh = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_base_sh, F_TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_sh;
+  // the pair's MMAs write one TMEM address in both CTAs
+  const uint32_t peer_base = ld_shared_cluster_u32(map_to_rank(tmem_base_sh, rank ^ 1u));
+  int total = p.total;
+  if (peer_base != tmem_base) {
+    if (threadIdx.x == 0 && p.dev_status) atomicOr(p.dev_status, 0x4);
+    total = 0;
+  }
+  WaitCtl ctl{abort_sh, p.wait_limit_ns, p.dev_status};
+  const int kblocks = p.K / BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int s = 0;
+    uint32_t ph = 0;
+    int n_arm = 0;
+    bool ok = true;
+    for (int tile = cluster; tile < total && ok; tile += nclusters) {
+      const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+      const int row0 = mt * 256 + static_cast<int>(rank) * 128;  // row within a rank's x1
+      const int col0 = nt * F_BN + static_cast<int>(rank) * 64;  // this CTA's half of B
+      for (int r = 0; r < p.W && ok; ++r) {
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (lane == 0) ok = mbar_wait_cluster(&empty[s], ph ^ 1, ctl);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full[s], F_STAGE_BYTES);
+            tma_load_2d(sA + s * F_A_STAGE, &tmA, &full[s], kb * BK, r * p.m + row0);
+            tma_load_3d(sB + s * F_B_STAGE, &tmB, &full[s], col0, kb * BK, r);
+          }
+          __syncwarp();
+          ++n_arm;
+          if (++s == F_STAGES) { s = 0; ph ^= 1; }
+        }
+      }
+    }
+    if (lane == 0) {  // every armed stage has landed and every commit to it has arrived
+      volatile int never = 0;
+      WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
+      for (int st = 0; st < F_STAGES && st < n_arm; ++st) {
+        const int last = st + F_STAGES * ((n_arm - 1 - st) / F_STAGES);
+        mbar_wait(&full[st], (last / F_STAGES) & 1, drain);
+        mbar_wait_cluster(&empty[st], (last / F_STAGES) & 1, drain);
+      }
+    }
+  } else if (warp == 1) {
+    if (leader) {
+      // ---------------------------------------------------------- MMA issuer
+      int s = 0, acc = 0;
+      uint32_t ph = 0, aph = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < total && ok; tile += nclusters) {
+        for (int r = 0; r < p.W && ok; ++r) {
+          if (lane == 0) ok = mbar_wait_cluster(&tempty[acc], aph ^ 1, ctl);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d0 = tmem_base + acc * acc_cols;
+          for (int kb = 0; kb < kblocks; ++kb) {
+            if (lane == 0) {
+              ok = mbar_wait(&full[s], ph, ctl);
+              if (ok) ok = mbar_wait_cluster(&pfull[s], ph, ctl);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t a_base = smem_u32(sA + s * F_A_STAGE);
+              const uint32_t b_base = smem_u32(sB + s * F_B_STAGE);
+              const uint32_t d = d0 + static_cast<uint32_t>((kb / F_CHUNK_KB) * F_BN);
+              const bool first = (kb % F_CHUNK_KB) == 0;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+                const uint64_t bdesc = smem_desc_sw128(b_base + kk * KK_B, F_B_STAGE, 1024);
+                umma_pair<0>(d, adesc, bdesc, IDESC, (first && kk == 0) ? 0u : 1u);
+              }
+              umma_commit_pair(&empty[s], 0x3);
+            }
+            __syncwarp();
+            if (++s == F_STAGES) { s = 0; ph ^= 1; }
+          }
+          if (!ok) break;
+          if (lane == 0) umma_commit_pair(&tfull[acc], 0x3);
+          __syncwarp();
+          if (bufs == 2) acc ^= 1;
+          if (acc == 0) aph ^= 1;
+        }
+      }
+      if (lane == 0) {
+        umma_commit_pair(mma_done, 0x1);
+        volatile int never = 0;
+        WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
+        mbar_wait_cluster(mma_done, 0, drain);
+      }
+      __syncwarp();
+    } else {
+      // ---------------------------------------------------------- relay (odd CTA)
+      const uint32_t leader_pfull = map_to_rank(pfull, 0);
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int tile = cluster; tile < total && ok; tile += nclusters) {
+        for (int r = 0; r < p.W && ok; ++r) {
+          for (int kb = 0; kb < kblocks; ++kb) {
+            if (lane == 0) {
+              ok = mbar_wait(&full[s], ph, ctl);
+              if (ok) mbar_arrive_remote_relaxed(leader_pfull + s * 8);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (++s == F_STAGES) { s = 0; ph ^= 1; }
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                  // TMEM lane quarter of this warp
+    uint8_t* stage = sOut + q * F_OUT_STAGE;
+    const uint32_t row_off = static_cast<uint32_t>(lane) * 128;
+    const uint32_t leader_tempty = map_to_rank(tempty, 0);
+    int acc = 0;
+    uint32_t aph = 0;
+    bool ok = true;
+    for (int tile = cluster; tile < total && ok; tile += nclusters) {
+      const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+      const int grow0 = mt * 256 + static_cast<int>(rank) * 128 + q * 32;
+      const int grow = grow0 + lane;
+      const bool valid = grow < p.m;
+      const int ncols = min(F_BN, p.n - nt * F_BN);   // 64 or 128 (n is a multiple of 64)
+      float sum[F_BN];
+#pragma unroll
+      for (int i = 0; i < F_BN; ++i) sum[i] = 0.f;
+      for (int r = 0; r < p.W; ++r) {
+        if (lane == 0) ok = mbar_wait_cluster(&tfull[acc], aph, ctl);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + acc * acc_cols + (static_cast<uint32_t>(q * 32) << 16);
+        const float xr = valid ? __ldg(p.xs + static_cast<int64_t>(r) * p.m + grow) : 0.f;
+        const float* wr = p.ws + static_cast<int64_t>(r) * p.n + nt * F_BN;
+#pragma unroll
+        for (int g = 0; g < F_BN / 32; ++g) {
+          if (g * 32 < ncols) {   // no scales exist past column n
+            int32_t si[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) si[i] = 0;
+#pragma unroll 1
+            for (int c = 0; c < nchunk; ++c) {   // exact int32 sum of the chunk sums
+              uint32_t v[32];
+              tmem_ld32(tbase + c * F_BN + g * 32, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) si[i] += __float2int_rn(__uint_as_float(v[i]));
+            }
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 w4 = __ldg(reinterpret_cast<const float4*>(wr + g * 32 + i));
+              sum[g * 32 + i] = __fmaf_rn(xr * w4.x, static_cast<float>(si[i]), sum[g * 32 + i]);
+              sum[g * 32 + i + 1] =
+                  __fmaf_rn(xr * w4.y, static_cast<float>(si[i + 1]), sum[g * 32 + i + 1]);
+              sum[g * 32 + i + 2] =
+                  __fmaf_rn(xr * w4.z, static_cast<float>(si[i + 2]), sum[g * 32 + i + 2]);
+              sum[g * 32 + i + 3] =
+                  __fmaf_rn(xr * w4.w, static_cast<float>(si[i + 3]), sum[g * 32 + i + 3]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(&tempty[acc]);
+          else mbar_arrive_remote_relaxed(leader_tempty + acc * 8);  // after tcgen05.wait::ld
+        }
+        if (bufs == 2) acc ^= 1;
+        if (acc == 0) aph ^= 1;
+      }
+      if (!ok) break;
+      if (grow0 < p.m) {  // rows past m fall outside the output map and are not written
+#pragma unroll
+        for (int h = 0; h < F_BN / 64; ++h) {
+          if (h * 64 < ncols) {
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const int c = h * 64 + v * 8;
+              *reinterpret_cast<uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4)) =
+                  make_uint4(pack_bf16x2(sum[c], sum[c + 1]), pack_bf16x2(sum[c + 2], sum[c + 3]),
+                             pack_bf16x2(sum[c + 4], sum[c + 5]),
+                             pack_bf16x2(sum[c + 6], sum[c + 7]));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmOut, stage, nt * F_BN + h * 64, grow0);
+              bulk_commit();
+            }
+            __syncwarp();
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, F_TMEM_COLS);
+}
+
+cudaError_t launch_mmrs_fused(const mc2_mmrs_shape_t& s, const void* x1b, const void* x2b,
+                              const float* xs, const float* ws, void* out, int32_t* dev_status,
+                              cudaStream_t st) {
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t rows = static_cast<uint64_t>(s.W) * s.m;
+  CUtensorMap tA, tB, tOut;
+  if (!encode_2d(&tA, bf, 2, x1b, s.k, rows, 64, 128) ||
+      !encode_3d(&tB, bf, 2, x2b, s.n, s.k, s.W, 64, 64) ||
+      !encode_2d(&tOut, bf, 2, out, s.n, s.m, 64, 32))
+    return cudaErrorInvalidValue;
+  FParams p;
+  p.xs = xs;
+  p.ws = ws;
+  p.dev_status = dev_status;
+  p.W = s.W;
+  p.m = s.m;
+  p.n = s.n;
+  p.K = s.k;
+  p.n_tiles = (s.n + F_BN - 1) / F_BN;
+  p.total = ((s.m + 255) / 256) * p.n_tiles;
+  p.nchunk = (s.k / 64 + F_CHUNK_KB - 1) / F_CHUNK_KB;
+  p.wait_limit_ns = wait_limit_ns();
+  // Persistent grid: as many pairs as can be resident at once (a pair needs
+  // two SMs of one GPC, so this can be fewer than SMs / 2).
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(mmrs_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(F_SMEM_BYTES));
+    if (attr_err != cudaSuccess) return;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms() & ~1, 1, 1);
+    cfg.blockDim = dim3(F_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = F_SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, mmrs_fused_kernel, &cfg) != cudaSuccess)
+      max_clusters = 0;
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+  const int grid = 2 * std::min(max_clusters, std::max(p.total, 1));
+  const cudaError_t e = launch_kernel(mmrs_fused_kernel, dim3(grid), dim3(F_THREADS), F_SMEM_BYTES,
+                                      st, 2, tA, tB, tOut, p);
+  note_launches(1);
+  return e;
 }
 
 bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -135,6 +500,11 @@ extern "C" mc2_status_t mc2_mm_reduce_scatter_i8(const mc2_mmrs_shape_t* s, cons
   cudaError_t e = launch_i8_to_bf16(x1, w + L.x1_b16, static_cast<size_t>(rows) * s->k, st);
   if (e == cudaSuccess)
     e = launch_i8_to_bf16(x2, w + L.x2_b16, static_cast<size_t>(s->W) * s->k * s->n, st);
+  if (mmrs_path_override() != 1) {  // fused: one kernel after the two copies
+    if (e == cudaSuccess)
+      e = launch_mmrs_fused(*s, w + L.x1_b16, w + L.x2_b16, x1_scale, x2_scale, out, dev_status, st);
+    return e == cudaSuccess ? MC2_OK : MC2_ERR_CUDA;
+  }
   int32_t* offsets = reinterpret_cast<int32_t*>(w + L.offsets);
   if (e == cudaSuccess) {
     e = launch_kernel(mmrs_offsets_kernel, dim3(1), dim3(128), 0, st, 1, offsets,

@@ -1,6 +1,9 @@
 """Quantised matmul + reduce-scatter over logical ranks on the GPU, against
-the CPU oracle: every rank's int32 partial product bit-exact (read from the
-workspace), the bf16 result within the block's tolerance rule."""
+the CPU oracle.  Two forms: the two-pass one writes every rank's int32
+partial product to the workspace (checked bit-exact); the fused one keeps
+them on chip, and its bf16 result must equal the two-pass result bit for bit
+(the same fma per rank, in rank order).  Both within the block's tolerance
+rule of the float64 oracle."""
 import numpy as np
 import pytest
 import torch
@@ -15,6 +18,23 @@ pytestmark = pytest.mark.gpu
 
 def _align(v, a=256):
     return (v + a - 1) // a * a
+
+
+@pytest.fixture(autouse=True)
+def _default_path():
+    yield
+    B.mc2_set_mmrs_path(0)
+
+
+def _call(s, d, ws, m, n, path):
+    B.mc2_set_mmrs_path(path)
+    out = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.mc2_mm_reduce_scatter_i8(s, d[0], d[1], d[2], d[3], out, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert B.mc2_last_launch_count() == (3 if path == 0 else 5)
+    return out
 
 
 def _run(W, m, k, n, seed=0, worst=False):
@@ -32,12 +52,11 @@ def _run(W, m, k, n, seed=0, worst=False):
     nbytes = B.mc2_mm_reduce_scatter_workspace_bytes(s)
     assert nbytes > 0
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    out = torch.empty(m, n, dtype=torch.bfloat16, device="cuda")
-    st = torch.zeros(1, dtype=torch.int32, device="cuda")
     d = [torch.from_numpy(a).cuda() for a in (x1, x1s, x2, x2s)]
-    B.mc2_mm_reduce_scatter_i8(s, d[0], d[1], d[2], d[3], out, ws, st)
-    torch.cuda.synchronize()
-    assert int(st.item()) == 0
+    out = _call(s, d, ws, m, n, 1)
+    fused = _call(s, d, ws, m, n, 0)
+    assert torch.equal(fused.view(torch.int16), out.view(torch.int16)), \
+        "fused result differs from the two-pass result"
     acc, total, per_rank = orc.mm_reduce_scatter(x1, x1s, x2, x2s)
     # workspace: bf16 x1 [W*m, k], bf16 x2 [W, k, n], int32 partials [W*m, n]
     off = _align(W * m * k * 2) + _align(W * k * n * 2)
@@ -53,14 +72,16 @@ def _run(W, m, k, n, seed=0, worst=False):
 
 
 @pytest.mark.parametrize("W,m,k,n", [(1, 64, 256, 128), (2, 64, 256, 128), (4, 256, 1024, 320),
-                                     (8, 136, 512, 192), (3, 300, 1088, 64)])
+                                     (8, 136, 512, 192), (3, 300, 1088, 64), (2, 512, 3072, 128),
+                                     (1, 512, 2048, 576), (8, 776, 128, 320)])
 def test_mm_reduce_scatter_parity(W, m, k, n):
     _run(W, m, k, n, seed=W * 7 + k)
 
 
 def test_mm_reduce_scatter_worst_case_accumulators():
     """k = 4096 with every product -127*127: |acc| = 66 M > 2^24 per rank, still
-    exact in int32 (four exact 1024-long chunks)."""
+    exact in int32 (four exact 1024-long chunks; the fused form then has one
+    accumulator set in TMEM instead of two)."""
     _run(2, 128, 4096, 128, worst=True)
 
 
@@ -70,7 +91,9 @@ def test_mm_reduce_scatter_empty_and_rejected():
     ws = torch.empty(B.mc2_mm_reduce_scatter_workspace_bytes(s), dtype=torch.uint8, device="cuda")
     x2 = torch.zeros(2, 256, 128, dtype=torch.int8, device="cuda")
     x2s = torch.ones(2, 128, device="cuda")
-    assert B.mc2_mm_reduce_scatter_i8(s, None, None, x2, x2s, None, ws, None) == B.MC2_OK
+    for path in (0, 1):
+        B.mc2_set_mmrs_path(path)
+        assert B.mc2_mm_reduce_scatter_i8(s, None, None, x2, x2s, None, ws, None) == B.MC2_OK
     bad = B.MmrsShape(6, 256, 128, 4)   # m not divisible by W
     assert B.mc2_mm_reduce_scatter_i8(bad, x2, x2s, x2, x2s, x2, ws, None,
                                       check=False) == B.MC2_ERR_INVALID_ARG
