@@ -118,7 +118,10 @@ __global__ void mmrs_reduce_kernel(const int32_t* __restrict__ acc, const float*
 // (K <= 2048) let rank r+1's MMAs run while rank r is folded in.  After the
 // last rank the sum is rounded to bf16 and stored with TMA: the int32
 // partials never leave the SM, and the arithmetic is that of the two-pass
-// form, so both give the same bits.
+// form, so both give the same bits.  Both CTAs' operand loads of a stage
+// complete on the even CTA's barrier (the odd CTA uses the pair form of the
+// TMA copy), so the even CTA's MMA thread starts a stage as soon as both
+// halves have landed, with no relay through the odd CTA.
 // ----------------------------------------------------------------------------
 constexpr int F_BN = 128;                    // UMMA N: output columns per tile
 constexpr int F_STAGES = 8;
@@ -153,9 +156,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + F_STAGES * F_A_STAGE;
   uint8_t* sOut = sB + F_STAGES * F_B_STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * F_OUT_STAGE);
-  uint64_t* pfull = full + F_STAGES;         // even CTA: the odd CTA's stage landed
-  uint64_t* empty = pfull + F_STAGES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * F_OUT_STAGE);  // even CTA: both halves
+  uint64_t* empty = full + F_STAGES;
   uint64_t* tfull = empty + F_STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* mma_done = tempty + 2;
@@ -173,7 +175,6 @@ __global__ void __launch_bounds__(F_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < F_STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&pfull[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -212,6 +213,10 @@ __global__ void __launch_bounds__(F_THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // Both CTAs' loads of a stage complete on the even CTA's full[s] (the even
+    // producer expects the bytes of both halves); the odd CTA loads with the
+    // pair form of the copy, straight onto that barrier.
+    const uint32_t leader_full = map_to_rank(full, 0);
     int s = 0;
     uint32_t ph = 0;
     int n_arm = 0;
@@ -226,9 +231,15 @@ __global__ void __launch_bounds__(F_THREADS, 1)
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           if (lane == 0) {
-            mbar_arrive_expect_tx(&full[s], F_STAGE_BYTES);
-            tma_load_2d(sA + s * F_A_STAGE, &tmA, &full[s], kb * BK, r * p.m + row0);
-            tma_load_3d(sB + s * F_B_STAGE, &tmB, &full[s], col0, kb * BK, r);
+            if (leader) {
+              mbar_arrive_expect_tx(&full[s], 2 * F_STAGE_BYTES);
+              tma_load_2d(sA + s * F_A_STAGE, &tmA, &full[s], kb * BK, r * p.m + row0);
+              tma_load_3d(sB + s * F_B_STAGE, &tmB, &full[s], col0, kb * BK, r);
+            } else {
+              tma_load_2d_pair(sA + s * F_A_STAGE, &tmA, leader_full + s * 8, kb * BK,
+                               r * p.m + row0);
+              tma_load_3d_pair(sB + s * F_B_STAGE, &tmB, leader_full + s * 8, col0, kb * BK, r);
+            }
           }
           __syncwarp();
           ++n_arm;
@@ -241,7 +252,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
       WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
       for (int st = 0; st < F_STAGES && st < n_arm; ++st) {
         const int last = st + F_STAGES * ((n_arm - 1 - st) / F_STAGES);
-        mbar_wait(&full[st], (last / F_STAGES) & 1, drain);
+        if (leader) mbar_wait_cluster(&full[st], (last / F_STAGES) & 1, drain);
         mbar_wait_cluster(&empty[st], (last / F_STAGES) & 1, drain);
       }
     }
@@ -259,10 +270,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
           tc_fence_after();
           const uint32_t d0 = tmem_base + acc * acc_cols;
           for (int kb = 0; kb < kblocks; ++kb) {
-            if (lane == 0) {
-              ok = mbar_wait(&full[s], ph, ctl);
-              if (ok) ok = mbar_wait_cluster(&pfull[s], ph, ctl);
-            }
+            if (lane == 0) ok = mbar_wait_cluster(&full[s], ph, ctl);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
@@ -296,26 +304,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         mbar_wait_cluster(mma_done, 0, drain);
       }
       __syncwarp();
-    } else {
-      // ---------------------------------------------------------- relay (odd CTA)
-      const uint32_t leader_pfull = map_to_rank(pfull, 0);
-      int s = 0;
-      uint32_t ph = 0;
-      bool ok = true;
-      for (int tile = cluster; tile < total && ok; tile += nclusters) {
-        for (int r = 0; r < p.W && ok; ++r) {
-          for (int kb = 0; kb < kblocks; ++kb) {
-            if (lane == 0) {
-              ok = mbar_wait(&full[s], ph, ctl);
-              if (ok) mbar_arrive_remote_relaxed(leader_pfull + s * 8);
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            if (++s == F_STAGES) { s = 0; ph ^= 1; }
-          }
-        }
-      }
-    }
+    }  // the odd CTA's MMA warp has nothing to do: its stages complete on the even CTA
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                  // TMEM lane quarter of this warp
