@@ -449,8 +449,11 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
 // -- fc1: the even CTA the gate half, the odd CTA the up half of the same 128
 // output columns -- so each SM streams 32 KB per k-block instead of 48 KB,
 // and six stages fit.  The even CTA issues the MMAs and commits to barriers
-// in both CTAs; the odd CTA's idle MMA warp relays "stage s landed here" to
-// the even CTA.  Each CTA's TMEM holds all 256 accumulator columns of its 128
+// in both CTAs.  With TMA-loaded operands (fc2, fc1 on permuted rows) the odd
+// CTA's copies complete on the even CTA's stage barrier (pair form of the
+// copy, which names a barrier in either CTA of the pair); with gathered rows
+// (cp.async, local barriers only) the odd CTA's idle MMA warp relays "stage s
+// landed here" to the even CTA.  Each CTA's TMEM holds all 256 accumulator columns of its 128
 // rows, so the epilogue is the single-CTA one; two accumulators in TMEM let
 // the epilogue of tile i overlap the mainloop of tile i+1.
 // ----------------------------------------------------------------------------
@@ -474,6 +477,9 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
   constexpr bool BKM = TR::B_KMAJOR;
   constexpr uint32_t IDESC = instr_desc(TR::FMT, false, !BKM, 2 * BM, BN);
   constexpr bool GATHER = MODE == MODE_FC1 || MODE == MODE_FC1_PRE;
+  // TMA-only modes: the odd CTA's loads complete on the even CTA's full[s]
+  // (pair form of the copy); gathering modes relay the odd CTA's stages.
+  constexpr bool DIRECT = !GATHER;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -559,6 +565,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    const uint32_t leader_full = map_to_rank(full, 0);
     int s = 0;
     uint32_t ph = 0;
     int n_arm = 0;
@@ -577,21 +584,34 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[s], GATHER ? P_B_STAGE : P_STAGE_BYTES);
           uint8_t* b_dst = sB + s * P_B_STAGE;
           const int k0 = kb * BK;
-          if (!GATHER) tma_load_2d(sA + s * A_STAGE, &tmA, &full[s], k0, row0);
           // this CTA's 128 columns of B: fc1 gate (even) or up (odd) half;
           // fc2 the first or second 128 of the 256-column tile
           const int nbase = MODE != MODE_FC2 ? static_cast<int>(rank) * p.I + n * (BN / 2)
                                              : n * BN + static_cast<int>(rank) * (BN / 2);
-          if constexpr (BKM) {
-            tma_load_3d(b_dst, &tmB, &full[s], k0, nbase, e);
+          if (DIRECT && !leader) {
+            const uint32_t bar = leader_full + s * 8;
+            tma_load_2d_pair(sA + s * A_STAGE, &tmA, bar, k0, row0);
+            if constexpr (BKM) {
+              tma_load_3d_pair(b_dst, &tmB, bar, k0, nbase, e);
+            } else {
+              if (MODE != MODE_FC2)
+                tma_load_5d_pair(b_dst, &tmB, bar, 0, k0, n * NBH, static_cast<int>(rank), e);
+              else
+                tma_load_4d_pair(b_dst, &tmB, bar, 0, k0, nbase / BNB, e);
+            }
           } else {
-            if (MODE != MODE_FC2)
-              tma_load_5d(b_dst, &tmB, &full[s], 0, k0, n * NBH, static_cast<int>(rank), e);
-            else
-              tma_load_4d(b_dst, &tmB, &full[s], 0, k0, nbase / BNB, e);
+            mbar_arrive_expect_tx(&full[s], GATHER ? P_B_STAGE : 2 * P_STAGE_BYTES);
+            if (!GATHER) tma_load_2d(sA + s * A_STAGE, &tmA, &full[s], k0, row0);
+            if constexpr (BKM) {
+              tma_load_3d(b_dst, &tmB, &full[s], k0, nbase, e);
+            } else {
+              if (MODE != MODE_FC2)
+                tma_load_5d(b_dst, &tmB, &full[s], 0, k0, n * NBH, static_cast<int>(rank), e);
+              else
+                tma_load_4d(b_dst, &tmB, &full[s], 0, k0, nbase / BNB, e);
+            }
           }
         }
         __syncwarp();
@@ -604,7 +624,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
       for (int st = 0; st < P_STAGES && st < n_arm; ++st) {
         const int last = st + P_STAGES * ((n_arm - 1 - st) / P_STAGES);
-        mbar_wait(&full[st], (last / P_STAGES) & 1, drain);
+        if (!DIRECT || leader) mbar_wait_cluster(&full[st], (last / P_STAGES) & 1, drain);
         mbar_wait_cluster(&empty[st], (last / P_STAGES) & 1, drain);
       }
     }
@@ -622,8 +642,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (lane == 0) {
-            ok = mbar_wait(&full[s], ph, ctl);
-            if (ok) ok = mbar_wait_cluster(&pfull[s], ph, ctl);
+            ok = mbar_wait_cluster(&full[s], ph, ctl);
+            if (ok && !DIRECT) ok = mbar_wait_cluster(&pfull[s], ph, ctl);
             if (GATHER && ok) fence_proxy_async_smem();  // gathered rows -> async proxy
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -657,7 +677,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
         mbar_wait_cluster(mma_done, 0, drain);
       }
       __syncwarp();
-    } else {
+    } else if (!DIRECT) {
       // ---------------------------------------------------------- relay (odd CTA)
       const uint32_t leader_pfull = map_to_rank(pfull, 0);
       int s = 0;
