@@ -109,30 +109,40 @@ __global__ void mmrs_reduce_kernel(const int32_t* __restrict__ acc, const float*
 }
 
 // ----------------------------------------------------------------------------
-// Fused form: one CTA-pair kernel (tcgen05 cta_group::2, UMMA M = 256, N = 128).
-// A cluster owns an output tile of 256 rows x 128 columns (each CTA 128 rows).
+// Fused form: one CTA-pair kernel (tcgen05 cta_group::2, UMMA M = 256, N = NB).
+// A cluster owns an output tile of 256 rows x NB columns (each CTA 128 rows).
 // For every rank r in ascending order it accumulates x1_r @ x2_r into TMEM
 // (K in exact chunks of 1024, one accumulator region each), and the epilogue
 // warps fold (x1_scale_r * x2_scale_r) * acc_r into an fp32 running sum held
-// in registers: one row and 128 columns per thread.  Two TMEM accumulator sets
-// (K <= 2048) let rank r+1's MMAs run while rank r is folded in.  After the
-// last rank the sum is rounded to bf16 and stored with TMA: the int32
-// partials never leave the SM, and the arithmetic is that of the two-pass
-// form, so both give the same bits.  Both CTAs' operand loads of a stage
-// complete on the even CTA's barrier (the odd CTA uses the pair form of the
-// TMA copy), so the even CTA's MMA thread starts a stage as soon as both
-// halves have landed, with no relay through the odd CTA.
+// in registers: one row and 128 columns per thread (NB / 32 epilogue warps).
+// Two TMEM accumulator sets, when they fit, let rank r+1's MMAs run while
+// rank r is folded in.  After the last rank the sum is rounded to bf16 and
+// stored with TMA: the int32 partials never leave the SM, and the arithmetic
+// is that of the two-pass form, so both give the same bits.  Both CTAs'
+// operand loads of a stage complete on the even CTA's barrier (the odd CTA
+// uses the pair form of the TMA copy), so the even CTA's MMA thread starts a
+// stage as soon as both halves have landed, with no relay through the odd CTA.
+//   NB = 256 (K <= 2048): 32 KB per CTA per 64-deep stage for 128 x 256 x 64
+//     MMAs, six stages, eight epilogue warps;
+//   NB = 128 (any K up to 4096): 24 KB per stage for 128 x 128 x 64, eight
+//     stages, four epilogue warps.
 // ----------------------------------------------------------------------------
-constexpr int F_BN = 128;                    // UMMA N: output columns per tile
-constexpr int F_STAGES = 8;
 constexpr int F_A_STAGE = 128 * 128;         // 128 rows x 64 K values x 2 B
-constexpr int F_B_STAGE = 64 * 128;          // 64 K rows x this CTA's 64 columns x 2 B
-constexpr int F_STAGE_BYTES = F_A_STAGE + F_B_STAGE;
 constexpr int F_OUT_STAGE = 32 * 128;        // per epilogue warp: 32 rows x 64 bf16
 constexpr int F_CHUNK_KB = 16;               // k-blocks of 64 per exact fp32 chunk (K 1024)
-constexpr int F_THREADS = 6 * 32;            // producer, MMA / relay, four epilogue warps
 constexpr uint32_t F_TMEM_COLS = 512;
-constexpr size_t F_SMEM_BYTES = 1024 + F_STAGES * F_STAGE_BYTES + 4 * F_OUT_STAGE + 256;
+
+template <int NB>
+struct FCfg {
+  static constexpr int kEpiWarps = NB / 32;             // 128 columns per epilogue thread
+  static constexpr int kThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue
+  static constexpr int kStages = NB == 256 ? 6 : 8;
+  static constexpr int kBStage = 64 * (NB / 2) * 2;      // 64 K rows x this CTA's NB/2 columns
+  static constexpr int kStageBytes = F_A_STAGE + kBStage;
+  static constexpr int kGW = NB == 256 ? 8 : 32;        // epilogue column group (registers)
+  static constexpr size_t kSmem =
+      1024 + static_cast<size_t>(kStages) * kStageBytes + kEpiWarps * F_OUT_STAGE + 256;
+};
 
 struct FParams {
   const float* xs;       // x1_scale [W, m]
@@ -142,23 +152,35 @@ struct FParams {
   uint64_t wait_limit_ns;
 };
 
-__global__ void __launch_bounds__(F_THREADS, 1)
+template <int GW>
+__device__ __forceinline__ void tmem_ld_group(uint32_t taddr, uint32_t (&v)[GW]) {
+  if constexpr (GW == 32) tmem_ld32(taddr, v);
+  else if constexpr (GW == 16) tmem_ld16(taddr, v);
+  else tmem_ld8(taddr, v);
+}
+
+template <int NB>
+__global__ void __launch_bounds__(FCfg<NB>::kThreads, 1)
     mmrs_fused_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmOut, const FParams p) {
+  using C = FCfg<NB>;
   constexpr int BK = 64;
+  constexpr int STAGES = C::kStages;
+  constexpr int B_STAGE = C::kBStage;
+  constexpr int GW = C::kGW;
   constexpr int KK_B = 16 * 128;             // B bytes per UMMA K step (16 K rows)
-  constexpr uint32_t IDESC = instr_desc(1, false, true, 256, F_BN);
+  constexpr uint32_t IDESC = instr_desc(1, false, true, 256, NB);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + F_STAGES * F_A_STAGE;
-  uint8_t* sOut = sB + F_STAGES * F_B_STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * F_OUT_STAGE);  // even CTA: both halves
-  uint64_t* empty = full + F_STAGES;
-  uint64_t* tfull = empty + F_STAGES;
+  uint8_t* sB = smem + STAGES * F_A_STAGE;
+  uint8_t* sOut = sB + STAGES * B_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + C::kEpiWarps * F_OUT_STAGE);  // even CTA
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* mma_done = tempty + 2;
   uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -169,17 +191,17 @@ __global__ void __launch_bounds__(F_THREADS, 1)
   const bool leader = rank == 0;
   const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
   const int nchunk = p.nchunk;
-  const int bufs = nchunk <= 2 ? 2 : 1;      // accumulator sets that fit in 512 columns
-  const uint32_t acc_cols = static_cast<uint32_t>(nchunk * F_BN);
+  const uint32_t acc_cols = static_cast<uint32_t>(nchunk * NB);
+  const int bufs = 2 * acc_cols <= F_TMEM_COLS ? 2 : 1;  // accumulator sets that fit
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < F_STAGES; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 2 * 4);  // one arrival per epilogue warp of both CTAs
+      mbar_init(&tempty[b], 2 * C::kEpiWarps);  // one arrival per epilogue warp of both CTAs
     }
     mbar_init(mma_done, 1);
     *abort_sh = 0;
@@ -223,37 +245,43 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     bool ok = true;
     for (int tile = cluster; tile < total && ok; tile += nclusters) {
       const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
-      const int row0 = mt * 256 + static_cast<int>(rank) * 128;  // row within a rank's x1
-      const int col0 = nt * F_BN + static_cast<int>(rank) * 64;  // this CTA's half of B
+      const int row0 = mt * 256 + static_cast<int>(rank) * 128;     // row within a rank's x1
+      const int col0 = nt * NB + static_cast<int>(rank) * (NB / 2);  // this CTA's half of B
       for (int r = 0; r < p.W && ok; ++r) {
         for (int kb = 0; kb < kblocks; ++kb) {
           if (lane == 0) ok = mbar_wait_cluster(&empty[s], ph ^ 1, ctl);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           if (lane == 0) {
+            uint8_t* a_dst = sA + s * F_A_STAGE;
+            uint8_t* b_dst = sB + s * B_STAGE;
             if (leader) {
-              mbar_arrive_expect_tx(&full[s], 2 * F_STAGE_BYTES);
-              tma_load_2d(sA + s * F_A_STAGE, &tmA, &full[s], kb * BK, r * p.m + row0);
-              tma_load_3d(sB + s * F_B_STAGE, &tmB, &full[s], col0, kb * BK, r);
+              mbar_arrive_expect_tx(&full[s], 2 * C::kStageBytes);
+              tma_load_2d(a_dst, &tmA, &full[s], kb * BK, r * p.m + row0);
+#pragma unroll
+              for (int j = 0; j < NB / 128; ++j)   // 64-column blocks, 8 KB apart
+                tma_load_3d(b_dst + j * 8192, &tmB, &full[s], col0 + 64 * j, kb * BK, r);
             } else {
-              tma_load_2d_pair(sA + s * F_A_STAGE, &tmA, leader_full + s * 8, kb * BK,
-                               r * p.m + row0);
-              tma_load_3d_pair(sB + s * F_B_STAGE, &tmB, leader_full + s * 8, col0, kb * BK, r);
+              const uint32_t bar = leader_full + s * 8;
+              tma_load_2d_pair(a_dst, &tmA, bar, kb * BK, r * p.m + row0);
+#pragma unroll
+              for (int j = 0; j < NB / 128; ++j)
+                tma_load_3d_pair(b_dst + j * 8192, &tmB, bar, col0 + 64 * j, kb * BK, r);
             }
           }
           __syncwarp();
           ++n_arm;
-          if (++s == F_STAGES) { s = 0; ph ^= 1; }
+          if (++s == STAGES) { s = 0; ph ^= 1; }
         }
       }
     }
     if (lane == 0) {  // every armed stage has landed and every commit to it has arrived
       volatile int never = 0;
       WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
-      for (int st = 0; st < F_STAGES && st < n_arm; ++st) {
-        const int last = st + F_STAGES * ((n_arm - 1 - st) / F_STAGES);
-        if (leader) mbar_wait_cluster(&full[st], (last / F_STAGES) & 1, drain);
-        mbar_wait_cluster(&empty[st], (last / F_STAGES) & 1, drain);
+      for (int st = 0; st < STAGES && st < n_arm; ++st) {
+        const int last = st + STAGES * ((n_arm - 1 - st) / STAGES);
+        if (leader) mbar_wait_cluster(&full[st], (last / STAGES) & 1, drain);
+        mbar_wait_cluster(&empty[st], (last / STAGES) & 1, drain);
       }
     }
   } else if (warp == 1) {
@@ -276,19 +304,19 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             tc_fence_after();
             if (lane == 0) {
               const uint32_t a_base = smem_u32(sA + s * F_A_STAGE);
-              const uint32_t b_base = smem_u32(sB + s * F_B_STAGE);
-              const uint32_t d = d0 + static_cast<uint32_t>((kb / F_CHUNK_KB) * F_BN);
+              const uint32_t b_base = smem_u32(sB + s * B_STAGE);
+              const uint32_t d = d0 + static_cast<uint32_t>((kb / F_CHUNK_KB) * NB);
               const bool first = (kb % F_CHUNK_KB) == 0;
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
-                const uint64_t bdesc = smem_desc_sw128(b_base + kk * KK_B, F_B_STAGE, 1024);
+                const uint64_t bdesc = smem_desc_sw128(b_base + kk * KK_B, 8192, 1024);
                 umma_pair<0>(d, adesc, bdesc, IDESC, (first && kk == 0) ? 0u : 1u);
               }
               umma_commit_pair(&empty[s], 0x3);
             }
             __syncwarp();
-            if (++s == F_STAGES) { s = 0; ph ^= 1; }
+            if (++s == STAGES) { s = 0; ph ^= 1; }
           }
           if (!ok) break;
           if (lane == 0) umma_commit_pair(&tfull[acc], 0x3);
@@ -307,8 +335,10 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     }  // the odd CTA's MMA warp has nothing to do: its stages complete on the even CTA
   } else {
     // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
     const int q = warp & 3;                  // TMEM lane quarter of this warp
-    uint8_t* stage = sOut + q * F_OUT_STAGE;
+    const int cbase = (ew >> 2) * 128;       // this warp's 128 columns of the tile
+    uint8_t* stage = sOut + ew * F_OUT_STAGE;
     const uint32_t row_off = static_cast<uint32_t>(lane) * 128;
     const uint32_t leader_tempty = map_to_rank(tempty, 0);
     int acc = 0;
@@ -319,42 +349,42 @@ __global__ void __launch_bounds__(F_THREADS, 1)
       const int grow0 = mt * 256 + static_cast<int>(rank) * 128 + q * 32;
       const int grow = grow0 + lane;
       const bool valid = grow < p.m;
-      const int ncols = min(F_BN, p.n - nt * F_BN);   // 64 or 128 (n is a multiple of 64)
-      float sum[F_BN];
+      const int c0 = nt * NB + cbase;                 // first output column of this warp
+      const int ncols = min(128, p.n - c0);           // <= 0, 64 or 128 (n % 64 == 0)
+      float sum[128];
 #pragma unroll
-      for (int i = 0; i < F_BN; ++i) sum[i] = 0.f;
+      for (int i = 0; i < 128; ++i) sum[i] = 0.f;
       for (int r = 0; r < p.W; ++r) {
         if (lane == 0) ok = mbar_wait_cluster(&tfull[acc], aph, ctl);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t tbase = tmem_base + acc * acc_cols + (static_cast<uint32_t>(q * 32) << 16);
+        const uint32_t tbase = tmem_base + acc * acc_cols + static_cast<uint32_t>(cbase) +
+                               (static_cast<uint32_t>(q * 32) << 16);
         const float xr = valid ? __ldg(p.xs + static_cast<int64_t>(r) * p.m + grow) : 0.f;
-        const float* wr = p.ws + static_cast<int64_t>(r) * p.n + nt * F_BN;
+        const float* wr = p.ws + static_cast<int64_t>(r) * p.n + c0;
 #pragma unroll
-        for (int g = 0; g < F_BN / 32; ++g) {
-          if (g * 32 < ncols) {   // no scales exist past column n
-            int32_t si[32];
+        for (int g = 0; g < 128 / GW; ++g) {
+          if (g * GW < ncols) {   // no scales exist past column n
+            int32_t si[GW];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) si[i] = 0;
+            for (int i = 0; i < GW; ++i) si[i] = 0;
 #pragma unroll 1
             for (int c = 0; c < nchunk; ++c) {   // exact int32 sum of the chunk sums
-              uint32_t v[32];
-              tmem_ld32(tbase + c * F_BN + g * 32, v);
+              uint32_t v[GW];
+              tmem_ld_group<GW>(tbase + c * NB + g * GW, v);
               tmem_ld_wait();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) si[i] += __float2int_rn(__uint_as_float(v[i]));
+              for (int i = 0; i < GW; ++i) si[i] += __float2int_rn(__uint_as_float(v[i]));
             }
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const float4 w4 = __ldg(reinterpret_cast<const float4*>(wr + g * 32 + i));
-              sum[g * 32 + i] = __fmaf_rn(xr * w4.x, static_cast<float>(si[i]), sum[g * 32 + i]);
-              sum[g * 32 + i + 1] =
-                  __fmaf_rn(xr * w4.y, static_cast<float>(si[i + 1]), sum[g * 32 + i + 1]);
-              sum[g * 32 + i + 2] =
-                  __fmaf_rn(xr * w4.z, static_cast<float>(si[i + 2]), sum[g * 32 + i + 2]);
-              sum[g * 32 + i + 3] =
-                  __fmaf_rn(xr * w4.w, static_cast<float>(si[i + 3]), sum[g * 32 + i + 3]);
+            for (int i = 0; i < GW; i += 4) {
+              const float4 w4 = __ldg(reinterpret_cast<const float4*>(wr + g * GW + i));
+              float* sp = sum + g * GW + i;
+              sp[0] = __fmaf_rn(xr * w4.x, static_cast<float>(si[i]), sp[0]);
+              sp[1] = __fmaf_rn(xr * w4.y, static_cast<float>(si[i + 1]), sp[1]);
+              sp[2] = __fmaf_rn(xr * w4.z, static_cast<float>(si[i + 2]), sp[2]);
+              sp[3] = __fmaf_rn(xr * w4.w, static_cast<float>(si[i + 3]), sp[3]);
             }
           }
         }
@@ -370,7 +400,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
       if (!ok) break;
       if (grow0 < p.m) {  // rows past m fall outside the output map and are not written
 #pragma unroll
-        for (int h = 0; h < F_BN / 64; ++h) {
+        for (int h = 0; h < 2; ++h) {
           if (h * 64 < ncols) {
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
@@ -385,7 +415,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmOut, stage, nt * F_BN + h * 64, grow0);
+              tma_store_2d(&tmOut, stage, c0 + h * 64, grow0);
               bulk_commit();
             }
             __syncwarp();
@@ -403,6 +433,45 @@ __global__ void __launch_bounds__(F_THREADS, 1)
   if (warp == 1) tmem_dealloc_pair(tmem_base, F_TMEM_COLS);
 }
 
+template <int NB>
+cudaError_t launch_fused(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tOut,
+                         FParams p, cudaStream_t st) {
+  using C = FCfg<NB>;
+  p.n_tiles = (p.n + NB - 1) / NB;
+  p.total = ((p.m + 255) / 256) * p.n_tiles;
+  // Persistent grid: as many pairs as can be resident at once (a pair needs
+  // two SMs of one GPC, so this can be fewer than SMs / 2).
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(mmrs_fused_kernel<NB>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(C::kSmem));
+    if (attr_err != cudaSuccess) return;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms() & ~1, 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, mmrs_fused_kernel<NB>, &cfg) !=
+        cudaSuccess)
+      max_clusters = 0;
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+  const int grid = 2 * std::min(max_clusters, std::max(p.total, 1));
+  return launch_kernel(mmrs_fused_kernel<NB>, dim3(grid), dim3(C::kThreads), C::kSmem, st, 2, tA,
+                       tB, tOut, p);
+}
+
+// 256-column tiles while two K chunks fit in TMEM (K <= 2048), else 128.
 cudaError_t launch_mmrs_fused(const mc2_mmrs_shape_t& s, const void* x1b, const void* x2b,
                               const float* xs, const float* ws, void* out, int32_t* dev_status,
                               cudaStream_t st) {
@@ -421,38 +490,10 @@ cudaError_t launch_mmrs_fused(const mc2_mmrs_shape_t& s, const void* x1b, const 
   p.m = s.m;
   p.n = s.n;
   p.K = s.k;
-  p.n_tiles = (s.n + F_BN - 1) / F_BN;
-  p.total = ((s.m + 255) / 256) * p.n_tiles;
   p.nchunk = (s.k / 64 + F_CHUNK_KB - 1) / F_CHUNK_KB;
   p.wait_limit_ns = wait_limit_ns();
-  // Persistent grid: as many pairs as can be resident at once (a pair needs
-  // two SMs of one GPC, so this can be fewer than SMs / 2).
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  static int max_clusters = 0;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(mmrs_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(F_SMEM_BYTES));
-    if (attr_err != cudaSuccess) return;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(num_sms() & ~1, 1, 1);
-    cfg.blockDim = dim3(F_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = F_SMEM_BYTES;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, mmrs_fused_kernel, &cfg) != cudaSuccess)
-      max_clusters = 0;
-  });
-  if (attr_err != cudaSuccess) return attr_err;
-  if (max_clusters < 1) return cudaErrorInvalidConfiguration;
-  const int grid = 2 * std::min(max_clusters, std::max(p.total, 1));
-  const cudaError_t e = launch_kernel(mmrs_fused_kernel, dim3(grid), dim3(F_THREADS), F_SMEM_BYTES,
-                                      st, 2, tA, tB, tOut, p);
+  const cudaError_t e = p.nchunk <= 2 ? launch_fused<256>(tA, tB, tOut, p, st)
+                                      : launch_fused<128>(tA, tB, tOut, p, st);
   note_launches(1);
   return e;
 }
