@@ -381,12 +381,10 @@ mc2_status_t mc2_prepack_weights(const mc2_shape_t* s, const void* w1, const voi
   const WsLayout L = ws_layout(*s);
   char* w = static_cast<char*>(ws);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_i8_to_bf16(static_cast<const int8_t*>(w1), w + L.w1_b16,
-                                    static_cast<size_t>(s->E) * s->H * 2 * s->I, st);
-  if (e == cudaSuccess)
-    e = launch_i8_to_bf16(static_cast<const int8_t*>(w2), w + L.w2_b16,
-                          static_cast<size_t>(s->E) * s->I * s->H, st);
-  return cuda_status(e);
+  return cuda_status(launch_i8_to_bf16_2(static_cast<const int8_t*>(w1), w + L.w1_b16,
+                                         static_cast<size_t>(s->E) * s->H * 2 * s->I,
+                                         static_cast<const int8_t*>(w2), w + L.w2_b16,
+                                         static_cast<size_t>(s->E) * s->I * s->H, st));
 }
 
 mc2_status_t mc2_selftest_wait(uint64_t limit_ns, int32_t* dev_status, void* stream) {

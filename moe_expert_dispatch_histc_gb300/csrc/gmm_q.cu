@@ -392,21 +392,25 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
-// int8 -> bf16 (exact), 16 values per thread step
-__global__ void i8_to_bf16_kernel(const int8_t* __restrict__ src, __nv_bfloat16* __restrict__ dst,
-                                  size_t n16) {
+// int8 -> bf16 (exact), 16 values per thread step, over one or two tensors
+// (one launch: segment 0 then segment 1 in one grid-stride range)
+__global__ void i8_to_bf16_kernel(const int8_t* __restrict__ src0, __nv_bfloat16* __restrict__ dst0,
+                                  size_t n16_0, const int8_t* __restrict__ src1,
+                                  __nv_bfloat16* __restrict__ dst1, size_t n16_1) {
   griddep_wait();
   griddep_launch_dependents();
   size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-  for (; i < n16; i += stride) {
-    const int4 v = __ldg(reinterpret_cast<const int4*>(src) + i);
+  for (; i < n16_0 + n16_1; i += stride) {
+    const bool first = i < n16_0;
+    const size_t j = first ? i : i - n16_0;
+    const int4 v = __ldg(reinterpret_cast<const int4*>(first ? src0 : src1) + j);
     const int8_t* b = reinterpret_cast<const int8_t*>(&v);
     uint32_t w[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      w[j] = pack_bf16x2(static_cast<float>(b[2 * j]), static_cast<float>(b[2 * j + 1]));
-    uint4* d = reinterpret_cast<uint4*>(dst) + 2 * i;
+    for (int t = 0; t < 8; ++t)
+      w[t] = pack_bf16x2(static_cast<float>(b[2 * t]), static_cast<float>(b[2 * t + 1]));
+    uint4* d = reinterpret_cast<uint4*>(first ? dst0 : dst1) + 2 * j;
     d[0] = make_uint4(w[0], w[1], w[2], w[3]);
     d[1] = make_uint4(w[4], w[5], w[6], w[7]);
   }
@@ -443,16 +447,24 @@ __global__ void requant_rows_kernel(const float* __restrict__ h, const int32_t* 
   }
 }
 
-cudaError_t launch_i8_to_bf16(const int8_t* src, void* dst, size_t n, cudaStream_t st) {
-  if (n == 0) return cudaSuccess;
-  const size_t n16 = n / 16;  // every int8 tensor of the block has a multiple of 64 elements
+cudaError_t launch_i8_to_bf16_2(const int8_t* src0, void* dst0, size_t n0, const int8_t* src1,
+                                void* dst1, size_t n1, cudaStream_t st) {
+  // every int8 tensor converted here has a multiple of 64 elements
+  const size_t n16_0 = n0 / 16, n16_1 = n1 / 16;
+  if (n16_0 + n16_1 == 0) return cudaSuccess;
   const int threads = 256;
-  const unsigned blocks =
-      static_cast<unsigned>(std::min<size_t>((n16 + threads - 1) / threads, 152 * 32));
-  const cudaError_t e = launch_kernel(i8_to_bf16_kernel, dim3(blocks), dim3(threads), 0, st, 1,
-                                      src, static_cast<__nv_bfloat16*>(dst), n16);
+  const unsigned blocks = static_cast<unsigned>(
+      std::min<size_t>((n16_0 + n16_1 + threads - 1) / threads, 152 * 32));
+  const cudaError_t e =
+      launch_kernel(i8_to_bf16_kernel, dim3(blocks), dim3(threads), 0, st, 1, src0,
+                    static_cast<__nv_bfloat16*>(dst0), n16_0, src1,
+                    static_cast<__nv_bfloat16*>(dst1), n16_1);
   note_launches(1);
   return e;
+}
+
+cudaError_t launch_i8_to_bf16(const int8_t* src, void* dst, size_t n, cudaStream_t st) {
+  return launch_i8_to_bf16_2(src, dst, n, nullptr, nullptr, 0, st);
 }
 
 cudaError_t launch_requant(const float* h, const int32_t* offsets, const mc2_shape_t& s, int8_t* hq,

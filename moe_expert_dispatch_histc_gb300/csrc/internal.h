@@ -131,6 +131,9 @@ struct QArgs {
 };
 cudaError_t launch_gemm_q(const QArgs& g, cudaStream_t st);
 cudaError_t launch_i8_to_bf16(const int8_t* src, void* dst, size_t n, cudaStream_t st);
+// the same for two tensors in one launch
+cudaError_t launch_i8_to_bf16_2(const int8_t* src0, void* dst0, size_t n0, const int8_t* src1,
+                                void* dst1, size_t n1, cudaStream_t st);
 cudaError_t launch_requant(const float* h, const int32_t* offsets, const mc2_shape_t& s, int8_t* hq,
                            float* hs, cudaStream_t st);
 

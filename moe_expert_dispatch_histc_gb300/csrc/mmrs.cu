@@ -527,10 +527,9 @@ extern "C" mc2_status_t mc2_mm_reduce_scatter_i8(const mc2_mmrs_shape_t* s, cons
   const MmrsLayout L = mmrs_layout(*s);
   char* w = static_cast<char*>(ws);
   const int64_t rows = static_cast<int64_t>(s->W) * s->m;
-  cudaError_t e = launch_i8_to_bf16(x1, w + L.x1_b16, static_cast<size_t>(rows) * s->k, st);
-  if (e == cudaSuccess)
-    e = launch_i8_to_bf16(x2, w + L.x2_b16, static_cast<size_t>(s->W) * s->k * s->n, st);
-  if (mmrs_path_override() != 1) {  // fused: one kernel after the two copies
+  cudaError_t e = launch_i8_to_bf16_2(x1, w + L.x1_b16, static_cast<size_t>(rows) * s->k, x2,
+                                      w + L.x2_b16, static_cast<size_t>(s->W) * s->k * s->n, st);
+  if (mmrs_path_override() != 1) {  // fused: one kernel after the copies
     if (e == cudaSuccess)
       e = launch_mmrs_fused(*s, w + L.x1_b16, w + L.x2_b16, x1_scale, x2_scale, out, dev_status, st);
     return e == cudaSuccess ? MC2_OK : MC2_ERR_CUDA;

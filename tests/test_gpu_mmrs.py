@@ -33,7 +33,7 @@ def _call(s, d, ws, m, n, path):
     B.mc2_mm_reduce_scatter_i8(s, d[0], d[1], d[2], d[3], out, ws, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    assert B.mc2_last_launch_count() == (3 if path == 0 else 5)
+    assert B.mc2_last_launch_count() == (2 if path == 0 else 4)
     return out
 
 
