@@ -16,7 +16,11 @@
 //   fc2: acc2 = h_q @ w2_q[e];  y = (hs[p] * w2s[e, n]) * acc2 -> scaled fp16 -> combine
 //
 // Tiles are 128 x 128 (fc1: 64 gate + 64 up columns), 6 stages of 32 KB, one
-// CTA per SM, the same warp roles as the bf16 kernel.  Operands are bf16
+// CTA per SM, the same warp roles as the bf16 kernel.  TMEM is a ring of four
+// 128-column chunk slots: chunk g of a CTA accumulates in slot g % 4, the
+// epilogue reads a tile's chunks once its last one is committed and then frees
+// their slots, so the MMAs of the next tile run during the epilogue (two tiles
+// in flight for K <= 2048, one chunk ahead for K <= 3072).  Operands are bf16
 // copies of the int8 tensors: weights expanded once by mc2_prepack_weights,
 // x and h_q per call.
 #include <algorithm>
@@ -31,6 +35,7 @@ constexpr int QB_STAGE = 16384;                // 64 K rows x 128 columns x 2 B
 constexpr int QSTAGE_BYTES = A_STAGE + QB_STAGE;
 constexpr int QCHUNK_KB = 16;                  // k-blocks (of 64) per exact fp32 chunk: K 1024
 constexpr int QMAX_CHUNKS = 4;                 // K <= 4096
+constexpr int QSLOTS = 4;                      // TMEM chunk slots of QBN columns (512 in all)
 constexpr size_t QSMEM_BYTES_FIXED = 1024 + QSTAGES * QSTAGE_BYTES + 4 * OUT_STAGE + 256;
 
 struct QParams {
@@ -70,9 +75,9 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
   uint8_t* sOut = sB + QSTAGES * QB_STAGE;
   uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * OUT_STAGE);
   uint64_t* empty = full + QSTAGES;
-  uint64_t* tfull = empty + QSTAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* mma_done = tempty + 2;
+  uint64_t* tfull = empty + QSTAGES;        // per TMEM chunk slot
+  uint64_t* tempty = tfull + QSLOTS;
+  uint64_t* mma_done = tempty + QSLOTS;
   uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_sh = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
   int32_t* prefix = reinterpret_cast<int32_t*>(tmem_base_sh + 2);
@@ -80,14 +85,13 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
   const int nchunk = p.nchunk;
-  const int bufs = nchunk <= 2 ? 2 : 1;      // accumulator sets that fit in 512 columns
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < QSTAGES; ++s) {
       mbar_init(&full[s], GATHER ? 1 + 32 * QRoles<MODE>::kGatherWarps : 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < QSLOTS; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 4 * 32);
     }
@@ -175,18 +179,25 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Chunk g of this CTA (tiles in order, chunks within a tile) accumulates
+    // in TMEM slot g % 4; a slot is reused once the epilogue has read it.
     int s = 0;
     uint32_t ph = 0;
-    int acc = 0;
-    uint32_t aph = 0;
+    int g = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      if (lane == 0) ok = mbar_wait(&tempty[acc], aph ^ 1, ctl);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t d0 = tmem_base + acc * 256;
+      uint32_t d = 0;
+      int slot = 0;
       for (int kb = 0; kb < kblocks; ++kb) {
+        if (kb % QCHUNK_KB == 0) {  // next chunk: wait until its slot is free
+          slot = g & (QSLOTS - 1);
+          if (lane == 0) ok = mbar_wait(&tempty[slot], ((g / QSLOTS) & 1) ^ 1, ctl);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          tc_fence_after();
+          d = tmem_base + static_cast<uint32_t>(slot * QBN);
+          ++g;
+        }
         if (lane == 0) {
           ok = mbar_wait(&full[s], ph, ctl);
           if (GATHER && ok) fence_proxy_async_smem();  // gathered rows -> async proxy
@@ -197,9 +208,7 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
         if (lane == 0) {
           const uint32_t a_base = smem_u32(sA + s * A_STAGE);
           const uint32_t b_base = smem_u32(sB + s * QB_STAGE);
-          const int chunk = kb / QCHUNK_KB;
           const bool first_of_chunk = (kb % QCHUNK_KB) == 0;
-          const uint32_t d = d0 + chunk * QBN;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
@@ -212,10 +221,8 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
         if (++s == QSTAGES) { s = 0; ph ^= 1; }
       }
       if (!ok) break;
-      if (lane == 0) umma_commit(&tfull[acc]);
+      if (lane == 0) umma_commit(&tfull[slot]);  // the tile's last chunk slot
       __syncwarp();
-      if (bufs == 2) acc ^= 1;
-      if (acc == 0) aph ^= 1;
     }
     if (lane == 0) {
       umma_commit(mma_done);
@@ -264,17 +271,19 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
     const int q = warp & 3;
     uint8_t* stage = sOut + q * OUT_STAGE;
     const uint32_t row_off = static_cast<uint32_t>(lane) * 128;
-    int acc = 0;
-    uint32_t aph = 0;
+    int g = 0;              // first chunk of the current tile (same count as the MMA warp)
+    uint32_t tf_phase = 0;  // bit b: parity of the next tfull[b] completion
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, n, row0, rows;
       decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(&tfull[acc], aph, ctl);
+      const int last = (g + nchunk - 1) & (QSLOTS - 1);
+      if (lane == 0) ok = mbar_wait(&tfull[last], (tf_phase >> last) & 1, ctl);
+      tf_phase ^= 1u << last;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + acc * 256 + (static_cast<uint32_t>(q * 32) << 16);
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
       const int wrows = min(32, rows - q * 32);
       const int grow0 = row0 + q * 32;
       const int grow = grow0 + lane;
@@ -303,12 +312,13 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
           for (int i = 0; i < 32; ++i) { s0[i] = 0; s1[i] = 0; }
 #pragma unroll 1
           for (int c = 0; c < nchunk; ++c) {
+            const uint32_t cs_base = tbase + ((g + c) & (QSLOTS - 1)) * QBN;
             uint32_t v[32];
-            tmem_ld32(tbase + c * QBN + gi * GW, v);
+            tmem_ld32(cs_base + gi * GW, v);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) s0[i] += __float2int_rn(__uint_as_float(v[i]));
-            tmem_ld32(tbase + c * QBN + gi * GW + S1_OFF, v);
+            tmem_ld32(cs_base + gi * GW + S1_OFF, v);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) s1[i] += __float2int_rn(__uint_as_float(v[i]));
@@ -378,9 +388,8 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
-      if (bufs == 2) acc ^= 1;
-      if (acc == 0) aph ^= 1;
+      for (int c = 0; c < nchunk; ++c) mbar_arrive(&tempty[(g + c) & (QSLOTS - 1)]);
+      g += nchunk;
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();

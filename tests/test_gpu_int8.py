@@ -121,3 +121,44 @@ def test_int8_full_size_sampled():
     ok, a, m = orc.bf16_tolerance_ok(out[toks], ref)
     assert ok, f"int8 sampled out: max {a:.3e}, mean {m:.3e}"
     assert int(b.dev_status.item()) == 0
+
+
+def test_int8_full_size_accumulators_sampled():
+    """The int8 workload at full size: fc1 sums K = 3072 in three exact chunks
+    and fc2 K = 1536 in two, and every CTA takes several tiles, so the TMEM
+    chunk-slot ring wraps many times.  Sampled permuted rows of both int32
+    accumulators (random rows, the first and last row of experts) bit-exact
+    against int64 products over the oracle's permutation."""
+    wl = WORKLOADS["int8"]
+    inp = make_inputs(wl, 3)
+    d, b = _run(wl, inp, out="i32")
+    acc1 = to_np(b.h)
+    _, src = orc.permute(np.zeros((wl.T, 1)), inp["sel"], wl.E)
+    offs = orc.expert_offsets(orc.rank_counts(inp["sel"], wl.E, wl.W))
+    n = int(offs[-1])
+    assert np.array_equal(to_np(b.permute_src)[:n], src[:n])
+    # fc2 in raw mode on random int8 rows
+    rng = np.random.default_rng(11)
+    hq = rng.integers(-127, 128, (wl.R, wl.I)).astype(np.int8)
+    acc2 = torch.empty((wl.R, wl.H), dtype=torch.int32, device="cuda")
+    B.mc2_gmm_alltoallv(blk.shape_of(wl, "i32"), torch.from_numpy(hq).cuda(), None, d["w2"], None,
+                        b.offsets, b.permute_src, None, None, b.ws, acc2, b.dev_status)
+    torch.cuda.synchronize()
+    acc2 = to_np(acc2)
+    assert int(b.dev_status.item()) == 0
+    rows = set(rng.choice(n, 40, replace=False).tolist())
+    for e in rng.choice(wl.E, 6, replace=False):
+        if offs[e + 1] > offs[e]:
+            rows |= {int(offs[e]), int(offs[e + 1]) - 1}
+    by_expert = {}
+    for p in sorted(rows):
+        by_expert.setdefault(int(np.searchsorted(offs, p, side="right") - 1), []).append(p)
+    for e, ps in by_expert.items():
+        w1 = inp["w1"][e].astype(np.int64)
+        w2 = inp["w2"][e].astype(np.int64)
+        for p in ps:
+            t = int(src[p] // wl.k)
+            assert np.array_equal(acc1[p].astype(np.int64), inp["x"][t].astype(np.int64) @ w1), \
+                f"fc1 row {p} (expert {e})"
+            assert np.array_equal(acc2[p].astype(np.int64), hq[p].astype(np.int64) @ w2), \
+                f"fc2 row {p} (expert {e})"
