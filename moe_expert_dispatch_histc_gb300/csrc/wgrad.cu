@@ -15,9 +15,8 @@
 // order, so each tile is written once (no split over K, no atomics).
 //
 // Warp roles: warp 0 TMA producer, warp 1 MMA issuer (all 32 lanes zero the
-// ragged rows), warps 2-5 epilogue (TMEM -> fp32 -> TMA store through two
-// staging buffers per warp, so one store drains while the next is staged;
-// zero tiles of experts without rows).
+// ragged rows), warps 2-5 epilogue (TMEM -> fp32 -> TMA store; zero tiles of
+// experts without rows).
 #include <algorithm>
 #include <mutex>
 
@@ -33,8 +32,8 @@ constexpr int WG_STAGES = 4;
 constexpr int WG_A_STAGE = 2 * 8192;           // two [64 rows][64 cols] blocks
 constexpr int WG_B_STAGE = 4 * 8192;           // four blocks
 constexpr int WG_STAGE_BYTES = WG_A_STAGE + WG_B_STAGE;
-constexpr int WG_OUT_STAGE = 4096;             // 32 rows x 32 fp32; two per epilogue warp
-constexpr size_t WG_SMEM = 1024 + WG_STAGES * WG_STAGE_BYTES + 8 * WG_OUT_STAGE + 256;
+constexpr int WG_OUT_STAGE = 4096;             // per epilogue warp: 32 rows x 32 fp32
+constexpr size_t WG_SMEM = 1024 + WG_STAGES * WG_STAGE_BYTES + 4 * WG_OUT_STAGE + 256;
 constexpr int WG_THREADS = 6 * 32;
 
 struct WgradParams {
@@ -62,7 +61,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + WG_STAGES * WG_A_STAGE;
   uint8_t* sOut = sB + WG_STAGES * WG_B_STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 8 * WG_OUT_STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * WG_OUT_STAGE);
   uint64_t* empty = full + WG_STAGES;
   uint64_t* tfull = empty + WG_STAGES;
   uint64_t* tempty = tfull + 2;
@@ -199,8 +198,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
-    uint8_t* stages = sOut + q * 2 * WG_OUT_STAGE;  // two staging buffers: one store in flight
-    int nst = 0;                                     // stores issued by this warp
+    uint8_t* stage = sOut + q * WG_OUT_STAGE;
     int acc = 0;
     uint32_t aph = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -220,8 +218,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
         for (int gi = 0; gi < WG_BN / 32; ++gi) {
           const int col0 = n * WG_BN + gi * 32;
           if (col0 >= p.N) break;
-          uint8_t* stage = stages + (nst & 1) * WG_OUT_STAGE;
-          if (lane == 0) bulk_wait_read_but_one();  // the store from this buffer is read out
+          if (lane == 0) bulk_wait_read_all();
           __syncwarp();
           uint32_t v[32];
           if (!empty_expert) {
@@ -241,7 +238,6 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
             tma_store_2d(&tmOut, stage, col0, grow0);
             bulk_commit();
           }
-          ++nst;
           __syncwarp();
         }
       }
