@@ -387,6 +387,8 @@ def run_cuda(args):
     fc2_ms = float(seg[:, segi["fc2_combine"]].mean())
     fc1_flops = 2 * wl.R * wl.H * 2 * wl.I
     peak = float(peaks["bf16_tflops"])
+    if wl.act == "f32":   # tf32 tensor cores: the bf16 measured peak x the nominal 1.1 / 2.25
+        peak *= 1.1 / 2.25
     tflops = wl.flops / ((fc1_ms + fc2_ms) / 1e3) / 1e12
     # fc1's algorithmic bytes: the weights of experts that got rows, x, h
     offs = b.offsets.cpu().numpy().astype(np.int64)
@@ -400,18 +402,26 @@ def run_cuda(args):
                 "unit": "GB/s", "peak_source": f"{src} hbm_gbs"}
     else:
         roof = {"bound": "tensor", "achieved": fc1_flops / (fc1_ms / 1e3) / 1e12, "peak": peak,
-                "unit": "TFLOP/s", "peak_source": f"{src} bf16_tflops (burst)"}
+                "unit": "TFLOP/s",
+                "peak_source": f"{src} bf16_tflops (burst)" +
+                               (" x 1.1/2.25 (nominal tf32 : bf16)" if wl.act == "f32" else "")}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["algorithmic"] = {"flops": fc1_flops, "bytes": fc1_bytes}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "tf32 (fp32 storage)" if wl.act == "f32" else "bf16",
         "data": "synthetic", "config": _config(wl, l2="flushed (256 MB write) between steps"),
         "tflops": tflops, "tflops_frac_of_peak": tflops / peak,
         "segments_ms": {name: float(seg[:, i].mean()) for name, i in segi.items()},
         "roofline": {"kernel": ("gmm_kernel<fc1 rows> (fc1 + SwiGLU on materialised rows)"
                                 if unfused else
+                                "gmm_q_kernel<fc1> (permute gather + exact int8 fc1 + dequant + "
+                                "SwiGLU), timed over its segment, which also holds the x copy to "
+                                "bf16 and the row requant" if wl.act == "i8" else
+                                "gmm_kernel<fc1, tf32> (permute gather + fc1 + SwiGLU)"
+                                if wl.act == "f32" else
                                 "gmm_kernel<fc1> (permute gather + fc1 + SwiGLU)"),
                      **roof,
                      "traffic": None if unfused else _ncu_traffic("gmm_fc1", wl.name)},
