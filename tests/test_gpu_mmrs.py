@@ -97,3 +97,33 @@ def test_mm_reduce_scatter_empty_and_rejected():
     bad = B.MmrsShape(6, 256, 128, 4)   # m not divisible by W
     assert B.mc2_mm_reduce_scatter_i8(bad, x2, x2s, x2, x2s, x2, ws, None,
                                       check=False) == B.MC2_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("W,m,k,n", [(2, 8192, 512, 2048), (2, 4096, 3072, 2048)])
+def test_mm_reduce_scatter_many_tiles_per_cluster(W, m, k, n):
+    """Shapes where every CTA pair of the fused kernel takes three or more
+    output tiles (256-column tiles with two accumulator sets at k = 512;
+    128-column tiles with three K chunks at k = 3072), so accumulators and
+    barrier phases are reused across tiles.  The fused result must equal the
+    two-pass result bit for bit; sampled rows of both, and the two-pass int32
+    partials, against the oracle on those rows."""
+    ensure_built()
+    rng = np.random.default_rng(k + n)
+    x1 = rng.integers(-127, 128, (W, m, k)).astype(np.int8)
+    x2 = rng.integers(-127, 128, (W, k, n)).astype(np.int8)
+    x1s = rng.uniform(1e-3, 1e-2, (W, m)).astype(np.float32)
+    x2s = rng.uniform(1e-3, 1e-2, (W, n)).astype(np.float32)
+    s = B.MmrsShape(m, k, n, W)
+    ws = torch.empty(B.mc2_mm_reduce_scatter_workspace_bytes(s), dtype=torch.uint8, device="cuda")
+    d = [torch.from_numpy(a).cuda() for a in (x1, x1s, x2, x2s)]
+    two = _call(s, d, ws, m, n, 1)
+    off = _align(W * m * k * 2) + _align(W * k * n * 2)
+    acc = ws[off:off + W * m * n * 4].view(torch.int32).view(W, m, n)
+    fused = _call(s, d, ws, m, n, 0)
+    assert torch.equal(fused.view(torch.int16), two.view(torch.int16)), \
+        "fused result differs from the two-pass result"
+    rows = np.sort(np.concatenate([rng.choice(m, 14, replace=False), [0, m - 1]]))
+    ref_acc, ref_total, _ = orc.mm_reduce_scatter(x1[:, rows], x1s[:, rows], x2, x2s)
+    assert np.array_equal(acc[:, torch.from_numpy(rows).cuda()].cpu().numpy(), ref_acc)
+    ok, a, b = orc.bf16_tolerance_ok(fused.float().cpu().numpy()[rows], ref_total)
+    assert ok, (a, b)
