@@ -273,6 +273,7 @@ def run_cuda(args):
     from moe_expert_dispatch_histc_gb300.build import build
     build()
     B.lib()
+    B.mc2_set_tile_pairing({"auto": 0, "single": 1, "pairs": 2}[args.tiling])
 
     wl = WORKLOADS[args.workload]
     inp = make_inputs(wl, 0)
@@ -437,6 +438,8 @@ def run_cuda(args):
     }
     if unfused:
         line["config"]["path"] = "unfused: materialised permute + plain grouped fc1"
+    if args.tiling != "auto":
+        line["config"]["tiling"] = args.tiling
     if wl.act == "i8":
         line["weight_prepack_ms"] = t_prepack * 1e3
         line["dtype"] = "int8 (exact, on bf16 tensor cores)"
@@ -696,6 +699,9 @@ def main():
                     help="unfused: the non-fused baseline (materialised permute, plain grouped "
                          "fc1), bf16 workloads only; twopass (--op mm_reduce_scatter): int32 "
                          "partials through memory, then a reduce kernel")
+    ap.add_argument("--tiling", default="auto", choices=["auto", "single", "pairs"],
+                    help="grouped-GEMM tiling of the block (mc2_set_tile_pairing): both give "
+                         "the same bits")
     ap.add_argument("--recompute-g", action="store_true",
                     help="--op backward: recompute G instead of taking the training forward's")
     ap.add_argument("--op", default="block", choices=["block", "backward", "mm_reduce_scatter"],

@@ -16,7 +16,11 @@
 //   fc2: acc2 = h_q @ w2_q[e];  y = (hs[p] * w2s[e, n]) * acc2 -> scaled fp16 -> combine
 //
 // Tiles are 128 x 128 (fc1: 64 gate + 64 up columns), 6 stages of 32 KB, one
-// CTA per SM, the same warp roles as the bf16 kernel.  TMEM is a ring of four
+// CTA per SM, the same warp roles as the bf16 kernel; or, when experts
+// average 256 rows or more, 256 x 128 tiles on CTA pairs (cta_group::2: each
+// CTA streams its 128 rows and one 64-column block of B, 24 KB per stage, 8
+// stages; fc2's odd CTA loads onto the even CTA's stage barrier, fc1's odd CTA
+// relays its gathered stages).  TMEM is a ring of four
 // 128-column chunk slots: chunk g of a CTA accumulates in slot g % 4, the
 // epilogue reads a tile's chunks once its last one is committed and then frees
 // their slots, so the MMAs of the next tile run during the epilogue (two tiles
@@ -30,13 +34,9 @@
 namespace mc2 {
 
 constexpr int QBN = 128;                       // UMMA N
-constexpr int QSTAGES = 6;
-constexpr int QB_STAGE = 16384;                // 64 K rows x 128 columns x 2 B
-constexpr int QSTAGE_BYTES = A_STAGE + QB_STAGE;
 constexpr int QCHUNK_KB = 16;                  // k-blocks (of 64) per exact fp32 chunk: K 1024
 constexpr int QMAX_CHUNKS = 4;                 // K <= 4096
 constexpr int QSLOTS = 4;                      // TMEM chunk slots of QBN columns (512 in all)
-constexpr size_t QSMEM_BYTES_FIXED = 1024 + QSTAGES * QSTAGE_BYTES + 4 * OUT_STAGE + 256;
 
 struct QParams {
   const void* a_ptr;           // fc1: x as bf16 [T, H] (gathered)
@@ -57,25 +57,49 @@ struct QRoles {
   static constexpr int kThreads = (6 + kGatherWarps) * 32;
 };
 
-template <int MODE>
+// Pipeline geometry.  Single CTA: 128 x 128 tiles, a 16 KB B stage (two 64-
+// column blocks).  CTA pair (cta_group::2, UMMA M = 256, N = 128): each CTA
+// holds 128 rows of A and one 64-column block of B (fc1: the even CTA the gate
+// block, the odd CTA the matching up block; fc2: the first or second 64 of the
+// 128 output columns), 24 KB per stage instead of 32 KB, eight stages; each
+// CTA's TMEM holds its 128 rows x all 128 columns, so the epilogue is the
+// single-CTA one.
+template <bool PAIR>
+struct QGeom {
+  static constexpr int kStages = PAIR ? 8 : 6;
+  static constexpr int kBStage = PAIR ? 8192 : 16384;
+  static constexpr int kStageBytes = A_STAGE + kBStage;
+  static constexpr size_t kSmemFixed = 1024 + static_cast<size_t>(kStages) * kStageBytes +
+                                       4 * OUT_STAGE + 512;
+};
+
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
     gmm_q_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmOut, const QParams p) {
+  using G = QGeom<PAIR>;
   constexpr int BK = 64;
+  constexpr int STAGES = G::kStages;
+  constexpr int B_STAGE = G::kBStage;
   constexpr int B_BLOCK = BK * 128;          // 64 K rows x 64 columns
   constexpr int KK_B = 16 * 128;             // B bytes per UMMA K step
-  constexpr uint32_t IDESC = instr_desc(1, false, true, BM, QBN);
+  constexpr int TM = PAIR ? 2 * BM : BM;     // rows per tile
+  constexpr uint32_t IDESC = instr_desc(1, false, true, TM, QBN);
   constexpr bool GATHER = MODE == MODE_FC1;
+  // pair with TMA-loaded A: the odd CTA's copies complete on the even CTA's
+  // full[s]; pair with gathered rows: the odd CTA relays its stages (pfull)
+  constexpr bool DIRECT = PAIR && !GATHER;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + QSTAGES * A_STAGE;
-  uint8_t* sOut = sB + QSTAGES * QB_STAGE;
+  uint8_t* sB = smem + STAGES * A_STAGE;
+  uint8_t* sOut = sB + STAGES * B_STAGE;
   uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * OUT_STAGE);
-  uint64_t* empty = full + QSTAGES;
-  uint64_t* tfull = empty + QSTAGES;        // per TMEM chunk slot
+  uint64_t* pfull = full + STAGES;
+  uint64_t* empty = pfull + STAGES;
+  uint64_t* tfull = empty + STAGES;         // per TMEM chunk slot
   uint64_t* tempty = tfull + QSLOTS;
   uint64_t* mma_done = tempty + QSLOTS;
   uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -85,15 +109,20 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
   const int nchunk = p.nchunk;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int nunits = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < QSTAGES; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], GATHER ? 1 + 32 * QRoles<MODE>::kGatherWarps : 1);
+      mbar_init(&pfull[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < QSLOTS; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4 * 32);
+      mbar_init(&tempty[b], PAIR ? 2 * 4 : 4);  // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(mma_done, 1);
     *abort_sh = 0;
@@ -106,19 +135,24 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
     if (!p.raw) tma_prefetch_desc(&tmOut);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_base_sh, TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_base_sh, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_base_sh, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   griddep_wait();
   griddep_launch_dependents();
-  if (warp == 2) {
+  if (warp == 2) {  // per-expert tile prefix: ceil(rows_e / TM) * n_tiles
     int run = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + lane;
       int t = 0;
       if (e < E) {
         const int rows = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
-        t = ((rows + BM - 1) / BM) * p.n_tiles;
+        t = ((rows + TM - 1) / TM) * p.n_tiles;
       }
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -131,106 +165,185 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
     if (lane == 0) prefix[0] = 0;
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_base_sh;
-  const int total = prefix[E];
+  int total = prefix[E];
+  if constexpr (PAIR) {  // the pair's MMAs write one TMEM address in both CTAs
+    const uint32_t peer_base = ld_shared_cluster_u32(map_to_rank(tmem_base_sh, rank ^ 1u));
+    if (peer_base != tmem_base) {
+      if (threadIdx.x == 0 && p.dev_status) atomicOr(p.dev_status, 0x4);
+      total = 0;
+    }
+  }
   WaitCtl ctl{abort_sh, p.wait_limit_ns, p.dev_status};
   const int kblocks = p.K / BK;
 
+  // This CTA's rows of a tile: [row0, row0 + rows) (rows may be <= 0 for the
+  // odd CTA of a pair tile at an expert's end); pair0 is the tile's first row.
+  auto tile_rows = [&](int tile, int& e, int& n, int& pair0, int& row0, int& rows) {
+    int r0, rr;
+    decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, r0, rr);
+    if constexpr (PAIR) {  // decode_tile counts in BM rows; a pair tile spans 2 * BM
+      const int local = tile - prefix[e];
+      const int m_pairs = (prefix[e + 1] - prefix[e]) / p.n_tiles;
+      const int mp = local - (local / m_pairs) * m_pairs;
+      pair0 = __ldg(p.offsets + e) + mp * TM;
+      row0 = pair0 + static_cast<int>(rank) * BM;
+      rows = __ldg(p.offsets + e + 1) - row0;
+    } else {
+      pair0 = r0;
+      row0 = r0;
+      rows = rr;
+    }
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    const uint32_t leader_full = PAIR ? map_to_rank(full, 0) : 0u;
     int s = 0;
     uint32_t ph = 0;
     int n_arm = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      int e, n, row0, rows;
-      decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
+    for (int tile = unit; tile < total && ok; tile += nunits) {
+      int e, n, pair0, row0, rows;
+      tile_rows(tile, e, n, pair0, row0, rows);
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, ctl);
+        if (lane == 0) ok = PAIR ? mbar_wait_cluster(&empty[s], ph ^ 1, ctl)
+                                 : mbar_wait(&empty[s], ph ^ 1, ctl);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[s], GATHER ? QB_STAGE : QSTAGE_BYTES);
-          uint8_t* b_dst = sB + s * QB_STAGE;
+          uint8_t* a_dst = sA + s * A_STAGE;
+          uint8_t* b_dst = sB + s * B_STAGE;
           const int k0 = kb * BK;
-          if (!GATHER) tma_load_2d(sA + s * A_STAGE, &tmA, &full[s], k0, row0);
-          if (MODE == MODE_FC1) {  // 64 gate columns, then the 64 up columns
-            tma_load_3d(b_dst, &tmB, &full[s], n * 64, k0, e);
-            tma_load_3d(b_dst + B_BLOCK, &tmB, &full[s], p.I + n * 64, k0, e);
+          if constexpr (PAIR) {
+            // this CTA's 64 columns: fc1 gate (even) / up (odd) block n;
+            // fc2 the even or odd half of the 128 output columns
+            const int col = MODE == MODE_FC1 ? static_cast<int>(rank) * p.I + n * 64
+                                             : n * QBN + static_cast<int>(rank) * 64;
+            if (DIRECT && !leader) {
+              const uint32_t bar = leader_full + s * 8;
+              tma_load_2d_pair(a_dst, &tmA, bar, k0, row0);
+              tma_load_3d_pair(b_dst, &tmB, bar, col, k0, e);
+            } else {
+              mbar_arrive_expect_tx(&full[s], GATHER ? B_STAGE : 2 * G::kStageBytes);
+              if (!GATHER) tma_load_2d(a_dst, &tmA, &full[s], k0, row0);
+              tma_load_3d(b_dst, &tmB, &full[s], col, k0, e);
+            }
           } else {
-            tma_load_3d(b_dst, &tmB, &full[s], n * QBN, k0, e);
-            tma_load_3d(b_dst + B_BLOCK, &tmB, &full[s], n * QBN + 64, k0, e);
+            mbar_arrive_expect_tx(&full[s], GATHER ? B_STAGE : G::kStageBytes);
+            if (!GATHER) tma_load_2d(a_dst, &tmA, &full[s], k0, row0);
+            if (MODE == MODE_FC1) {  // 64 gate columns, then the 64 up columns
+              tma_load_3d(b_dst, &tmB, &full[s], n * 64, k0, e);
+              tma_load_3d(b_dst + B_BLOCK, &tmB, &full[s], p.I + n * 64, k0, e);
+            } else {
+              tma_load_3d(b_dst, &tmB, &full[s], n * QBN, k0, e);
+              tma_load_3d(b_dst + B_BLOCK, &tmB, &full[s], n * QBN + 64, k0, e);
+            }
           }
         }
         __syncwarp();
         ++n_arm;
-        if (++s == QSTAGES) { s = 0; ph ^= 1; }
+        if (++s == STAGES) { s = 0; ph ^= 1; }
       }
     }
-    if (lane == 0) {
+    if (lane == 0) {  // every armed stage has landed and every commit to it has arrived
       volatile int never = 0;
       WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
-      for (int st = 0; st < QSTAGES && st < n_arm; ++st) {
-        const int last = st + QSTAGES * ((n_arm - 1 - st) / QSTAGES);
-        mbar_wait(&full[st], (last / QSTAGES) & 1, drain);
+      for (int st = 0; st < STAGES && st < n_arm; ++st) {
+        const int last = st + STAGES * ((n_arm - 1 - st) / STAGES);
+        if (!DIRECT || leader) mbar_wait_cluster(&full[st], (last / STAGES) & 1, drain);
+        if (PAIR) mbar_wait_cluster(&empty[st], (last / STAGES) & 1, drain);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Chunk g of this CTA (tiles in order, chunks within a tile) accumulates
-    // in TMEM slot g % 4; a slot is reused once the epilogue has read it.
-    int s = 0;
-    uint32_t ph = 0;
-    int g = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      uint32_t d = 0;
-      int slot = 0;
-      for (int kb = 0; kb < kblocks; ++kb) {
-        if (kb % QCHUNK_KB == 0) {  // next chunk: wait until its slot is free
-          slot = g & (QSLOTS - 1);
-          if (lane == 0) ok = mbar_wait(&tempty[slot], ((g / QSLOTS) & 1) ^ 1, ctl);
+    if (leader) {
+      // ---------------------------------------------------------- MMA issuer
+      // Chunk g of this CTA (tiles in order, chunks within a tile) accumulates
+      // in TMEM slot g % 4; a slot is reused once the epilogue has read it.
+      int s = 0;
+      uint32_t ph = 0;
+      int g = 0;
+      bool ok = true;
+      for (int tile = unit; tile < total && ok; tile += nunits) {
+        uint32_t d = 0;
+        int slot = 0;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (kb % QCHUNK_KB == 0) {  // next chunk: wait until its slot is free
+            slot = g & (QSLOTS - 1);
+            if (lane == 0) {
+              const uint32_t par = ((g / QSLOTS) & 1) ^ 1;
+              ok = PAIR ? mbar_wait_cluster(&tempty[slot], par, ctl)
+                        : mbar_wait(&tempty[slot], par, ctl);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            d = tmem_base + static_cast<uint32_t>(slot * QBN);
+            ++g;
+          }
+          if (lane == 0) {
+            ok = mbar_wait_cluster(&full[s], ph, ctl);
+            if (ok && PAIR && !DIRECT) ok = mbar_wait_cluster(&pfull[s], ph, ctl);
+            if (GATHER && ok) fence_proxy_async_smem();  // gathered rows -> async proxy
+          }
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           tc_fence_after();
-          d = tmem_base + static_cast<uint32_t>(slot * QBN);
-          ++g;
-        }
-        if (lane == 0) {
-          ok = mbar_wait(&full[s], ph, ctl);
-          if (GATHER && ok) fence_proxy_async_smem();  // gathered rows -> async proxy
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a_base = smem_u32(sA + s * A_STAGE);
-          const uint32_t b_base = smem_u32(sB + s * QB_STAGE);
-          const bool first_of_chunk = (kb % QCHUNK_KB) == 0;
+          if (lane == 0) {
+            const uint32_t a_base = smem_u32(sA + s * A_STAGE);
+            const uint32_t b_base = smem_u32(sB + s * B_STAGE);
+            const bool first_of_chunk = (kb % QCHUNK_KB) == 0;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
-            const uint64_t bdesc = smem_desc_sw128(b_base + kk * KK_B, B_BLOCK, 1024);
-            umma<0>(d, adesc, bdesc, IDESC, (first_of_chunk && kk == 0) ? 0u : 1u);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+              const uint64_t bdesc = smem_desc_sw128(b_base + kk * KK_B, B_BLOCK, 1024);
+              const uint32_t acc = (first_of_chunk && kk == 0) ? 0u : 1u;
+              if constexpr (PAIR) umma_pair<0>(d, adesc, bdesc, IDESC, acc);
+              else umma<0>(d, adesc, bdesc, IDESC, acc);
+            }
+            if constexpr (PAIR) umma_commit_pair(&empty[s], 0x3);
+            else umma_commit(&empty[s]);
           }
-          umma_commit(&empty[s]);
+          __syncwarp();
+          if (++s == STAGES) { s = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        if (lane == 0) {  // the tile's last chunk slot
+          if constexpr (PAIR) umma_commit_pair(&tfull[slot], 0x3);
+          else umma_commit(&tfull[slot]);
         }
         __syncwarp();
-        if (++s == QSTAGES) { s = 0; ph ^= 1; }
       }
-      if (!ok) break;
-      if (lane == 0) umma_commit(&tfull[slot]);  // the tile's last chunk slot
+      if (lane == 0) {
+        if constexpr (PAIR) umma_commit_pair(mma_done, 0x1);
+        else umma_commit(mma_done);
+        volatile int never = 0;
+        WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
+        mbar_wait_cluster(mma_done, 0, drain);
+      }
       __syncwarp();
+    } else if (!DIRECT) {
+      // ---------------------------------------------------------- relay (odd CTA of a pair)
+      const uint32_t leader_pfull = map_to_rank(pfull, 0);
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int tile = unit; tile < total && ok; tile += nunits) {
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (lane == 0) {
+            ok = mbar_wait(&full[s], ph, ctl);
+            if (GATHER && ok) fence_proxy_async_smem();  // gathered rows -> async proxy
+            if (ok) mbar_arrive_remote_relaxed(leader_pfull + s * 8);
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (++s == STAGES) { s = 0; ph ^= 1; }
+        }
+      }
     }
-    if (lane == 0) {
-      umma_commit(mma_done);
-      volatile int never = 0;
-      WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
-      mbar_wait(mma_done, 0, drain);
-    }
-    __syncwarp();
   } else if (warp >= 6) {
     // ------------------------------------------------------------ fc1 row gather
     const int t = threadIdx.x - 6 * 32;
@@ -240,10 +353,10 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      int e, n, row0, rows;
-      decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
-      const int tok0 = __ldg(p.permute_src + row0) / p.k;
+    for (int tile = unit; tile < total && ok; tile += nunits) {
+      int e, n, pair0, row0, rows;
+      tile_rows(tile, e, n, pair0, row0, rows);
+      const int tok0 = __ldg(p.permute_src + pair0) / p.k;  // a valid row for padding
       const char* src[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -252,7 +365,8 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
         src[i] = xg + tok * row_bytes + chunk * 16;
       }
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, ctl);
+        if (lane == 0) ok = PAIR ? mbar_wait_cluster(&empty[s], ph ^ 1, ctl)
+                                 : mbar_wait(&empty[s], ph ^ 1, ctl);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         const uint32_t a_dst = smem_u32(sA + s * A_STAGE);
@@ -262,7 +376,7 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
           cp_async16(a_dst + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + kb * 128);
         }
         cp_async_mbar_arrive_noinc(&full[s]);
-        if (++s == QSTAGES) { s = 0; ph ^= 1; }
+        if (++s == STAGES) { s = 0; ph ^= 1; }
       }
     }
     cp_async_wait<0>();
@@ -271,14 +385,18 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
     const int q = warp & 3;
     uint8_t* stage = sOut + q * OUT_STAGE;
     const uint32_t row_off = static_cast<uint32_t>(lane) * 128;
+    const uint32_t leader_tempty = PAIR ? map_to_rank(tempty, 0) : 0u;
     int g = 0;              // first chunk of the current tile (same count as the MMA warp)
     uint32_t tf_phase = 0;  // bit b: parity of the next tfull[b] completion
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      int e, n, row0, rows;
-      decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
+    for (int tile = unit; tile < total; tile += nunits) {
+      int e, n, pair0, row0, rows;
+      tile_rows(tile, e, n, pair0, row0, rows);
       bool ok = true;
       const int last = (g + nchunk - 1) & (QSLOTS - 1);
-      if (lane == 0) ok = mbar_wait(&tfull[last], (tf_phase >> last) & 1, ctl);
+      if (lane == 0) {
+        ok = PAIR ? mbar_wait_cluster(&tfull[last], (tf_phase >> last) & 1, ctl)
+                  : mbar_wait(&tfull[last], (tf_phase >> last) & 1, ctl);
+      }
       tf_phase ^= 1u << last;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
@@ -388,7 +506,14 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
         }
       }
       tc_fence_before();
-      for (int c = 0; c < nchunk; ++c) mbar_arrive(&tempty[(g + c) & (QSLOTS - 1)]);
+      __syncwarp();
+      if (lane == 0) {  // free the tile's chunk slots (after tcgen05.wait::ld)
+        for (int c = 0; c < nchunk; ++c) {
+          const int sl = (g + c) & (QSLOTS - 1);
+          if (!PAIR || leader) mbar_arrive(&tempty[sl]);
+          else mbar_arrive_remote_relaxed(leader_tempty + sl * 8);
+        }
+      }
       g += nchunk;
     }
     if (lane == 0) bulk_wait_all();
@@ -396,9 +521,13 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
+  }
 }
 
 // int8 -> bf16 (exact), 16 values per thread step, over one or two tensors
@@ -488,7 +617,7 @@ cudaError_t launch_requant(const float* h, const int32_t* offsets, const mc2_sha
   return e;
 }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 static cudaError_t launch_q(const QArgs& g, cudaStream_t st) {
   const mc2_shape_t& s = *g.s;
   const int64_t R = static_cast<int64_t>(s.T) * s.k;
@@ -528,23 +657,63 @@ static cudaError_t launch_q(const QArgs& g, cudaStream_t st) {
   if (!ok) return cudaErrorInvalidValue;
   p.nchunk = (p.K / 64 + QCHUNK_KB - 1) / QCHUNK_KB;
   if (p.nchunk > QMAX_CHUNKS) return cudaErrorInvalidValue;
-  const size_t smem = QSMEM_BYTES_FIXED + (s.E + 1) * sizeof(int32_t);
+  using G = QGeom<PAIR>;
+  const size_t smem = G::kSmemFixed + (s.E + 1) * sizeof(int32_t);
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(gmm_q_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(QSMEM_BYTES_FIXED + 1025 * sizeof(int32_t)));
+    attr_err = cudaFuncSetAttribute(gmm_q_kernel<MODE, PAIR>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(G::kSmemFixed + 1025 * sizeof(int32_t)));
+    if (attr_err != cudaSuccess || !PAIR) return;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms() & ~1, 1, 1);
+    cfg.blockDim = dim3(QRoles<MODE>::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = G::kSmemFixed + 1025 * sizeof(int32_t);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, gmm_q_kernel<MODE, PAIR>, &cfg) !=
+        cudaSuccess)
+      max_clusters = 0;
   });
   if (attr_err != cudaSuccess) return attr_err;
+  if (PAIR) {  // persistent grid: as many pairs as can be resident at once
+    if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+    const int64_t tiles_upper = (R / (2 * BM) + s.E) * static_cast<int64_t>(p.n_tiles);
+    const int grid =
+        2 * static_cast<int>(std::min<int64_t>(max_clusters, std::max<int64_t>(tiles_upper, 1)));
+    return launch_kernel(gmm_q_kernel<MODE, PAIR>, dim3(grid), dim3(QRoles<MODE>::kThreads), smem,
+                         st, 2, tA, tB, tOut, p);
+  }
   const int64_t tiles_upper = (R / BM + s.E) * static_cast<int64_t>(p.n_tiles);
   const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_upper, 1)));
-  return launch_kernel(gmm_q_kernel<MODE>, dim3(grid), dim3(QRoles<MODE>::kThreads), smem, st, 1,
-                       tA, tB, tOut, p);
+  return launch_kernel(gmm_q_kernel<MODE, PAIR>, dim3(grid), dim3(QRoles<MODE>::kThreads), smem,
+                       st, 1, tA, tB, tOut, p);
+}
+
+// CTA pairs when experts average at least 256 rows (mc2_set_tile_pairing
+// forces either form; both give the same bits: every output accumulates its
+// chunks in the same K order).
+static bool use_pairs_q(const mc2_shape_t& s) {
+  const int forced = tile_pairing_override();
+  if (forced == 1) return false;
+  if (forced == 2) return num_sms() >= 2;
+  const int64_t R = static_cast<int64_t>(s.T) * s.k;
+  return num_sms() >= 2 && R >= 2 * BM * static_cast<int64_t>(s.E);
 }
 
 cudaError_t launch_gemm_q(const QArgs& g, cudaStream_t st) {
   if (static_cast<int64_t>(g.s->T) * g.s->k == 0) return cudaSuccess;
-  const cudaError_t e = g.mode == MODE_FC1 ? launch_q<MODE_FC1>(g, st) : launch_q<MODE_FC2>(g, st);
+  const bool pairs = use_pairs_q(*g.s);
+  const cudaError_t e =
+      g.mode == MODE_FC1 ? (pairs ? launch_q<MODE_FC1, true>(g, st) : launch_q<MODE_FC1, false>(g, st))
+                         : (pairs ? launch_q<MODE_FC2, true>(g, st) : launch_q<MODE_FC2, false>(g, st));
   note_launches(1);
   return e;
 }

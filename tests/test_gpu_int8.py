@@ -32,6 +32,15 @@ def _run(wl, inp, out):
     return d, b
 
 
+@pytest.fixture(params=[1, 2], ids=["single_cta", "cta_pairs"])
+def pairing(request):
+    """Force one int8 GEMM tiling (single CTAs or CTA pairs) for the test."""
+    ensure_built()
+    B.mc2_set_tile_pairing(request.param)
+    yield request.param
+    B.mc2_set_tile_pairing(0)
+
+
 SMALL_I8 = [
     Workload("i8_small", 256, 256, 128, 8, 2, 2, "i8"),
     Workload("i8_chunk_edge", 128, 2112, 192, 4, 2, 2, "i8"),    # K = 33 k-blocks: chunks 16+16+1
@@ -40,7 +49,7 @@ SMALL_I8 = [
 
 
 @pytest.mark.parametrize("wl", SMALL_I8, ids=lambda w: w.name)
-def test_int8_fc1_accumulators_exact(wl):
+def test_int8_fc1_accumulators_exact(wl, pairing):
     inp = make_inputs(wl, 7)
     d, b = _run(wl, inp, out="i32")
     ref = orc.quant_block_forward(inp["x"], inp["xs"], inp["w1"], inp["w1s"], inp["w2"],
@@ -50,7 +59,7 @@ def test_int8_fc1_accumulators_exact(wl):
     assert int(b.dev_status.item()) == 0
 
 
-def test_int8_worst_case_magnitudes_exact():
+def test_int8_worst_case_magnitudes_exact(pairing):
     """All values +-127 at K = 3072: |acc| = 49.5M > 2^24, exact only by chunking."""
     wl = Workload("i8_worst", 64, 3072, 128, 2, 1, 1, "i8")
     inp = make_inputs(wl, 0)
@@ -66,7 +75,7 @@ def test_int8_worst_case_magnitudes_exact():
 
 
 @pytest.mark.parametrize("wl", SMALL_I8, ids=lambda w: w.name)
-def test_int8_block_parity(wl):
+def test_int8_block_parity(wl, pairing):
     inp = make_inputs(wl, 8)
     d, b = _run(wl, inp, out="bf16")
     hq = to_np(b.h)
@@ -123,7 +132,7 @@ def test_int8_full_size_sampled():
     assert int(b.dev_status.item()) == 0
 
 
-def test_int8_full_size_accumulators_sampled():
+def test_int8_full_size_accumulators_sampled(pairing):
     """The int8 workload at full size: fc1 sums K = 3072 in three exact chunks
     and fc2 K = 1536 in two, and every CTA takes several tiles, so the TMEM
     chunk-slot ring wraps many times.  Sampled permuted rows of both int32
@@ -162,3 +171,22 @@ def test_int8_full_size_accumulators_sampled():
                 f"fc1 row {p} (expert {e})"
             assert np.array_equal(acc2[p].astype(np.int64), hq[p].astype(np.int64) @ w2), \
                 f"fc2 row {p} (expert {e})"
+
+
+def test_int8_pairs_equal_single_bitwise():
+    """Both int8 GEMM tilings accumulate every output's K chunks in the same
+    order: h_q, its scales and the block output are identical bit for bit
+    (a workload with several tiles per CTA and per CTA pair)."""
+    wl = Workload("i8_mid", 2048, 1024, 512, 16, 4, 4, "i8")
+    inp = make_inputs(wl, 4)
+    res = []
+    for mode in (1, 2):
+        B.mc2_set_tile_pairing(mode)
+        try:
+            d, b = _run(wl, inp, out="bf16")
+            res.append((to_np(b.h), to_np(b.h_scale), to_np(b.out)))
+            assert int(b.dev_status.item()) == 0
+        finally:
+            B.mc2_set_tile_pairing(0)
+    for a, c in zip(res[0], res[1]):
+        assert np.array_equal(a.view(np.uint8), c.view(np.uint8))
