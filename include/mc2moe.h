@@ -312,10 +312,9 @@ mc2_status_t mc2_selftest_wait(uint64_t limit_ns, int32_t* dev_status, void* str
 void mc2_set_wait_limit_ns(uint64_t limit_ns);
 
 /* Grouped-GEMM tiling for later launches of this process: 0 = automatic
- * (when experts average >= 256 rows: bf16/tf32 fc2 on CTA pairs with 256x256
- * tiles and both int8 GEMMs on CTA pairs with 256x128 tiles; everything else
- * on one CTA per 128x256 tile, int8 128x128), 1 = always single CTAs, 2 =
- * always CTA pairs.  The choice does not change any result bit: both tilings
+ * (bf16/tf32 fc2 on CTA pairs with 256x256 tiles when experts average >= 256
+ * rows; everything else on one CTA per 128x256 tile, int8 GEMMs 128x128),
+ * 1 = always single CTAs, 2 = always CTA pairs (int8 GEMMs: 256x128 tiles).  The choice does not change any result bit: both tilings
  * accumulate each output in the same K order.  Host only. */
 void mc2_set_tile_pairing(int32_t mode);
 

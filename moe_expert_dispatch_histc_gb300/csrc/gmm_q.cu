@@ -16,8 +16,8 @@
 //   fc2: acc2 = h_q @ w2_q[e];  y = (hs[p] * w2s[e, n]) * acc2 -> scaled fp16 -> combine
 //
 // Tiles are 128 x 128 (fc1: 64 gate + 64 up columns), 6 stages of 32 KB, one
-// CTA per SM, the same warp roles as the bf16 kernel; or, when experts
-// average 256 rows or more, 256 x 128 tiles on CTA pairs (cta_group::2: each
+// CTA per SM, the same warp roles as the bf16 kernel; or (when the tile
+// pairing is forced) 256 x 128 tiles on CTA pairs (cta_group::2: each
 // CTA streams its 128 rows and one 64-column block of B, 24 KB per stage, 8
 // stages; fc2's odd CTA loads onto the even CTA's stage barrier, fc1's odd CTA
 // relays its gathered stages).  TMEM is a ring of four
@@ -697,15 +697,14 @@ static cudaError_t launch_q(const QArgs& g, cudaStream_t st) {
                        st, 1, tA, tB, tOut, p);
 }
 
-// CTA pairs when experts average at least 256 rows (mc2_set_tile_pairing
-// forces either form; both give the same bits: every output accumulates its
-// chunks in the same K order).
-static bool use_pairs_q(const mc2_shape_t& s) {
-  const int forced = tile_pairing_override();
-  if (forced == 1) return false;
-  if (forced == 2) return num_sms() >= 2;
-  const int64_t R = static_cast<int64_t>(s.T) * s.k;
-  return num_sms() >= 2 && R >= 2 * BM * static_cast<int64_t>(s.E);
+// Single CTAs unless mc2_set_tile_pairing forces pairs (both give the same
+// bits: every output accumulates its chunks in the same K order).  Measured
+// on GB300 with the 8192-token int8 workload (about 512 rows per expert):
+// pairs 1.736 ms per block against 1.509 ms (fc1 1.190 vs 0.999 ms, fc2 +
+// combine 0.530 vs 0.495 ms): 256-row tiles pad more rows, and fc1's odd CTA
+// still relays its gathered stages.
+static bool use_pairs_q(const mc2_shape_t&) {
+  return tile_pairing_override() == 2 && num_sms() >= 2;
 }
 
 cudaError_t launch_gemm_q(const QArgs& g, cudaStream_t st) {
