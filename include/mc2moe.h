@@ -45,7 +45,7 @@ extern "C" {
 typedef enum {
   MC2_OK = 0,
   MC2_ERR_INVALID_ARG = 1,    /* shape rule or pointer rule broken; nothing launched */
-  MC2_ERR_UNSUPPORTED = 2,    /* valid request this build does not implement */
+  MC2_ERR_UNSUPPORTED = 2,    /* valid request the library does not implement */
   MC2_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
   MC2_ERR_DEVICE_TIMEOUT = 4, /* never returned synchronously: the device reports MC2_DEV_TIMEOUT;
                                  the code exists so callers can map that bit to a status */
