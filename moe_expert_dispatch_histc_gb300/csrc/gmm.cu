@@ -1195,15 +1195,30 @@ cudaError_t launch_combine(const mc2_shape_t& s, const void* y, const float* ysc
 
 // Materialised permute of the non-fused path: xp[p, :] = x[permute_src[p] / k, :]
 // for every permuted row (16 bytes per thread).
+// xp[p, :] = x[permute_src[p] / k, :]: one block per 8 permuted rows, each
+// thread copying one 16-byte column of all 8 rows per step (8 row loads in
+// flight per thread, one index load per row).
+constexpr int PR_ROWS = 8;
+constexpr int PR_THREADS = 128;
+
 __global__ void permute_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src,
                                     int k, int64_t R, int H8, uint4* __restrict__ xp) {
   griddep_wait();
   griddep_launch_dependents();
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= R * H8) return;
-  const int64_t p = i / H8;
-  const int c = static_cast<int>(i - p * H8);
-  xp[i] = __ldg(x + static_cast<int64_t>(__ldg(src + p) / k) * H8 + c);
+  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * PR_ROWS;
+  int64_t tok[PR_ROWS];
+#pragma unroll
+  for (int r = 0; r < PR_ROWS; ++r)
+    tok[r] = row0 + r < R ? static_cast<int64_t>(__ldg(src + row0 + r) / k) : -1;
+  for (int c = threadIdx.x; c < H8; c += PR_THREADS) {
+    uint4 v[PR_ROWS];
+#pragma unroll
+    for (int r = 0; r < PR_ROWS; ++r)
+      if (tok[r] >= 0) v[r] = __ldg(x + tok[r] * H8 + c);
+#pragma unroll
+    for (int r = 0; r < PR_ROWS; ++r)
+      if (tok[r] >= 0) xp[(row0 + r) * H8 + c] = v[r];
+  }
 }
 
 cudaError_t launch_permute_rows(const mc2_shape_t& s, const void* x, const int32_t* permute_src,
@@ -1211,10 +1226,9 @@ cudaError_t launch_permute_rows(const mc2_shape_t& s, const void* x, const int32
   const int64_t R = static_cast<int64_t>(s.T) * s.k;
   const int H8 = s.H / 8;  // bf16: 8 per 16 bytes
   if (R == 0) return cudaSuccess;
-  const int threads = 256;
-  const int64_t blocks = (R * H8 + threads - 1) / threads;
+  const int64_t blocks = (R + PR_ROWS - 1) / PR_ROWS;
   const cudaError_t e = launch_kernel(permute_rows_kernel, dim3(static_cast<unsigned>(blocks)),
-                                      dim3(threads), 0, st, 1, static_cast<const uint4*>(x),
+                                      dim3(PR_THREADS), 0, st, 1, static_cast<const uint4*>(x),
                                       permute_src, static_cast<int>(s.k), R, H8,
                                       static_cast<uint4*>(xp));
   note_launches(1);
