@@ -7,6 +7,8 @@ and shares no code with it; the two meet only through the seeded inputs of
 
 It is written to be slow and obviously correct: float64 throughout (int64 for
 the int8 path), numpy matmul as the only library step, no blocking or fusion.
+Integer products go through a float64 matmul whose every partial sum is
+checked to stay below 2**53, so they are exact (``exact_int_matmul``).
 
 Sources (page title, then section):
 
@@ -63,11 +65,12 @@ __all__ = [
     "rank_counts", "send_recv_counts", "permute", "unpermute",
     "expert_offsets", "grouped_matmul", "block_forward", "ep_mc2_forward_emulated",
     "brute_force_token", "quant_block_forward", "requant_rows", "mm_reduce_scatter",
+    "exact_int_matmul",
     "silu_grad", "block_backward", "ORACLE_UNPINNED",
 ]
 
 # Functions with no pin independent of this file (see tests/test_oracle_pins.py).
-ORACLE_UNPINNED = ("requant_rows: exact ties of h/hs at .5 (parity unpinned beyond +-1 code)",)
+ORACLE_UNPINNED = ()
 
 
 # ---------------------------------------------------------------------------
@@ -390,6 +393,22 @@ def brute_force_token(x_t, w1, w2, sel_t, probs_t, E, h_dtype=None):
 # ---------------------------------------------------------------------------
 # int8 path [RSQ]: (x1_scale * x2_scale) * (x1 @ x2), no bias
 # ---------------------------------------------------------------------------
+def exact_int_matmul(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Integer matrix product a @ b, exact, returned as int64.
+
+    Computed as a float64 library matmul: every product and every partial
+    sum is an integer of magnitude at most K * max|a| * max|b|, and below
+    2**53 each of them is a float64 exactly, so the result does not depend
+    on the library's summation order.  The bound is checked first."""
+    a = np.asarray(a)
+    b = np.asarray(b)
+    K = a.shape[-1]
+    ma = int(np.abs(a.astype(np.int64)).max(initial=0))
+    mb = int(np.abs(b.astype(np.int64)).max(initial=0))
+    assert K * ma * mb < 2 ** 53, "integer product too large for an exact float64 sum"
+    return (a.astype(np.float64) @ b.astype(np.float64)).astype(np.int64)
+
+
 def requant_rows(h: np.ndarray):
     """Symmetric per-row int8 re-quantisation of h, decided in float32:
     hs = fp32(max|h|) / 127 (1 when the row is all zero);
@@ -422,8 +441,7 @@ def quant_block_forward(xq, xs, w1q, w1s, w2q, w2s, sel, probs, E, W, hq_overrid
         a, b = int(offsets[e]), int(offsets[e + 1])
         if a == b:
             continue
-        rows = xq[tok[a:b]].astype(np.int64)
-        acc1[a:b] = rows @ w1q[e].astype(np.int64)
+        acc1[a:b] = exact_int_matmul(xq[tok[a:b]], w1q[e])
         scale = xs[tok[a:b]].astype(np.float64)[:, None] * w1s[e].astype(np.float64)[None, :]
         g[a:b] = scale * acc1[a:b]
     h = swiglu(g)
@@ -434,7 +452,7 @@ def quant_block_forward(xq, xs, w1q, w1s, w2q, w2s, sel, probs, E, W, hq_overrid
         a, b = int(offsets[e]), int(offsets[e + 1])
         if a == b:
             continue
-        acc2[a:b] = hq[a:b].astype(np.int64) @ w2q[e].astype(np.int64)
+        acc2[a:b] = exact_int_matmul(hq[a:b], w2q[e])
         y[a:b] = (hs[a:b].astype(np.float64)[:, None] * w2s[e].astype(np.float64)[None, :]) * acc2[a:b]
     out = unpermute(y, sorted_indices, probs, valid_rows=nvalid)
     return dict(cnt=num_global, offsets=offsets, permute_src=sorted_indices,
@@ -454,7 +472,7 @@ def mm_reduce_scatter(x1q, x1s, x2q, x2s):
     acc = np.zeros((W, m, n), dtype=np.int64)
     total = np.zeros((m, n))
     for r in range(W):
-        acc[r] = x1q[r].astype(np.int64) @ x2q[r].astype(np.int64)
+        acc[r] = exact_int_matmul(x1q[r], x2q[r])
         scale = x1s[r].astype(np.float64)[:, None] * x2s[r].astype(np.float64)[None, :]
         total += scale * acc[r]
     per_rank = total.reshape(W, m // W, n)

@@ -19,18 +19,17 @@ def ensure_built():
         _built = True
 
 
-class LazyF64:
-    """w[e] -> float64 copy of expert e's weights, converted on first use."""
+class F64Experts:
+    """w[e] -> float64 copy of expert e's weights, converted on every use and
+    not kept, so the oracle can walk a weight set whose float64 copy would
+    not fit in host memory (the decode workload's w1 is 12.9 GB in float64)."""
 
     def __init__(self, arr, act):
-        self.arr, self.act, self.cache = arr, act, {}
+        self.arr, self.act = arr, act
         self.shape = arr.shape
 
     def __getitem__(self, e):
-        e = int(e)
-        if e not in self.cache:
-            self.cache[e] = as_f64(self.arr[e], self.act)
-        return self.cache[e]
+        return as_f64(self.arr[int(e)], self.act)
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:

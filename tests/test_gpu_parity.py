@@ -16,7 +16,7 @@ from oracle import mc2_oracle as orc
 from moe_expert_dispatch_histc_gb300 import binding as B
 from moe_expert_dispatch_histc_gb300.workloads import WORKLOADS, Workload, as_f64, make_inputs
 
-from gpu_util import LazyF64, ensure_built, run_gpu, to_np
+from gpu_util import F64Experts, ensure_built, run_gpu, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -202,18 +202,32 @@ def test_unfused_baseline_equals_fused_block(wl):
     """Materialised permute + plain grouped fc1, then fc2 + combine: the same
     h and out bits as the fused block, and xp[p] = x[permute_src[p] / k]."""
     inp, d, b, xp = _unfused(wl, 10)
-    _, _, bf = run_gpu(wl, seed=10)
-    src = to_np(b.permute_src)
+    src, offsets = _counts_exact(wl, inp, b)
+    xa = as_f64(inp["x"], wl.act)
+    ref = orc.block_forward(xa, as_f64(inp["w1"], wl.act), as_f64(inp["w2"], wl.act), inp["sel"],
+                            inp["probs"], wl.E, wl.W, h_dtype="bf16")
+    nvalid = int(offsets[-1])
+    _tol(to_np(b.h)[:nvalid], ref["h"], "non-fused h")
+    _tol(to_np(b.out), ref["out"], "non-fused out")
     x = torch.from_numpy(inp["x"].view(np.int16)).cuda()
     assert torch.equal(xp.view(torch.int16), x[torch.from_numpy(src // wl.k).cuda().long()])
+    _, _, bf = run_gpu(wl, seed=10)
     assert torch.equal(b.h.view(torch.int16), bf.h.view(torch.int16))
     assert torch.equal(b.out.view(torch.int16), bf.out.view(torch.int16))
     assert int(b.dev_status.item()) == 0
 
 
 def test_unfused_baseline_full_size_uniform():
+    """The non-fused path at full size against the float64 oracle (every
+    element), and bitwise against the fused block."""
     wl = WORKLOADS["uniform"]
-    _, _, b, _ = _unfused(wl, 0)
+    inp, _, b, _ = _unfused(wl, 0)
+    src, offsets = _counts_exact(wl, inp, b)
+    ref = orc.block_forward(as_f64(inp["x"], wl.act), F64Experts(inp["w1"], wl.act),
+                            F64Experts(inp["w2"], wl.act), inp["sel"], inp["probs"], wl.E, wl.W,
+                            h_dtype="bf16")
+    _tol(to_np(b.h)[:int(offsets[-1])], ref["h"], "non-fused h (full size)")
+    _tol(to_np(b.out), ref["out"], "non-fused out (full size)")
     _, _, bf = run_gpu(wl, seed=0)
     assert torch.equal(b.out.view(torch.int16), bf.out.view(torch.int16))
     assert int(b.dev_status.item()) == 0
@@ -267,32 +281,23 @@ def test_empty_input():
 
 # ------------------------------------------------------------------ full size
 @pytest.mark.parametrize("name", ["uniform", "skew", "decode"])
-def test_full_size_sampled(name):
+def test_full_size_full(name):
+    """The named workloads at full size, in the launch configuration of the
+    benchmark (one mc2_moe_forward call): counts and indices bit-exact, and
+    every element of h and out within the tolerance of the float64 oracle."""
     wl = WORKLOADS[name]
     inp, d, b = run_gpu(wl, seed=0)
     src, offsets = _counts_exact(wl, inp, b)
     x = as_f64(inp["x"], wl.act)
-    w1, w2 = LazyF64(inp["w1"], wl.act), LazyF64(inp["w2"], wl.act)
-    rng = np.random.default_rng(123)
-    toks = np.unique(np.concatenate([rng.choice(wl.T, 24, replace=False), [0, wl.T - 1]]))
-    out = to_np(b.out)
-    got, ref = [], []
-    for t in toks:
-        ref.append(orc.brute_force_token(x[t], w1, w2, inp["sel"][t], inp["probs"][t], wl.E,
-                                         h_dtype="bf16"))
-        got.append(out[t])
-    _tol(np.array(got), np.array(ref), f"{name}: sampled out rows")
-    # sampled h rows, including the first and last row of the busiest expert
+    w1, w2 = F64Experts(inp["w1"], wl.act), F64Experts(inp["w2"], wl.act)
+    ref = orc.block_forward(x, w1, w2, inp["sel"], inp["probs"], wl.E, wl.W, h_dtype="bf16")
+    nvalid = int(offsets[-1])
+    _tol(to_np(b.h)[:nvalid], ref["h"], f"{name}: h (all rows)")
+    _tol(to_np(b.out), ref["out"], f"{name}: out (all tokens)")
+    # the first and last row of the busiest expert and the last token
     cnt = np.diff(offsets)
     e_big = int(np.argmax(cnt))
-    rows = np.unique(np.concatenate([rng.choice(int(offsets[-1]), 24, replace=False),
-                                     [offsets[e_big], offsets[e_big + 1] - 1]]))
-    h = to_np(b.h)
-    hg, hr = [], []
-    for p in rows:
-        t, e = int(src[p]) // wl.k, int(np.searchsorted(offsets, p, side="right") - 1)
-        g = x[t][None, :] @ w1[e]
-        hr.append(orc.round_to_bf16(orc.swiglu(g))[0])
-        hg.append(h[p])
-    _tol(np.array(hg), np.array(hr), f"{name}: sampled h rows")
+    for p in (int(offsets[e_big]), int(offsets[e_big + 1]) - 1):
+        _tol(to_np(b.h)[p:p + 1], ref["h"][p:p + 1], f"{name}: h row {p}")
+    _tol(to_np(b.out)[-1:], ref["out"][-1:], f"{name}: last token")
     assert int(b.dev_status.item()) == 0

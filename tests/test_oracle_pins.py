@@ -260,10 +260,6 @@ def test_quant_block_integer_parts_by_brute_force():
             acc = sum(int(xq[t, a]) * int(w1q[e, a, n]) for a in range(H))
             assert r["acc1"][p, n] == acc
             assert r["h"].shape == (T * k, I)
-            # dequant formula (x1_scale * x2_scale) * (x1 @ x2), no bias
-            assert math.isclose(
-                (float(xs[t]) * float(w1s[e, n])) * acc,
-                float(xs[t]) * float(w1s[e, n]) * acc, rel_tol=1e-15)
         for c in range(H):
             acc2 = sum(int(r["hq"][p, i]) * int(w2q[e, i, c]) for i in range(I))
             assert r["acc2"][p, c] == acc2
@@ -281,6 +277,138 @@ def test_quant_worst_case_accumulator_fits_int32():
                                 np.zeros((1, 1), np.int32), np.ones((1, 1), np.float32), 1, 1)
     assert r["acc1"][0, 0] == -K * 127 * 127
     assert abs(int(r["acc1"][0, 0])) < 2 ** 31
+
+
+def test_exact_int_matmul_against_python_integers():
+    """The float64 route of the integer products equals Python's exact
+    integers, including sums far above 2**24 and the int8 extreme -128."""
+    rng = np.random.default_rng(3)
+    a = rng.integers(-128, 128, (5, 3072)).astype(np.int8)
+    b = rng.integers(-128, 128, (3072, 4)).astype(np.int8)
+    a[0] = -128
+    b[:, 0] = -128
+    got = orc.exact_int_matmul(a, b)
+    assert got.dtype == np.int64
+    for i in range(5):
+        for j in range(4):
+            assert got[i, j] == sum(int(a[i, t]) * int(b[t, j]) for t in range(3072))
+    assert got[0, 0] == 3072 * 128 * 128
+    with pytest.raises(AssertionError):
+        orc.exact_int_matmul(np.full((1, 2 ** 20), 2 ** 20, np.int64),
+                             np.full((2 ** 20, 1), 2 ** 20, np.int64))
+
+
+def _quant_case(seed):
+    """A small int8 block whose scale shapes make transposition mistakes fit:
+    E = 2I, so a transposed [E, 2I] channel scale still has the right shape."""
+    rng = np.random.default_rng(seed)
+    T, H, I, E, k, W = 12, 5, 2, 4, 2, 2
+    xq = rng.integers(-127, 128, (T, H)).astype(np.int8)
+    w1q = rng.integers(-127, 128, (E, H, 2 * I)).astype(np.int8)
+    w2q = rng.integers(-127, 128, (E, I, H)).astype(np.int8)
+    xs = rng.uniform(1e-3, 1e-2, T).astype(np.float32)
+    w1s = rng.uniform(1e-3, 1e-2, (E, 2 * I)).astype(np.float32)
+    w2s = rng.uniform(1e-3, 1e-2, (E, H)).astype(np.float32)
+    sel = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    probs = rng.uniform(0.1, 1.0, (T, k)).astype(np.float32)
+    return dict(xq=xq, xs=xs, w1q=w1q, w1s=w1s, w2q=w2q, w2s=w2s, sel=sel, probs=probs,
+                E=E, W=W, k=k, I=I, H=H)
+
+
+def test_quant_dequant_equals_float_block_on_dequantised_operands():
+    """(x1_scale * x2_scale) * (x1 @ x2) with x1_scale per token (m, 1) and
+    x2_scale per channel (1, n): fc1 of the int8 block equals the float block
+    run on x = xs[t] * xq[t, :] and w1 = w1q[e] * w1s[e, None, :], so their
+    SwiGLU outputs agree; fc2's rows equal (hs[p] * hq[p, :]) @ (w2q[e] *
+    w2s[e]), written out here element by element; the output is the
+    probability-weighted sum of a token's rows, also written out here."""
+    c = _quant_case(0)
+    r = orc.quant_block_forward(c["xq"], c["xs"], c["w1q"], c["w1s"], c["w2q"], c["w2s"],
+                                c["sel"], c["probs"], c["E"], c["W"])
+    xf = c["xs"].astype(np.float64)[:, None] * c["xq"].astype(np.float64)
+    w1f = c["w1q"].astype(np.float64) * c["w1s"].astype(np.float64)[:, None, :]
+    w2f = c["w2q"].astype(np.float64) * c["w2s"].astype(np.float64)[:, None, :]
+    ref = orc.block_forward(xf, w1f, w2f, c["sel"], c["probs"], c["E"], c["W"])
+    assert np.allclose(r["h"], ref["h"], rtol=1e-12, atol=0)
+    offs, src, k = r["offsets"], r["permute_src"], c["k"]
+    n = int(offs[-1])
+    for p in range(n):
+        e = int(np.searchsorted(offs, p, side="right") - 1)
+        for col in range(c["H"]):
+            v = sum((float(r["hs"][p]) * int(r["hq"][p, i])) *
+                    (int(c["w2q"][e, i, col]) * float(c["w2s"][e, col])) for i in range(c["I"]))
+            assert math.isclose(r["y"][p, col], v, rel_tol=1e-12, abs_tol=1e-300)
+    T = c["sel"].shape[0]
+    for t in range(T):
+        for col in range(c["H"]):
+            v = 0.0
+            for p in range(n):
+                if int(src[p]) // k == t:
+                    v += float(c["probs"][t, int(src[p]) % k]) * r["y"][p, col]
+            assert math.isclose(r["out"][t, col], v, rel_tol=1e-12, abs_tol=1e-300)
+
+
+def test_requant_rows_ties_worked_example():
+    """Hand-worked rows whose h / hs lands exactly on .5 (scales that are powers
+    of two, so every quotient is exact): ties go to the even code."""
+    g = _golden("requant_ties.json")
+    for h, hs, hq in zip(g["h"], g["hs"], g["hq"]):
+        q, s = orc.requant_rows(np.array([h]))
+        assert float(s[0]) == hs
+        assert q[0].astype(int).tolist() == hq
+
+
+@pytest.mark.parametrize("mutation", ["w1s_transposed", "w1s_wrong_expert", "xs_wrong_token",
+                                      "w2s_dropped", "w2s_wrong_expert", "hs_dropped",
+                                      "requant_half_away", "requant_by_128"])
+def test_planted_quant_mistakes_are_caught(monkeypatch, mutation):
+    """Each plausible mistake in the int8 block's scale handling or its
+    re-quantisation, planted in the oracle, makes a pin fail."""
+    real = orc.quant_block_forward
+    real_rq = orc.requant_rows
+
+    def bad(xq, xs, w1q, w1s, w2q, w2s, sel, probs, E, W, hq_override=None):
+        if mutation == "w1s_transposed":
+            w1s = np.ascontiguousarray(w1s.T)
+        elif mutation == "w1s_wrong_expert":
+            w1s = np.roll(w1s, 1, axis=0)
+        elif mutation == "xs_wrong_token":
+            xs = xs[::-1].copy()
+        elif mutation == "w2s_dropped":
+            w2s = np.ones_like(w2s)
+        elif mutation == "w2s_wrong_expert":
+            w2s = np.roll(w2s, 1, axis=0)
+        res = real(xq, xs, w1q, w1s, w2q, w2s, sel, probs, E, W, hq_override=hq_override)
+        if mutation == "hs_dropped":   # fc2 dequantised without the row scale
+            res["y"] = res["y"] / res["hs"].astype(np.float64)[:, None]
+            res["out"] = orc.unpermute(res["y"], res["permute_src"], probs,
+                                       valid_rows=int(res["offsets"][-1]))
+        return res
+
+    def bad_rq(h):
+        h32 = np.asarray(h, dtype=np.float64).astype(np.float32)
+        amax = np.abs(h32).max(axis=1)
+        if mutation == "requant_by_128":
+            hs = np.where(amax > 0, amax / np.float32(128.0), np.float32(1.0)).astype(np.float32)
+            q = np.rint(h32 / hs[:, None])
+        else:   # requant_half_away: ties away from zero
+            hs = np.where(amax > 0, amax / np.float32(127.0), np.float32(1.0)).astype(np.float32)
+            v = (h32 / hs[:, None]).astype(np.float32)
+            q = np.sign(v) * np.floor(np.abs(v) + 0.5)
+        return np.clip(q, -127, 127).astype(np.int8), hs
+
+    if mutation.startswith("requant"):
+        monkeypatch.setattr(orc, "requant_rows", bad_rq)
+    else:
+        monkeypatch.setattr(orc, "quant_block_forward", bad)
+    failures = 0
+    for fn in (test_quant_dequant_equals_float_block_on_dequantised_operands,
+               test_requant_rows_ties_worked_example, test_requant_rows_properties):
+        try:
+            fn()
+        except (AssertionError, ValueError, IndexError):
+            failures += 1
+    assert failures > 0, f"no pin caught the planted mistake {mutation}"
 
 
 def test_requant_rows_properties():
