@@ -1,15 +1,20 @@
 """Benchmark of the MoE expert block on GB300.
 
 A step is one pass of the whole block (counts -> fc1 + SwiGLU -> fc2 +
-weighted combine) over the ``uniform`` workload (T=4096 tokens, H=2048,
-I=768, E=64 experts, top-8, W=4 logical ranks, bf16), inputs already in HBM.
-L2 is flushed (a 256 MB write) between timed steps, outside the timed events.
+weighted combine) over one workload, inputs already in HBM.  The headline
+workload is ``skew``, the largest one that fits one GPU (T=16384 tokens,
+H=2048, I=768, E=128 experts, top-8, W=8 logical ranks, bf16, Zipf(1.2)
+routing).  L2 is flushed (a 256 MB write) between timed steps, outside the
+timed events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle, timed on host cores
 
-Prints one JSON line.  N > 1 (under torchrun) runs one independent replica
-per GPU (weak scaling): the block has no exchange step on one GPU.
+With no --workload it prints one full JSON line for each of the context
+workloads (tiny, decode, uniform, int8) and then the headline skew line,
+last; with --workload, that workload's line only.  N > 1 (under torchrun)
+runs one independent replica per GPU (weak scaling): the block has no
+exchange step on one GPU.
 """
 from __future__ import annotations
 
@@ -32,6 +37,7 @@ from moe_expert_dispatch_histc_gb300.workloads import WORKLOADS, as_f64, make_in
 METRIC = "MoE expert-block tokens/s (1 GPU); grouped-GEMM TFLOP/s as fraction of GB300 bf16 peak"
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 GMM_SRC = os.path.join(ROOT, "moe_expert_dispatch_histc_gb300", "csrc", "gmm.cu")
+GMMQ_SRC = os.path.join(ROOT, "moe_expert_dispatch_histc_gb300", "csrc", "gmm_q.cu")
 
 
 def _peaks():
@@ -55,16 +61,16 @@ def _src_hash(path):
     return hashlib.sha256(src.encode()).hexdigest()[:16]
 
 
-def _ncu_traffic(kernel_key, workload):
+def _ncu_traffic(kernel_key, workload, src=GMM_SRC):
     """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
-    the current kernel source; else None."""
+    the current source of the kernel's file; else None."""
     p = os.path.join(PROFILE_DIR, "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     ent = d.get(f"{kernel_key}:{workload}")
-    if not ent or ent.get("src_sha256_16") != _src_hash(GMM_SRC):
+    if not ent or ent.get("src_sha256_16") != _src_hash(src):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -153,7 +159,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    wl = WORKLOADS[args.workload]
+    wl = WORKLOADS[args.workload or HEADLINE]
     inp = make_inputs(wl, 0)
     run = _oracle_sample(wl, inp)
     Ts = max(wl.W, (64 // wl.W) * wl.W)   # bounded sample of the workload per step
@@ -259,23 +265,44 @@ def e2e_pipelined(wl, d, b, stream, steps, run):
     return ms, bi, bo
 
 
+HEADLINE = "skew"                                # the largest single-GPU workload
+CONTEXT = ("tiny", "decode", "uniform", "int8")  # printed before the headline line
+
+
 def run_cuda(args):
+    """One JSON line per workload: with no --workload, the four context
+    workloads first and the headline (skew) line last; else that workload."""
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from moe_expert_dispatch_histc_gb300 import binding as B
+    from moe_expert_dispatch_histc_gb300.build import build
+    build()
+    B.lib()
+    B.mc2_set_tile_pairing({"auto": 0, "single": 1, "pairs": 2}[args.tiling])
+    names = [args.workload] if args.workload else [*CONTEXT, HEADLINE]
+    if args.path == "unfused":   # the non-fused baseline exists for bf16 workloads only
+        names = [n for n in names if WORKLOADS[n].act == "bf16"]
+    for name in names:
+        run_cuda_workload(args, WORKLOADS[name], headline=(name == HEADLINE))
+        torch.cuda.empty_cache()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_cuda_workload(args, wl, headline):
     import torch
     import torch.distributed as dist
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
     from moe_expert_dispatch_histc_gb300 import binding as B, block as blk
-    from moe_expert_dispatch_histc_gb300.build import build
-    build()
-    B.lib()
-    B.mc2_set_tile_pairing({"auto": 0, "single": 1, "pairs": 2}[args.tiling])
-
-    wl = WORKLOADS[args.workload]
     inp = make_inputs(wl, 0)
     d = blk.inputs_to_device(inp, wl)
     b = blk.alloc_buffers(wl)
@@ -381,7 +408,8 @@ def run_cuda(args):
     e2e_val = job_tokens_per_s(wl.T, world, e2e_steps, e2e_ms)
 
     if rank != 0:
-        dist.barrier() if world > 1 else None
+        if world > 1:
+            dist.barrier()
         return
     peaks, src = _peaks()
     fc1_ms = float(seg[:, segi["fc1_swiglu"]].mean())
@@ -425,7 +453,8 @@ def run_cuda(args):
                                 if wl.act == "f32" else
                                 "gmm_kernel<fc1> (permute gather + fc1 + SwiGLU)"),
                      **roof,
-                     "traffic": None if unfused else _ncu_traffic("gmm_fc1", wl.name)},
+                     "traffic": None if unfused else
+                     _ncu_traffic("gmm_fc1", wl.name, GMMQ_SRC if wl.act == "i8" else GMM_SRC)},
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "steps": e2e_steps,
                 "mode": ("counts, mc2_permute_rows, mc2_gmm_swiglu, mc2_gmm_alltoallv per step"
@@ -444,8 +473,12 @@ def run_cuda(args):
         line["weight_prepack_ms"] = t_prepack * 1e3
         line["dtype"] = "int8 (exact, on bf16 tensor cores)"
         line["roofline"]["peak_source"] += "; int8 runs at the bf16 rate (no integer tcgen05 MMA on sm_103a)"
+    if wl.name == "tiny":
+        line["config"]["note"] = ("correctness only: 64 tokens, a few-microsecond block; its "
+                                  "roofline fraction says nothing about the kernels")
+    line["config"]["role"] = "headline" if headline else "context (the headline line is last)"
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, inp)
+        line["cpu_baseline"] = cpu_baseline(wl, inp, budget_s=12.0 if headline else 6.0)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -463,7 +496,7 @@ def run_backward(args):
     from moe_expert_dispatch_histc_gb300.build import build
     build()
     B.lib()
-    wl = WORKLOADS[args.workload]
+    wl = WORKLOADS[args.workload or "uniform"]
     if wl.act != "bf16":
         raise SystemExit("--op backward: bf16 workloads only")
     inp = make_inputs(wl, 0)
@@ -693,7 +726,9 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--workload", default="uniform", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=None, choices=sorted(WORKLOADS),
+                    help="one workload; default: tiny, decode, uniform and int8 as context "
+                         "lines, then the headline skew line (the largest workload) last")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="fused", choices=["fused", "unfused", "twopass"],
                     help="unfused: the non-fused baseline (materialised permute, plain grouped "

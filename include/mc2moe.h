@@ -162,8 +162,11 @@ mc2_status_t mc2_gmm_alltoallv(const mc2_shape_t* s, const void* h, const float*
  *     shape must satisfy (E + 1) * W * ceil(T*k / W / 256) <= 131072, else the
  *     call returns MC2_ERR_UNSUPPORTED and launches nothing.
  *   - The first call on a device looks up that array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     that device current) and caches it, keyed on the device's current
+ *     context (after cudaDeviceReset the next call looks it up again); make
+ *     that first call before any stream capture.
+ *   - Pointer rules as for mc2_moe_counts (16-byte aligned arrays, else
+ *     MC2_ERR_INVALID_ARG with nothing launched).
  *   - Allocates nothing and calls no allocating routine.
  *   - Every call shares the one array: calls whose kernels may overlap on the
  *     GPU (other streams, other host threads) race and corrupt each other's
@@ -307,25 +310,32 @@ mc2_status_t mc2_moe_forward(const mc2_shape_t* s, const void* x, const float* x
  */
 mc2_status_t mc2_selftest_wait(uint64_t limit_ns, int32_t* dev_status, void* stream);
 
+/*
+ * Test and diagnostic hooks.  A production caller needs none of them.  Each
+ * setting holds for later calls made on the host thread that set it (and on
+ * no other thread) until that thread sets it again; apart from the wait
+ * limit, none of them changes any result bit (the tests check this).
+ */
+
 /* Set the device-side wait limit (nanoseconds) used by later launches of
- * this process; 0 restores the default (2 s). Host only. */
+ * this thread's calls; 0 restores the default (2 s). Host only. */
 void mc2_set_wait_limit_ns(uint64_t limit_ns);
 
-/* Grouped-GEMM tiling for later launches of this process: 0 = automatic
+/* Grouped-GEMM tiling for later calls of this thread: 0 = automatic
  * (bf16/tf32 fc2 on CTA pairs with 256x256 tiles when experts average >= 256
  * rows; everything else on one CTA per 128x256 tile, int8 GEMMs 128x128),
  * 1 = always single CTAs, 2 = always CTA pairs (int8 GEMMs: 256x128 tiles).  The choice does not change any result bit: both tilings
  * accumulate each output in the same K order.  Host only. */
 void mc2_set_tile_pairing(int32_t mode);
 
-/* Which counts pass later calls of this process use: 0 (default) one launch
+/* Which counts pass later calls of this thread use: 0 (default) one launch
  * of a thread-block cluster (up to 16 CTAs, per-CTA tables in shared memory)
  * whenever its tables fit, else three launches over the workspace tables;
  * 1 always three launches; 2 the same as 0 (the cluster pass when it fits).
  * Outputs are identical either way.  Host only. */
 void mc2_set_counts_path(int32_t mode);
 
-/* Which form later mc2_mm_reduce_scatter_i8 calls of this process take:
+/* Which form later mc2_mm_reduce_scatter_i8 calls of this thread take:
  * 0 (default) fused, one CTA-pair kernel after the int8 -> bf16 copies that
  * folds every rank's dequantised product into an on-chip fp32 sum; 1 two
  * passes, the int32 partial product of every rank written to the workspace
@@ -336,7 +346,7 @@ void mc2_set_counts_path(int32_t mode);
 void mc2_set_mmrs_path(int32_t mode);
 
 /* Programmatic dependent launch between the kernels of later calls of this
- * process: 1 (default) lets each kernel's set-up overlap the end of the
+ * thread: 1 (default) lets each kernel's set-up overlap the end of the
  * previous kernel on the stream (each kernel still waits for its
  * predecessors' results before reading or writing global memory); 0 launches
  * them in plain stream order.  Results are identical either way.  Host only. */

@@ -2,7 +2,6 @@
 // order of launches for each entry point.  No allocation, no synchronisation.
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cstring>
 #include <initializer_list>
 
@@ -10,25 +9,25 @@
 
 namespace mc2 {
 
-static std::atomic<uint64_t> g_wait_limit_ns{0};
-static std::atomic<int> g_tile_pairing{0};
-static std::atomic<int> g_launch_overlap{1};
-static std::atomic<int> g_counts_path{0};
-static std::atomic<int> g_mmrs_path{0};
+// Test and diagnostic hooks (mc2_set_*): each holds for later calls made on
+// the host thread that set it, and on no other thread.  Apart from the wait
+// limit, none of them changes a result bit.
+static thread_local uint64_t tl_wait_limit_ns = 0;
+static thread_local int tl_tile_pairing = 0;
+static thread_local int tl_launch_overlap = 1;
+static thread_local int tl_counts_path = 0;
+static thread_local int tl_mmrs_path = 0;
 static thread_local int tl_launches = 0;
 
-uint64_t wait_limit_ns() {
-  const uint64_t v = g_wait_limit_ns.load();
-  return v ? v : 2000000000ull;  // 2 s
-}
+uint64_t wait_limit_ns() { return tl_wait_limit_ns ? tl_wait_limit_ns : 2000000000ull; }  // 2 s
 
-int tile_pairing_override() { return g_tile_pairing.load(); }
+int tile_pairing_override() { return tl_tile_pairing; }
 
-bool launch_overlap_enabled() { return g_launch_overlap.load() != 0; }
+bool launch_overlap_enabled() { return tl_launch_overlap != 0; }
 
-int counts_path_override() { return g_counts_path.load(); }
+int counts_path_override() { return tl_counts_path; }
 
-int mmrs_path_override() { return g_mmrs_path.load(); }
+int mmrs_path_override() { return tl_mmrs_path; }
 
 void note_launches(int n) { tl_launches += n; }
 
@@ -86,14 +85,6 @@ bool shape_ok(const mc2_shape_t* s) {
 }
 
 mc2_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MC2_OK : MC2_ERR_CUDA; }
-
-// Pointer rule: every array 16-byte aligned (vector and TMA accesses), the
-// workspace 256-byte aligned.  NULL passes (the null rules are separate).
-bool aligned(std::initializer_list<const void*> ps, uintptr_t a = 16) {
-  for (const void* p : ps)
-    if (reinterpret_cast<uintptr_t>(p) & (a - 1)) return false;
-  return true;
-}
 
 mc2_status_t do_counts(const mc2_shape_t* s, const int32_t* sel, int32_t* cnt, int32_t* recv,
                        int32_t* offsets, int32_t* permute_src, int32_t* unpermute_dst, void* ws,
@@ -393,15 +384,15 @@ mc2_status_t mc2_selftest_wait(uint64_t limit_ns, int32_t* dev_status, void* str
   return cuda_status(launch_selftest_wait(limit_ns, dev_status, static_cast<cudaStream_t>(stream)));
 }
 
-void mc2_set_wait_limit_ns(uint64_t limit_ns) { g_wait_limit_ns.store(limit_ns); }
+void mc2_set_wait_limit_ns(uint64_t limit_ns) { tl_wait_limit_ns = limit_ns; }
 
-void mc2_set_tile_pairing(int32_t mode) { g_tile_pairing.store(mode == 1 || mode == 2 ? mode : 0); }
+void mc2_set_tile_pairing(int32_t mode) { tl_tile_pairing = mode == 1 || mode == 2 ? mode : 0; }
 
-void mc2_set_launch_overlap(int32_t enabled) { g_launch_overlap.store(enabled ? 1 : 0); }
+void mc2_set_launch_overlap(int32_t enabled) { tl_launch_overlap = enabled ? 1 : 0; }
 
-void mc2_set_counts_path(int32_t mode) { g_counts_path.store(mode == 1 || mode == 2 ? mode : 0); }
+void mc2_set_counts_path(int32_t mode) { tl_counts_path = mode == 1 || mode == 2 ? mode : 0; }
 
-void mc2_set_mmrs_path(int32_t mode) { g_mmrs_path.store(mode == 1 ? 1 : 0); }
+void mc2_set_mmrs_path(int32_t mode) { tl_mmrs_path = mode == 1 ? 1 : 0; }
 
 int32_t mc2_last_launch_count(void) { return tl_launches; }
 

@@ -583,21 +583,54 @@ static __device__ __align__(256) int32_t g_counts_scratch[2 * kStaticCountsEntri
 
 static std::mutex g_counts_scratch_mu;
 static int32_t* g_counts_scratch_ptr[kStaticMaxDevices] = {};
+static void* g_counts_scratch_ctx[kStaticMaxDevices] = {};
+
+// The driver's cuCtxGetCurrent, looked up at run time (the library does not
+// link the driver library).  Returns the current context, or NULL.
+static void* current_context() {
+  using Fn = int (*)(void**);
+  static Fn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<Fn>(ptr);
+  });
+  void* ctx = nullptr;
+  if (fn && fn(&ctx) != 0) ctx = nullptr;
+  return ctx;
+}
 
 // Device address of g_counts_scratch on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address is looked up
-// once per device (with that device current) and cached.
+// with that device current and cached per device, together with the
+// context it was looked up in: after cudaDeviceReset (or any teardown of the
+// primary context) the module is loaded again, possibly elsewhere, so a
+// changed context triggers a fresh lookup instead of reusing a dangling
+// address.
 static cudaError_t counts_scratch_on_current_device(int32_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kStaticMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_counts_scratch_mu);
+  void* p = nullptr;
   if (!g_counts_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_counts_scratch);
+    e = cudaGetSymbolAddress(&p, g_counts_scratch);   // also makes the context current
     if (e != cudaSuccess) return e;
     g_counts_scratch_ptr[dev] = static_cast<int32_t*>(p);
+    g_counts_scratch_ctx[dev] = current_context();
+  } else {
+    void* ctx = current_context();
+    if (ctx != g_counts_scratch_ctx[dev]) {
+      e = cudaGetSymbolAddress(&p, g_counts_scratch);
+      if (e != cudaSuccess) return e;
+      g_counts_scratch_ptr[dev] = static_cast<int32_t*>(p);
+      g_counts_scratch_ctx[dev] = current_context();
+    }
   }
   *out = g_counts_scratch_ptr[dev];
   return cudaSuccess;
@@ -614,6 +647,8 @@ extern "C" mc2_status_t mc2_moe_counts_static(const mc2_shape_t* s, const int32_
   if (mc2_check_shape(s) != MC2_OK) return MC2_ERR_INVALID_ARG;
   if (!cnt || !recv || !offsets) return MC2_ERR_INVALID_ARG;
   if (s->T > 0 && (!sel || !permute_src || !unpermute_dst)) return MC2_ERR_INVALID_ARG;
+  if (!aligned({sel, cnt, recv, offsets, permute_src, unpermute_dst}))  // as mc2_moe_counts
+    return MC2_ERR_INVALID_ARG;
   const CountsGeom geo = counts_geom(*s);
   if (geo.EB * geo.G > kStaticCountsEntries) return MC2_ERR_UNSUPPORTED;  // beyond the fixed scratch
   int32_t* scratch = nullptr;

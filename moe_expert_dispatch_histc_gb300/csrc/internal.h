@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <initializer_list>
+
 #include <utility>
 
 #include "mc2moe.h"
@@ -15,6 +17,15 @@ constexpr int kCountsWarpsPerBlock = 8;
 constexpr size_t kWsAlign = 256;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Pointer rule of the C ABI: every array 16-byte aligned (vector and TMA
+// accesses), the workspace 256-byte aligned.  NULL passes (the null rules
+// are separate).
+inline bool aligned(std::initializer_list<const void*> ps, uintptr_t a = 16) {
+  for (const void* p : ps)
+    if (reinterpret_cast<uintptr_t>(p) & (a - 1)) return false;
+  return true;
+}
 
 // Sub-chunk geometry of the counts pass: every logical rank's entries
 // [r*RW, (r+1)*RW) are split into CPR chunks of kCountsSub (last one ragged),

@@ -101,6 +101,13 @@ def test_misaligned_pointers_are_rejected():
                                stream=0, check=False) == B.MC2_ERR_INVALID_ARG
     assert B.mc2_gmm_alltoallv(s, fake, None, fake, None, fake, fake, fake, fake, fake, odd,
                                stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+    # the allocation-free counts take the same pointer rule (on this machine a
+    # call that got past it would fail its device lookup with MC2_ERR_CUDA)
+    for i in range(6):
+        ptrs = [fake] * 6
+        ptrs[i] = odd
+        assert B.mc2_moe_counts_static(s, *ptrs, None, stream=0,
+                                       check=False) == B.MC2_ERR_INVALID_ARG, i
 
 
 def test_forward_validates_every_segment_before_enqueuing():

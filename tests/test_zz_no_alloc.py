@@ -44,10 +44,24 @@ def test_counts_static_matches_workspace_counts_twice():
             assert torch.equal(a, b), f"{name}: static-scratch counts differ from mc2_moe_counts"
 
 
+@pytest.mark.gpu
 def test_counts_static_rejects_shapes_beyond_its_scratch():
+    """A shape whose tables exceed the fixed scratch returns
+    MC2_ERR_UNSUPPORTED and launches nothing.  Every buffer passed is a real
+    device buffer of the size the shape asks for, so even a broken size check
+    would launch on valid memory."""
     build()
     # (E + 1) * W * ceil(T*k/W/256) = 1025 * 8 * 64 > 131072
-    big = B.Shape.make(131072, 64, 64, 1024, 1, 8, "bf16")
-    fake = 1 << 40  # never dereferenced: the size check comes first
-    assert B.mc2_moe_counts_static(big, fake, fake, fake, fake, fake, fake, None, stream=0,
+    T, E, k, W = 131072, 1024, 1, 8
+    big = B.Shape.make(T, 64, 64, E, k, W, "bf16")
+    i32 = dict(dtype=torch.int32, device="cuda")
+    sel = torch.zeros((T, k), **i32)
+    cnt, recv = torch.full((W, E), -7, **i32), torch.full((W, E), -7, **i32)
+    offsets = torch.full((E + 1,), -7, **i32)
+    src, dst = torch.full((T * k,), -7, **i32), torch.full((T * k,), -7, **i32)
+    st = torch.zeros(1, **i32)
+    assert B.mc2_moe_counts_static(big, sel, cnt, recv, offsets, src, dst, st,
                                    check=False) == B.MC2_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert int(cnt.min()) == -7 and int(cnt.max()) == -7, "a rejected call wrote its outputs"
+    assert int(st.item()) == 0
