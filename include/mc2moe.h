@@ -345,6 +345,15 @@ void mc2_set_counts_path(int32_t mode);
  * identical bit for bit.  Host only. */
 void mc2_set_mmrs_path(int32_t mode);
 
+/* Where later bf16/fp32 mc2_gmm_alltoallv calls of this thread do the
+ * weighted combine: 0 (default) in a separate kernel after fc2; 1 inside
+ * the fc2 kernel (top-k up to 8; larger k take the separate kernel): the
+ * fc2 kernel counts the rows of every (token, 256-column tile) as their
+ * stores complete, sums a few completed tokens per stored row block itself
+ * and leaves the rest to a follow-up kernel.  Both sum the same products in
+ * the same order: the outputs are identical bit for bit.  Host only. */
+void mc2_set_combine_path(int32_t mode);
+
 /* Programmatic dependent launch between the kernels of later calls of this
  * thread: 1 (default) lets each kernel's set-up overlap the end of the
  * previous kernel on the stream (each kernel still waits for its

@@ -65,6 +65,7 @@ _SIGS = {
     "mc2_set_launch_overlap": (None, [ctypes.c_int32]),
     "mc2_set_counts_path": (None, [ctypes.c_int32]),
     "mc2_set_mmrs_path": (None, [ctypes.c_int32]),
+    "mc2_set_combine_path": (None, [ctypes.c_int32]),
     "mc2_last_launch_count": (ctypes.c_int32, []),
     "mc2_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -283,6 +284,11 @@ def mc2_set_counts_path(mode: int) -> None:
 
 def mc2_set_mmrs_path(mode: int) -> None:
     lib().mc2_set_mmrs_path(int(mode))
+
+
+def mc2_set_combine_path(mode: int) -> None:
+    """0: the weighted combine in its own kernel (default); 1: inside the fc2 kernel."""
+    lib().mc2_set_combine_path(int(mode))
 
 
 def mc2_last_launch_count() -> int:

@@ -17,6 +17,7 @@ static thread_local int tl_tile_pairing = 0;
 static thread_local int tl_launch_overlap = 1;
 static thread_local int tl_counts_path = 0;
 static thread_local int tl_mmrs_path = 0;
+static thread_local int tl_combine_path = 0;
 static thread_local int tl_launches = 0;
 
 uint64_t wait_limit_ns() { return tl_wait_limit_ns ? tl_wait_limit_ns : 2000000000ull; }  // 2 s
@@ -28,6 +29,8 @@ bool launch_overlap_enabled() { return tl_launch_overlap != 0; }
 int counts_path_override() { return tl_counts_path; }
 
 int mmrs_path_override() { return tl_mmrs_path; }
+
+int combine_path_override() { return tl_combine_path; }
 
 void note_launches(int n) { tl_launches += n; }
 
@@ -48,6 +51,8 @@ WsLayout ws_layout(const mc2_shape_t& s) {
   L.base = take(static_cast<size_t>(g.EB) * g.G * 4);
   L.y = take(R * s.H * 2);
   L.yscale = take(R * (s.H / 64) * 4);
+  L.ctr = take(static_cast<size_t>(s.T) * ((s.H + 255) / 256) * 4);
+  L.defer = take(16 + static_cast<size_t>(s.T) * ((s.H + 255) / 256) * 4);
   if (s.act == MC2_F32) {
     L.x_t32 = take(static_cast<size_t>(s.T) * s.H * 4);
     L.w1_t32 = take(static_cast<size_t>(s.E) * s.H * 2 * s.I * 4);
@@ -256,6 +261,18 @@ mc2_status_t do_fc2(const mc2_shape_t* s, const void* h, const float* h_scale, c
     g.b = w2;
     g.a_elem_bytes = 2;
   }
+  if (fused_combine_supported(*s) && combine_path_override() == 1) {
+    // the fc2 kernel sums every token's rows itself as they complete
+    g.mode = MODE_FC2C;
+    g.probs = probs;
+    g.unpermute_dst = unpermute_dst;
+    g.ctr = reinterpret_cast<int32_t*>(w + L.ctr);
+    g.defer_count = reinterpret_cast<int32_t*>(w + L.defer);
+    g.defer_items = reinterpret_cast<int32_t*>(w + L.defer + 16);
+    g.comb_out = out;
+    g.out_dtype = s->out;
+    return cuda_status(launch_gemm(g, st));
+  }
   cudaError_t e = launch_gemm(g, st);
   if (e == cudaSuccess)
     e = launch_combine(*s, y, yscale, probs, offsets, unpermute_dst, out, s->out, st);
@@ -393,6 +410,8 @@ void mc2_set_launch_overlap(int32_t enabled) { tl_launch_overlap = enabled ? 1 :
 void mc2_set_counts_path(int32_t mode) { tl_counts_path = mode == 1 || mode == 2 ? mode : 0; }
 
 void mc2_set_mmrs_path(int32_t mode) { tl_mmrs_path = mode == 1 ? 1 : 0; }
+
+void mc2_set_combine_path(int32_t mode) { tl_combine_path = mode == 1 ? 1 : 0; }
 
 int32_t mc2_last_launch_count(void) { return tl_launches; }
 

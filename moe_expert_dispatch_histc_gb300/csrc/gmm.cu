@@ -45,13 +45,253 @@
 namespace mc2 {
 
 template <int MODE>
+constexpr bool kIsFc2 = MODE == MODE_FC2 || MODE == MODE_FC2C;
+
+// Warps 6..9: fc1's row gather, or fc2's combine warps when the combine is fused.
+template <int MODE>
 struct Roles {
-  static constexpr int kGatherWarps = MODE == MODE_FC1 || MODE == MODE_FC1_PRE ? 4 : 0;
+  static constexpr int kGatherWarps =
+      MODE == MODE_FC1 || MODE == MODE_FC1_PRE || MODE == MODE_FC2C ? 4 : 0;
   static constexpr int kThreads = (6 + kGatherWarps) * 32;
 };
 
 constexpr size_t SMEM_BYTES_FIXED = 1024 + STAGES * STAGE_BYTES + 4 * OUT_STAGE + 256;
 constexpr int NB1 = BN / 64;  // 64-column blocks of a bf16 B tile
+
+// ----------------------------------------------------------------------------
+// The weighted combine fused into fc2 (MODE_FC2C; selected by
+// mc2_set_combine_path(1), the separate combine_kernel is the default).
+//
+// out[t, :] = sum_j probs[t, j] * y(t, j) needs the k fc2 rows of token t,
+// which different tiles (different experts) produce on different SMs.  Each
+// (token, BN-column tile) has an arrival counter in the workspace, set by
+// combine_prep_kernel to k minus the token's valid slots.  An epilogue warp,
+// once the stores of its 32 rows of a tile have completed (checked one tile
+// later, so the wait costs nothing), hands the row range through a
+// shared-memory queue to its paired combine warp (warps 6..9).  The combine
+// warp publishes the rows at GPU scope and adds one arrival per row; the
+// row that brings a counter to k is its token's last.  It sums up to
+// COMBINE_LOCAL_TOKENS such tokens per row range itself -- 8 columns per
+// lane, all k rows of two tokens loaded before the first add -- and appends
+// the rest to a list that combine_deferred_kernel sums after fc2.  Every sum
+// uses combine_kernel's arithmetic and slot order, so the output is bitwise
+// the same as the separate pass.
+//
+// Measured on GB300 (fc2 + combine, 4096- / 16384-token workloads): separate
+// kernel 0.132 / 0.407 ms; this form 0.157 / 0.457 ms with 4 local tokens,
+// 0.144 / 0.432 ms deferring all, 0.221 / 0.563 ms summing all locally.  A
+// token completes only with its highest-numbered expert, so in the
+// expert-major tile order most tokens complete in the last tiles, where four
+// latency-bound warps per SM cannot keep up; and sums during the mainloop
+// take issue slots and memory bandwidth from the GEMM.
+// ----------------------------------------------------------------------------
+constexpr int CQ_SLOTS = 8;
+constexpr int KMAX_FUSED = 8;   // top-k handled by the fused combine
+
+struct CombineSlot {  // rows [grow0, grow0 + wrows) of column tile n are stored; n = -1: done
+  int32_t n, grow0, wrows;
+};
+
+struct CombineQueue {  // one per epilogue warp
+  uint64_t full[CQ_SLOTS];
+  uint64_t empty[CQ_SLOTS];
+  CombineSlot slot[CQ_SLOTS];
+};
+
+constexpr int CQ_BYTES = static_cast<int>((4 * sizeof(CombineQueue) + 7) / 8 * 8);
+
+template <int MODE>
+constexpr int kQueueBytes = MODE == MODE_FC2C ? CQ_BYTES : 0;
+
+__device__ __forceinline__ void combine_queue_init(CombineQueue* cq) {
+  for (int q = 0; q < 4; ++q)
+    for (int s = 0; s < CQ_SLOTS; ++s) {
+      mbar_init(&cq[q].full[s], 1);
+      mbar_init(&cq[q].empty[s], 1);
+    }
+}
+
+// Epilogue side: rows [grow0, grow0 + wrows) of column tile n have been
+// stored and lane 0 has waited for its bulk stores and fenced the async
+// proxy; hand the rows to the paired combine warp.  Lane 0 only.
+__device__ __forceinline__ bool combine_push(CombineQueue* q, int& qs, uint32_t& qph, int n,
+                                             int grow0, int wrows, const WaitCtl& ctl) {
+  if (!mbar_wait(&q->empty[qs], qph ^ 1, ctl)) return false;
+  q->slot[qs] = CombineSlot{n, grow0, wrows};
+  mbar_arrive(&q->full[qs]);  // release (CTA scope): the stores this warp made or waited for
+  if (++qs == CQ_SLOTS) { qs = 0; qph ^= 1; }
+  return true;
+}
+
+__device__ __forceinline__ void combine_add(float (&acc)[8], float pj, float f, const uint4& raw) {
+  const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __half22float2(h2[i]);
+    acc[2 * i] += __fmul_rn(pj, v.x * f);
+    acc[2 * i + 1] += __fmul_rn(pj, v.y * f);
+  }
+}
+
+struct CombineArgs {
+  const __half* y;          // fc2 rows [R, H], fp16 scaled
+  const float* yscale;      // [R, H/64]
+  void* out;                // [T, H] bf16 or fp32
+  int H, out_f32;
+  int32_t nvalid;           // rows p >= nvalid belong to invalid ids
+};
+
+// Sums NJ (token, column) jobs: out[t[u], col[u] .. +8) = sum over j
+// ascending of pj[u][j] * y(r[u][j]) for the valid rows r < nvalid.  A job
+// with t < 0 or an inactive column is skipped.  Every load of all jobs is
+// issued before the first add.
+template <int NJ>
+__device__ __forceinline__ void combine_jobs(const CombineArgs& a, const int (&t)[NJ],
+                                             const int (&col)[NJ],
+                                             const int32_t (&r)[NJ][KMAX_FUSED],
+                                             const float (&pj)[NJ][KMAX_FUSED]) {
+  float f[NJ][KMAX_FUSED];
+  uint4 raw[NJ][KMAX_FUSED];
+  const int HG = a.H / 64;
+#pragma unroll
+  for (int u = 0; u < NJ; ++u)
+#pragma unroll
+    for (int j = 0; j < KMAX_FUSED; ++j) {
+      const bool ok = t[u] >= 0 && col[u] < a.H && r[u][j] < a.nvalid;
+      const int64_t rr = ok ? r[u][j] : 0;
+      f[u][j] = ok ? ld_cg_f32(a.yscale + rr * HG + col[u] / 64) : 0.f;
+      raw[u][j] = ok ? ld_cg_u4(a.y + rr * a.H + col[u]) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+  for (int u = 0; u < NJ; ++u) {
+    if (t[u] < 0 || col[u] >= a.H) continue;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < KMAX_FUSED; ++j)
+      if (r[u][j] < a.nvalid) combine_add(acc, pj[u][j], f[u][j], raw[u][j]);
+    const int64_t o = static_cast<int64_t>(t[u]) * a.H + col[u];
+    if (a.out_f32) {
+      float4* d = reinterpret_cast<float4*>(static_cast<float*>(a.out) + o);
+      d[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      d[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + o) =
+          make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                     pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    }
+  }
+}
+
+// Tokens whose last row arrives while a combine warp still has a backlog are
+// not summed there but appended to a list in the workspace (item = token *
+// n_tiles + column tile); combine_deferred_kernel sums them after fc2 with
+// the whole GPU.  A combine warp sums at most this many tokens per batch of
+// stored rows itself, which keeps pace with the tiles during the mainloop;
+// the burst at the end (a token completes with its highest expert, so most
+// tokens complete in the last tiles of the expert-major order) is deferred.
+constexpr int COMBINE_LOCAL_TOKENS = 4;
+
+// A combine warp: takes stored row ranges from its queue until the epilogue
+// warp sends n = -1 (or the CTA aborts).  For each range: publish the rows
+// at GPU scope, add one arrival per row, and sum (or defer) every token whose
+// last row this was.
+__device__ __forceinline__ void combine_warp(const GemmParams& p, CombineQueue* q, int lane,
+                                             const WaitCtl& ctl) {
+  const int k = p.k;
+  CombineArgs a;
+  a.y = static_cast<const __half*>(p.out);
+  a.yscale = p.yscale;
+  a.out = p.comb_out;
+  a.H = p.out_cols;
+  a.out_f32 = p.out_f32;
+  a.nvalid = __ldg(p.offsets + p.E);
+  int qs = 0;
+  uint32_t qph = 0;
+  while (true) {
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait(&q->full[qs], qph, ctl);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) break;
+    const CombineSlot sl = q->slot[qs];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&q->empty[qs]);
+    if (++qs == CQ_SLOTS) { qs = 0; qph ^= 1; }
+    if (sl.n < 0) break;
+    fence_acq_rel_gpu();  // release the stored rows (observed through the queue) before arriving
+    int tok = 0;
+    bool last = false;
+    int32_t myr[KMAX_FUSED];
+    float myp[KMAX_FUSED];
+    if (lane < sl.wrows) {
+      tok = __ldg(p.permute_src + sl.grow0 + lane) / k;
+      const int old = atomicAdd(p.ctr + static_cast<int64_t>(tok) * p.n_tiles + sl.n, 1);
+#pragma unroll
+      for (int j = 0; j < KMAX_FUSED; ++j) {  // this token's rows and weights, in case it is done
+        myr[j] = j < k ? __ldg(p.unpermute_dst + static_cast<int64_t>(tok) * k + j) : a.nvalid;
+        myp[j] = j < k ? __ldg(p.probs + static_cast<int64_t>(tok) * k + j) : 0.f;
+      }
+      last = old == k - 1;
+    } else {
+#pragma unroll
+      for (int j = 0; j < KMAX_FUSED; ++j) {
+        myr[j] = a.nvalid;
+        myp[j] = 0.f;
+      }
+    }
+    uint32_t mask = __ballot_sync(0xffffffffu, last);
+    if (!mask) continue;
+    // beyond the local budget: defer (warp-aggregated append to the list)
+    uint32_t local = 0;
+    for (int i = 0; i < COMBINE_LOCAL_TOKENS && (mask & ~local); ++i)
+      local |= (mask & ~local) & (0u - (mask & ~local));  // lowest remaining bit
+    const uint32_t defer = mask & ~local;
+    if (defer) {
+      int base = 0;
+      if (lane == 0) base = atomicAdd(p.defer_count, __popc(defer));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if ((defer >> lane) & 1u)
+        p.defer_items[base + __popc(defer & ((1u << lane) - 1u))] = tok * p.n_tiles + sl.n;
+    }
+    if (!local) continue;
+    fence_acq_rel_gpu();  // acquire the tokens' other rows, released by their writers
+    const int colv = sl.n * BN + 8 * lane;
+    mask = local;
+    while (mask) {
+      const int b0 = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const bool two = mask != 0;
+      const int b1 = two ? __ffs(mask) - 1 : b0;
+      if (two) mask &= mask - 1;
+      int t[2] = {__shfl_sync(0xffffffffu, tok, b0), __shfl_sync(0xffffffffu, tok, b1)};
+      if (!two) t[1] = -1;
+      const int col[2] = {colv, colv};
+      int32_t r[2][KMAX_FUSED];
+      float pj[2][KMAX_FUSED];
+#pragma unroll
+      for (int j = 0; j < KMAX_FUSED; ++j) {
+        r[0][j] = __shfl_sync(0xffffffffu, myr[j], b0);
+        pj[0][j] = __shfl_sync(0xffffffffu, myp[j], b0);
+        r[1][j] = __shfl_sync(0xffffffffu, myr[j], b1);
+        pj[1][j] = __shfl_sync(0xffffffffu, myp[j], b1);
+      }
+      combine_jobs<2>(a, t, col, r, pj);
+    }
+  }
+}
+
+// Wait until at most `keep` of this thread's most recent bulk-store groups
+// are still in flight (keep = 0..4).
+__device__ __forceinline__ void bulk_wait_keep_n(int keep) {
+  switch (keep) {
+    case 0: bulk_wait_keep<0>(); break;
+    case 1: bulk_wait_keep<1>(); break;
+    case 2: bulk_wait_keep<2>(); break;
+    case 3: bulk_wait_keep<3>(); break;
+    default: bulk_wait_keep<4>(); break;
+  }
+}
 
 template <int MODE, int ES>
 __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
@@ -73,7 +313,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_STAGE;
   uint8_t* sOut = sB + STAGES * B_STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * OUT_STAGE);
+  CombineQueue* cq = reinterpret_cast<CombineQueue*>(sOut + 4 * OUT_STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * OUT_STAGE + kQueueBytes<MODE>);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -96,6 +337,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       mbar_init(&tempty[b], 4 * 32);
     }
     mbar_init(mma_done, 1);
+    if constexpr (MODE == MODE_FC2C) combine_queue_init(cq);
     *abort_sh = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -161,7 +403,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           if constexpr (BKM) {
             // K-major B: N rows of 128 bytes of K; fc1 loads the gate rows
             // and the up rows of the same output columns as two boxes
-            if (MODE != MODE_FC2) {
+            if (!kIsFc2<MODE>) {
               tma_load_3d(b_dst, &tmB, &full[s], k0, n * (BN / 2), e);
               tma_load_3d(b_dst + (BN / 2) * 128, &tmB, &full[s], k0, p.I + n * (BN / 2), e);
             } else {
@@ -170,7 +412,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           } else {
             // all NB 64-column blocks in one box: fc1 takes the gate and the
             // up blocks of the same output columns, fc2 NB adjacent blocks
-            if (MODE != MODE_FC2)
+            if (!kIsFc2<MODE>)
               tma_load_5d(b_dst, &tmB, &full[s], 0, k0, n * (NB / 2), 0, e);
             else
               tma_load_4d(b_dst, &tmB, &full[s], 0, k0, n * NB, e);
@@ -239,6 +481,9 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       mbar_wait(mma_done, 0, drain);
     }
     __syncwarp();
+  } else if (MODE == MODE_FC2C && warp >= 6) {
+    // ------------------------------------------------------------ fused combine
+    combine_warp(p, cq + (warp - 6), lane, ctl);
   } else if (warp >= 6) {
     // ------------------------------------------------------------ fc1 row gather
     // Thread t copies 16-byte chunk (t % 8) of rows t/8 + 16*i, i = 0..7, of
@@ -292,9 +537,13 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     const uint32_t row_off = static_cast<uint32_t>(lane) * 128;
     int acc = 0;
     uint32_t aph = 0;
+    // fused combine: the previous tile's rows wait here until their stores complete
+    int pend_grow0 = 0, pend_wrows = 0, pend_n = 0, qs = 0;
+    uint32_t qph = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, n, row0, rows;
       decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
+      int ngroups_tma = 0;
       bool ok = true;
       if (lane == 0) ok = mbar_wait(&tfull[acc], aph, ctl);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -304,11 +553,11 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       const int wrows = min(32, rows - q * 32);       // valid rows of this warp
       const int grow0 = row0 + q * 32;                 // first global row of this warp
       if (wrows > 0) {
-        constexpr int GROUP_COLS = 128 / (MODE != MODE_FC2 ? ES : 2);  // output cols per 128 B
-        constexpr int NGROUPS = (MODE != MODE_FC2 ? BN / 2 : BN) / GROUP_COLS;
+        constexpr int GROUP_COLS = 128 / (!kIsFc2<MODE> ? ES : 2);  // output cols per 128 B
+        constexpr int NGROUPS = (!kIsFc2<MODE> ? BN / 2 : BN) / GROUP_COLS;
 #pragma unroll 1
         for (int gi = 0; gi < NGROUPS; ++gi) {
-          const int col0 = n * (MODE != MODE_FC2 ? BN / 2 : BN) + gi * GROUP_COLS;
+          const int col0 = n * (!kIsFc2<MODE> ? BN / 2 : BN) + gi * GROUP_COLS;
           if (col0 >= p.out_cols) break;
           // the previous store out of this warp's staging buffer has read it
           if (lane == 0) bulk_wait_read_all();
@@ -356,7 +605,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
             }
             continue;
           }
-          if (MODE != MODE_FC2 && ES == 2) {
+          if (!kIsFc2<MODE> && ES == 2) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               uint32_t g[32], u[32];
@@ -377,7 +626,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
                     make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
               }
             }
-          } else if (MODE == MODE_FC2) {  // y as fp16 with a power-of-two scale per 64 columns
+          } else if (kIsFc2<MODE>) {  // y as fp16 with a power-of-two scale per 64 columns
             uint32_t a[32], b2[32], pk[32];
             tmem_ld32(tbase + gi * 64, a);
             tmem_ld32(tbase + gi * 64 + 32, b2);
@@ -391,7 +640,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
                   make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           } else {
             uint32_t v32[32];
-            if (MODE != MODE_FC2) {  // fp32 h, tf32-rounded for the fc2 tensor-core pass
+            if (!kIsFc2<MODE>) {  // fp32 h, tf32-rounded for the fc2 tensor-core pass
               uint32_t g[32];
               tmem_ld32(tbase + gi * 32, g);
               tmem_ld32(tbase + BN / 2 + gi * 32, v32);
@@ -416,10 +665,11 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
               tma_store_2d(&tmOut, stage, col0, grow0);
               bulk_commit();
             }
+            ++ngroups_tma;
           } else if (lane < wrows) {  // tail rows: plain stores of this lane's row
             char* dst = static_cast<char*>(p.out) +
                         (static_cast<int64_t>(grow0 + lane) * p.out_cols + col0) *
-                            (MODE != MODE_FC2 ? ES : 2);
+                            (!kIsFc2<MODE> ? ES : 2);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               reinterpret_cast<uint4*>(dst)[v] =
@@ -432,8 +682,30 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
       if (acc == 0) aph ^= 1;
+      if constexpr (MODE == MODE_FC2C) {
+        if (pend_wrows > 0) {
+          bool pushed = true;
+          if (lane == 0) {  // the previous tile's stores; this tile's may stay in flight
+            bulk_wait_keep_n(ngroups_tma);
+            fence_proxy_async_global();
+            pushed = combine_push(cq + q, qs, qph, pend_n, pend_grow0, pend_wrows, ctl);
+          }
+          if (!__shfl_sync(0xffffffffu, pushed, 0)) break;
+        }
+        pend_grow0 = grow0;
+        pend_wrows = wrows > 0 ? wrows : 0;
+        pend_n = n;
+      }
     }
     if (lane == 0) bulk_wait_all();
+    if constexpr (MODE == MODE_FC2C) {
+      if (lane == 0 && *abort_sh == 0) {
+        fence_proxy_async_global();
+        bool ok = true;
+        if (pend_wrows > 0) ok = combine_push(cq + q, qs, qph, pend_n, pend_grow0, pend_wrows, ctl);
+        if (ok) combine_push(cq + q, qs, qph, -1, 0, 0, ctl);  // no more work
+      }
+    }
     __syncwarp();
   }
 
@@ -487,7 +759,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + P_STAGES * A_STAGE;
   uint8_t* sOut = sB + P_STAGES * P_B_STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * OUT_STAGE);
+  CombineQueue* cq = reinterpret_cast<CombineQueue*>(sOut + 4 * OUT_STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * OUT_STAGE + kQueueBytes<MODE>);
   uint64_t* pfull = full + P_STAGES;       // even CTA: the odd CTA's stage landed
   uint64_t* empty = pfull + P_STAGES;
   uint64_t* tfull = empty + P_STAGES;
@@ -514,6 +787,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       mbar_init(&tempty[b], 2 * 4);  // one arrival per epilogue warp of both CTAs
     }
     mbar_init(mma_done, 1);
+    if constexpr (MODE == MODE_FC2C) combine_queue_init(cq);
     *abort_sh = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -588,7 +862,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           const int k0 = kb * BK;
           // this CTA's 128 columns of B: fc1 gate (even) or up (odd) half;
           // fc2 the first or second 128 of the 256-column tile
-          const int nbase = MODE != MODE_FC2 ? static_cast<int>(rank) * p.I + n * (BN / 2)
+          const int nbase = !kIsFc2<MODE> ? static_cast<int>(rank) * p.I + n * (BN / 2)
                                              : n * BN + static_cast<int>(rank) * (BN / 2);
           if (DIRECT && !leader) {
             const uint32_t bar = leader_full + s * 8;
@@ -596,7 +870,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
             if constexpr (BKM) {
               tma_load_3d_pair(b_dst, &tmB, bar, k0, nbase, e);
             } else {
-              if (MODE != MODE_FC2)
+              if (!kIsFc2<MODE>)
                 tma_load_5d_pair(b_dst, &tmB, bar, 0, k0, n * NBH, static_cast<int>(rank), e);
               else
                 tma_load_4d_pair(b_dst, &tmB, bar, 0, k0, nbase / BNB, e);
@@ -607,7 +881,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
             if constexpr (BKM) {
               tma_load_3d(b_dst, &tmB, &full[s], k0, nbase, e);
             } else {
-              if (MODE != MODE_FC2)
+              if (!kIsFc2<MODE>)
                 tma_load_5d(b_dst, &tmB, &full[s], 0, k0, n * NBH, static_cast<int>(rank), e);
               else
                 tma_load_4d(b_dst, &tmB, &full[s], 0, k0, nbase / BNB, e);
@@ -696,6 +970,9 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
         }
       }
     }
+  } else if (MODE == MODE_FC2C && warp >= 6) {
+    // ------------------------------------------------------------ fused combine
+    combine_warp(p, cq + (warp - 6), lane, ctl);
   } else if (warp >= 6) {
     // ------------------------------------------------------------ fc1 row gather
     const int t = threadIdx.x - 6 * 32;
@@ -745,9 +1022,13 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     const uint32_t leader_tempty = map_to_rank(tempty, 0);
     int acc = 0;
     uint32_t aph = 0;
+    // fused combine: the previous tile's rows wait here until their stores complete
+    int pend_grow0 = 0, pend_wrows = 0, pend_n = 0, qs = 0;
+    uint32_t qph = 0;
     for (int tile = cluster; tile < total; tile += nclusters) {
       int e, n, prow0, prows;
       decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, prow0, prows);
+      int ngroups_tma = 0;
       const int local = tile - prefix[e];
       const int m_pairs = (prefix[e + 1] - prefix[e]) / p.n_tiles;
       const int mp = local - (local / m_pairs) * m_pairs;
@@ -762,15 +1043,15 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       const int wrows = min(32, rows - q * 32);
       const int grow0 = row0 + q * 32;
       if (wrows > 0) {
-        constexpr int GROUP_COLS = 128 / (MODE != MODE_FC2 ? ES : 2);
-        constexpr int NGROUPS = (MODE != MODE_FC2 ? BN / 2 : BN) / GROUP_COLS;
+        constexpr int GROUP_COLS = 128 / (!kIsFc2<MODE> ? ES : 2);
+        constexpr int NGROUPS = (!kIsFc2<MODE> ? BN / 2 : BN) / GROUP_COLS;
 #pragma unroll 1
         for (int gi = 0; gi < NGROUPS; ++gi) {
-          const int col0 = n * (MODE != MODE_FC2 ? BN / 2 : BN) + gi * GROUP_COLS;
+          const int col0 = n * (!kIsFc2<MODE> ? BN / 2 : BN) + gi * GROUP_COLS;
           if (col0 >= p.out_cols) break;
           if (lane == 0) bulk_wait_read_all();
           __syncwarp();
-          if (MODE != MODE_FC2 && ES == 2) {
+          if (!kIsFc2<MODE> && ES == 2) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               uint32_t g[32], u[32];
@@ -791,7 +1072,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
                     make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
               }
             }
-          } else if (MODE == MODE_FC2) {  // y as fp16 with a power-of-two scale per 64 columns
+          } else if (kIsFc2<MODE>) {  // y as fp16 with a power-of-two scale per 64 columns
             uint32_t a[32], b2[32], pk[32];
             tmem_ld32(tbase + gi * 64, a);
             tmem_ld32(tbase + gi * 64 + 32, b2);
@@ -805,7 +1086,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
                   make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           } else {
             uint32_t v32[32];
-            if (MODE != MODE_FC2) {
+            if (!kIsFc2<MODE>) {
               uint32_t g[32];
               tmem_ld32(tbase + gi * 32, g);
               tmem_ld32(tbase + BN / 2 + gi * 32, v32);
@@ -830,10 +1111,11 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
               tma_store_2d(&tmOut, stage, col0, grow0);
               bulk_commit();
             }
+            ++ngroups_tma;
           } else if (lane < wrows) {
             char* dst = static_cast<char*>(p.out) +
                         (static_cast<int64_t>(grow0 + lane) * p.out_cols + col0) *
-                            (MODE != MODE_FC2 ? ES : 2);
+                            (!kIsFc2<MODE> ? ES : 2);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               reinterpret_cast<uint4*>(dst)[v] =
@@ -850,8 +1132,30 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       }
       acc ^= 1;
       if (acc == 0) aph ^= 1;
+      if constexpr (MODE == MODE_FC2C) {
+        if (pend_wrows > 0) {
+          bool pushed = true;
+          if (lane == 0) {  // the previous tile's stores; this tile's may stay in flight
+            bulk_wait_keep_n(ngroups_tma);
+            fence_proxy_async_global();
+            pushed = combine_push(cq + q, qs, qph, pend_n, pend_grow0, pend_wrows, ctl);
+          }
+          if (!__shfl_sync(0xffffffffu, pushed, 0)) break;
+        }
+        pend_grow0 = grow0;
+        pend_wrows = wrows > 0 ? wrows : 0;
+        pend_n = n;
+      }
     }
     if (lane == 0) bulk_wait_all();
+    if constexpr (MODE == MODE_FC2C) {
+      if (lane == 0 && *abort_sh == 0) {
+        fence_proxy_async_global();
+        bool ok = true;
+        if (pend_wrows > 0) ok = combine_push(cq + q, qs, qph, pend_n, pend_grow0, pend_wrows, ctl);
+        if (ok) combine_push(cq + q, qs, qph, -1, 0, 0, ctl);  // no more work
+      }
+    }
     __syncwarp();
   }
 
@@ -1012,8 +1316,15 @@ static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
   p.k = s.k;
   p.I = s.I;
   p.wait_limit_ns = wait_limit_ns();
+  p.probs = g.probs;
+  p.unpermute_dst = g.unpermute_dst;
+  p.ctr = g.ctr;
+  p.defer_items = g.defer_items;
+  p.defer_count = g.defer_count;
+  p.comb_out = g.comb_out;
+  p.out_f32 = g.out_dtype == MC2_F32 ? 1 : 0;
   bool ok;
-  if (MODE != MODE_FC2) {
+  if (!kIsFc2<MODE>) {
     p.K = s.H;
     p.n_tiles = (s.I + BN / 2 - 1) / (BN / 2);
     p.out_cols = s.I;
@@ -1034,13 +1345,14 @@ static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
          encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.out, s.H, R, 64, 32);
   }
   if (!ok) return cudaErrorInvalidValue;
-  const size_t smem = SMEM_BYTES_FIXED + (s.E + 1) * sizeof(int32_t);
+  constexpr size_t fixed = SMEM_BYTES_FIXED + kQueueBytes<MODE>;
+  const size_t smem = fixed + (s.E + 1) * sizeof(int32_t);
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(gmm_kernel<MODE, ES>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(SMEM_BYTES_FIXED + 1025 * sizeof(int32_t)));
+                                    static_cast<int>(fixed + 1025 * sizeof(int32_t)));
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t tiles_upper = (R / BM + s.E) * static_cast<int64_t>(p.n_tiles);
@@ -1068,8 +1380,15 @@ static cudaError_t launch_pair(const GemmArgs& g, cudaStream_t st) {
   p.k = s.k;
   p.I = s.I;
   p.wait_limit_ns = wait_limit_ns();
+  p.probs = g.probs;
+  p.unpermute_dst = g.unpermute_dst;
+  p.ctr = g.ctr;
+  p.defer_items = g.defer_items;
+  p.defer_count = g.defer_count;
+  p.comb_out = g.comb_out;
+  p.out_f32 = g.out_dtype == MC2_F32 ? 1 : 0;
   bool ok;
-  if (MODE != MODE_FC2) {
+  if (!kIsFc2<MODE>) {
     p.K = s.H;
     p.n_tiles = (s.I + BN / 2 - 1) / (BN / 2);
     p.out_cols = s.I;
@@ -1090,13 +1409,14 @@ static cudaError_t launch_pair(const GemmArgs& g, cudaStream_t st) {
          encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.out, s.H, R, 64, 32);
   }
   if (!ok) return cudaErrorInvalidValue;
-  const size_t smem = P_SMEM_BYTES_FIXED + (s.E + 1) * sizeof(int32_t);
+  constexpr size_t fixed = P_SMEM_BYTES_FIXED + kQueueBytes<MODE>;
+  const size_t smem = fixed + (s.E + 1) * sizeof(int32_t);
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(gmm_pair_kernel<MODE, ES>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(P_SMEM_BYTES_FIXED + 1025 * sizeof(int32_t)));
+                                    static_cast<int>(fixed + 1025 * sizeof(int32_t)));
   });
   if (attr_err != cudaSuccess) return attr_err;
   cudaLaunchConfig_t cfg = {};
@@ -1139,7 +1459,101 @@ static bool use_pairs(const mc2_shape_t& s, int mode) {
   if (forced == 1) return false;
   if (forced == 2) return num_sms() >= 2;
   const int64_t R = static_cast<int64_t>(s.T) * s.k;
-  return mode == MODE_FC2 && num_sms() >= 2 && R >= 2 * BM * static_cast<int64_t>(s.E);
+  return (mode == MODE_FC2 || mode == MODE_FC2C) && num_sms() >= 2 &&
+         R >= 2 * BM * static_cast<int64_t>(s.E);
+}
+
+bool fused_combine_supported(const mc2_shape_t& s) {
+  const int64_t items = static_cast<int64_t>(s.T) * ((s.H + BN - 1) / BN);
+  return s.k >= 1 && s.k <= KMAX_FUSED && items < (int64_t(1) << 31);
+}
+
+// Before a fused fc2 + combine: every (token, column tile) counter starts at
+// k minus the token's valid slots (so the last of its rows brings it to k),
+// and a token with no valid slot gets its zero output row here (no fc2 row
+// will ever complete it).  One thread per token.
+__global__ void combine_prep_kernel(const int32_t* __restrict__ offsets,
+                                    const int32_t* __restrict__ unpermute_dst, int32_t* ctr,
+                                    int32_t* defer_count, void* out, int64_t T, int k, int E,
+                                    int H, int n_tiles, int out_f32) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t == 0) *defer_count = 0;
+  if (t >= T) return;
+  const int32_t nvalid = __ldg(offsets + E);
+  int valid = 0;
+  for (int j = 0; j < k; ++j) valid += __ldg(unpermute_dst + t * k + j) < nvalid;
+  for (int n = 0; n < n_tiles; ++n) ctr[t * n_tiles + n] = k - valid;
+  if (valid == 0) {
+    if (out_f32) {
+      float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + t * H);
+      for (int c = 0; c < H / 4; ++c) o[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + t * H);
+      for (int c = 0; c < H / 8; ++c) o[c] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+static cudaError_t launch_combine_prep(const GemmArgs& g, cudaStream_t st) {
+  const mc2_shape_t& s = *g.s;
+  const int threads = 256;
+  const int64_t blocks = (static_cast<int64_t>(s.T) + threads - 1) / threads;
+  const cudaError_t e = launch_kernel(
+      combine_prep_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st, 1,
+      g.offsets, g.unpermute_dst, g.ctr, g.defer_count, g.comb_out, static_cast<int64_t>(s.T),
+      static_cast<int>(s.k), static_cast<int>(s.E), static_cast<int>(s.H), (s.H + BN - 1) / BN,
+      g.out_dtype == MC2_F32 ? 1 : 0);
+  note_launches(1);
+  return e;
+}
+
+// After a fused fc2 + combine: the (token, column tile) sums the combine
+// warps deferred, one per warp iteration, over a grid-stride loop.
+__global__ void __launch_bounds__(256) combine_deferred_kernel(
+    const __half* __restrict__ y, const float* __restrict__ yscale,
+    const float* __restrict__ probs, const int32_t* __restrict__ offsets,
+    const int32_t* __restrict__ unpermute_dst, const int32_t* __restrict__ items,
+    const int32_t* __restrict__ count, void* out, int H, int k, int E, int n_tiles,
+    int out_f32) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int n_items = *count;
+  CombineArgs a;
+  a.y = y;
+  a.yscale = yscale;
+  a.out = out;
+  a.H = H;
+  a.out_f32 = out_f32;
+  a.nvalid = __ldg(offsets + E);
+  for (int64_t i = warp; i < n_items; i += nwarps) {
+    const int item = __ldg(items + i);
+    const int t[1] = {item / n_tiles};
+    const int col[1] = {(item - t[0] * n_tiles) * BN + 8 * lane};
+    int32_t r[1][KMAX_FUSED];
+    float pj[1][KMAX_FUSED];
+#pragma unroll
+    for (int j = 0; j < KMAX_FUSED; ++j) {
+      r[0][j] = j < k ? __ldg(unpermute_dst + static_cast<int64_t>(t[0]) * k + j) : a.nvalid;
+      pj[0][j] = j < k ? __ldg(probs + static_cast<int64_t>(t[0]) * k + j) : 0.f;
+    }
+    combine_jobs<1>(a, t, col, r, pj);
+  }
+}
+
+static cudaError_t launch_combine_deferred(const GemmArgs& g, cudaStream_t st) {
+  const mc2_shape_t& s = *g.s;
+  const cudaError_t e = launch_kernel(
+      combine_deferred_kernel, dim3(static_cast<unsigned>(num_sms() * 8)), dim3(256), 0, st, 1,
+      static_cast<const __half*>(g.out), g.yscale, g.probs, g.offsets, g.unpermute_dst,
+      g.defer_items, g.defer_count, g.comb_out, static_cast<int>(s.H), static_cast<int>(s.k),
+      static_cast<int>(s.E), (s.H + BN - 1) / BN, g.out_dtype == MC2_F32 ? 1 : 0);
+  note_launches(1);
+  return e;
 }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
@@ -1157,6 +1571,19 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
   } else if (g.mode == MODE_FC1_ROWS) {  // bf16 only
     if (g.a_elem_bytes != 2) return cudaErrorInvalidValue;
     e = pairs ? launch_pair<MODE_FC1_ROWS, 2>(g, st) : launch_one<MODE_FC1_ROWS, 2>(g, st);
+  } else if (g.mode == MODE_FC2C) {  // fc2 with the weighted combine fused in
+    if (!fused_combine_supported(*g.s) || !g.probs || !g.unpermute_dst || !g.ctr ||
+        !g.defer_items || !g.defer_count || !g.comb_out)
+      return cudaErrorInvalidValue;
+    e = launch_combine_prep(g, st);
+    if (e != cudaSuccess) return e;
+    if (pairs)
+      e = g.a_elem_bytes == 2 ? launch_pair<MODE_FC2C, 2>(g, st) : launch_pair<MODE_FC2C, 4>(g, st);
+    else
+      e = g.a_elem_bytes == 2 ? launch_one<MODE_FC2C, 2>(g, st) : launch_one<MODE_FC2C, 4>(g, st);
+    note_launches(1);
+    if (e == cudaSuccess) e = launch_combine_deferred(g, st);
+    return e;
   } else {
     if (pairs)
       e = g.a_elem_bytes == 2 ? launch_pair<MODE_FC2, 2>(g, st) : launch_pair<MODE_FC2, 4>(g, st);

@@ -31,6 +31,14 @@ struct GemmParams {
   void* out;                    // fc1: h [R, I]; fc2: y [R, H] fp16 (scaled)
   float* yscale;                // fc2: decode factor per (row, 64 columns) [R, H/64]
   int32_t* dev_status;
+  // fc2 with the combine fused (MODE_FC2C)
+  const float* probs;           // routing weights [T, k]
+  const int32_t* unpermute_dst; // [T*k]
+  int32_t* ctr;                 // arrivals per (token, BN-column tile) [T, n_tiles]
+  int32_t* defer_items;         // (token, column tile) sums left to combine_deferred_kernel
+  int32_t* defer_count;         // number of deferred items
+  void* comb_out;               // the block output [T, H], bf16 or fp32
+  int out_f32;
   int E, k, K, n_tiles, out_cols, I;
   uint64_t wait_limit_ns;
 };

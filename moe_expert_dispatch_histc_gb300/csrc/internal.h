@@ -41,13 +41,17 @@ CountsGeom counts_geom(const mc2_shape_t& s);
 // fc1 + SwiGLU on rows that are already permuted (the non-fused baseline
 // path; plain TMA A tiles); MODE_FC1_PRE: fc1 with the permute folded in,
 // writing the pre-activation gate|up rows G [R, 2I] in bf16 (the backward).
-enum { MODE_FC1 = 0, MODE_FC2 = 1, MODE_FC1_ROWS = 2, MODE_FC1_PRE = 3 };
+// MODE_FC2C: fc2 with the weighted combine fused in (the block's output is
+// written by the fc2 kernel itself).
+enum { MODE_FC1 = 0, MODE_FC2 = 1, MODE_FC1_ROWS = 2, MODE_FC1_PRE = 3, MODE_FC2C = 4 };
 
 // Workspace layout (byte offsets from ws).
 struct WsLayout {
   size_t hist, base;     // int32 [EB * G] each
   size_t y;              // fp16 [R, H] fc2 rows, expert-major, scaled (combine input)
   size_t yscale;         // fp32 [R, H/64] decode factor of each 64-column group of y
+  size_t ctr;            // int32 [T, ceil(H/256)] row arrivals of the fused combine
+  size_t defer;          // int32 count, then [T * ceil(H/256)] deferred (token, tile) sums
   size_t x_t32, w1_t32, w2_t32;  // fp32 tf32-rounded copies, weights transposed to [E, N, K] (act F32 only)
   size_t h_f32;          // fp32 [R, I] pre-requant SwiGLU output (act I8 only)
   size_t rowmax;         // uint32 [R] row absmax bits (act I8 only)
@@ -60,6 +64,7 @@ WsLayout ws_layout(const mc2_shape_t& s);
 uint64_t wait_limit_ns();
 bool launch_overlap_enabled();  // programmatic dependent launch between the block's kernels
 int counts_path_override();     // 0 auto, 1 three launches, 2 one cluster launch when it fits
+int combine_path_override();    // 0 separate combine kernel, 1 fused into fc2 when supported
 int mmrs_path_override();       // 0 fused (default), 1 two passes through int32 partials
 
 // Launch `kernel` on `st` with programmatic stream serialization (so its
@@ -116,8 +121,19 @@ struct GemmArgs {
   int32_t* dev_status;
   int a_elem_bytes;         // 2 (bf16) or 4 (f32)
   int mode;                 // see gmm.cu
+  // MODE_FC2C only: the combine's inputs and output
+  const float* probs;
+  const int32_t* unpermute_dst;
+  int32_t* ctr;             // workspace counters [T, ceil(H/256)]
+  int32_t* defer_items;     // workspace list [T * ceil(H/256)] of deferred sums
+  int32_t* defer_count;     // workspace int32: its length
+  void* comb_out;           // [T, H], bf16 (out_dtype MC2_BF16) or fp32
+  int out_dtype;
 };
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st);
+// Whether the fc2 kernel can fuse the combine for this shape (top-k 1, 2, 4
+// or 8); otherwise the separate combine kernel runs.
+bool fused_combine_supported(const mc2_shape_t& s);
 cudaError_t launch_permute_rows(const mc2_shape_t& s, const void* x, const int32_t* permute_src,
                                 void* xp, cudaStream_t st);
 // dW [E, M, N] fp32 = per expert A_e^T @ B_e over its permuted rows; A [R, M],

@@ -223,6 +223,46 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Every committed bulk store but the N most recent groups has completed.
+template <int N>
+__device__ __forceinline__ void bulk_wait_keep() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Orders this thread's accesses through the async proxy (completed bulk
+// stores to global memory) with its later generic-proxy accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Acquire-release fence at GPU scope (publishes this thread's earlier writes
+// before a later flag write; orders a flag read before later reads).
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// 16-byte global load cached in L2 only (data written by other SMs during
+// this kernel: never served from a possibly stale L1 line).
+__device__ __forceinline__ uint4 ld_cg_u4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float ld_cg_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
+// Drop a 128-byte L2 line without writing it back: its contents become
+// undefined.  For intermediate data that no one reads again.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // ----------------------------------------------------------------------------
 // cp.async (16-byte, L2-cached) for row gathers the tensor maps cannot express
 // ----------------------------------------------------------------------------

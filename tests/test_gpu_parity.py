@@ -186,6 +186,70 @@ def test_launch_overlap_changes_nothing(wl):
     assert int(b1.dev_status.item()) == 0
 
 
+COMBINE_SHAPES = [
+    Workload("c_multi_mtile", 1024, 256, 128, 8, 2, 2, "bf16"),
+    Workload("c_ragged_n", 384, 320, 192, 6, 3, 3, "bf16"),     # k = 3; H = 320: a partial tile
+    Workload("c_k8", 512, 512, 128, 16, 8, 4, "bf16"),
+    Workload("c_k1", 200, 128, 64, 4, 1, 2, "bf16"),
+    Workload("c_fp32", 96, 192, 64, 4, 2, 2, "f32"),
+    Workload("c_k10", 128, 256, 64, 16, 10, 2, "bf16"),         # k > 8: the separate kernel
+]
+
+
+@pytest.mark.parametrize("wl", COMBINE_SHAPES, ids=lambda w: w.name)
+def test_fused_combine_equals_separate_bitwise(wl, pairing):
+    """The combine inside the fc2 kernel and the separate combine kernel sum
+    the same products in the same slot order: bitwise the same output, also
+    with invalid ids and a token whose every slot is invalid (a zero row)."""
+    inp = make_inputs(wl, 12)
+    sel = inp["sel"].copy()
+    sel[0, :] = wl.E                     # token 0: no valid slot
+    sel[5 % wl.T, 0] = -1
+    sel[wl.T - 1, wl.k - 1] = 1 << 20
+    inp["sel"] = np.ascontiguousarray(sel)
+    outs = []
+    for mode in (0, 1):   # separate kernel, then fused into fc2
+        B.mc2_set_combine_path(mode)
+        try:
+            _, _, b = run_gpu(wl, inputs=inp)
+        finally:
+            B.mc2_set_combine_path(0)
+        outs.append(b)
+        assert int(b.dev_status.item()) == B.MC2_DEV_BAD_EXPERT_ID
+    o0, o1 = outs[0].out, outs[1].out
+    iv = torch.int32 if o0.dtype == torch.float32 else torch.int16
+    assert torch.equal(o0.view(iv), o1.view(iv)), "fused combine differs from the separate kernel"
+    assert float(o1[0].abs().max()) == 0.0
+    x, w1, w2 = (as_f64(inp[n], wl.act) for n in ("x", "w1", "w2"))
+    ref = orc.block_forward(x, w1, w2, inp["sel"], inp["probs"], wl.E, wl.W,
+                            h_dtype=H_DTYPE[wl.act])
+    _tol(to_np(o1), ref["out"], "out with the fused combine")
+
+
+@pytest.mark.parametrize("name", ["uniform", "skew"])
+def test_fused_combine_full_size_repeated_calls(name):
+    """The fused combine at full size (CTA pairs, many tokens completing in
+    the last tiles, so both the local sums and the deferred list are used):
+    three fc2 calls in a row on one workspace (counters and list re-armed by
+    every call) give the separate kernel's bits each time."""
+    from moe_expert_dispatch_histc_gb300 import block as blk
+    wl = WORKLOADS[name]
+    inp, d, b = run_gpu(wl, seed=13)
+    ref = b.out.clone()
+    try:
+        B.mc2_set_combine_path(1)
+        for _ in range(3):
+            b.out.zero_()
+            B.mc2_gmm_alltoallv(blk.shape_of(wl), b.h, None, d["w2"], None, b.offsets,
+                                b.permute_src, b.unpermute_dst, d["probs"], b.ws, b.out,
+                                b.dev_status)
+            torch.cuda.synchronize()
+            assert torch.equal(ref.view(torch.int16), b.out.view(torch.int16))
+    finally:
+        B.mc2_set_combine_path(0)
+    assert int(b.dev_status.item()) == 0
+
+
 def _unfused(wl, seed, out=None):
     from moe_expert_dispatch_histc_gb300 import block as blk
     inp = make_inputs(wl, seed)
