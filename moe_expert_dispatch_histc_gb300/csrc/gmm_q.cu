@@ -218,30 +218,34 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
           uint8_t* a_dst = sA + s * A_STAGE;
           uint8_t* b_dst = sB + s * B_STAGE;
           const int k0 = kb * BK;
+          // B through a blocked map (64-column blocks of 128 bytes): one box
+          // per stage.  Single CTA: fc1 the gate block n and the up block n
+          // ([half][k row][128 B]), fc2 blocks 2n and 2n + 1.  Pair: this
+          // CTA's one block -- fc1 gate (even CTA) or up (odd CTA) block n,
+          // fc2 block 2n + rank.
           if constexpr (PAIR) {
-            // this CTA's 64 columns: fc1 gate (even) / up (odd) block n;
-            // fc2 the even or odd half of the 128 output columns
-            const int col = MODE == MODE_FC1 ? static_cast<int>(rank) * p.I + n * 64
-                                             : n * QBN + static_cast<int>(rank) * 64;
             if (DIRECT && !leader) {
               const uint32_t bar = leader_full + s * 8;
               tma_load_2d_pair(a_dst, &tmA, bar, k0, row0);
-              tma_load_3d_pair(b_dst, &tmB, bar, col, k0, e);
+              if (MODE == MODE_FC1)
+                tma_load_5d_pair(b_dst, &tmB, bar, 0, k0, n, static_cast<int>(rank), e);
+              else
+                tma_load_4d_pair(b_dst, &tmB, bar, 0, k0, 2 * n + static_cast<int>(rank), e);
             } else {
               mbar_arrive_expect_tx(&full[s], GATHER ? B_STAGE : 2 * G::kStageBytes);
               if (!GATHER) tma_load_2d(a_dst, &tmA, &full[s], k0, row0);
-              tma_load_3d(b_dst, &tmB, &full[s], col, k0, e);
+              if (MODE == MODE_FC1)
+                tma_load_5d(b_dst, &tmB, &full[s], 0, k0, n, static_cast<int>(rank), e);
+              else
+                tma_load_4d(b_dst, &tmB, &full[s], 0, k0, 2 * n + static_cast<int>(rank), e);
             }
           } else {
             mbar_arrive_expect_tx(&full[s], GATHER ? B_STAGE : G::kStageBytes);
             if (!GATHER) tma_load_2d(a_dst, &tmA, &full[s], k0, row0);
-            if (MODE == MODE_FC1) {  // 64 gate columns, then the 64 up columns
-              tma_load_3d(b_dst, &tmB, &full[s], n * 64, k0, e);
-              tma_load_3d(b_dst + B_BLOCK, &tmB, &full[s], p.I + n * 64, k0, e);
-            } else {
-              tma_load_3d(b_dst, &tmB, &full[s], n * QBN, k0, e);
-              tma_load_3d(b_dst + B_BLOCK, &tmB, &full[s], n * QBN + 64, k0, e);
-            }
+            if (MODE == MODE_FC1)
+              tma_load_5d(b_dst, &tmB, &full[s], 0, k0, n, 0, e);
+            else
+              tma_load_4d(b_dst, &tmB, &full[s], 0, k0, 2 * n, e);
           }
         }
         __syncwarp();
@@ -642,7 +646,7 @@ static cudaError_t launch_q(const QArgs& g, cudaStream_t st) {
   if (MODE == MODE_FC1) {
     p.K = s.H;
     p.n_tiles = s.I / 64;
-    ok = encode_3d(&tB, bf, 2, g.b, 2ull * s.I, s.H, s.E, 64, 64);
+    ok = encode_b_blocked(&tB, g.b, s.H, 2ull * s.I, s.E, 2, 64, 1, PAIR ? 1 : 2);
     tA = tB;  // unused: fc1's A rows are gathered with cp.async
     tOut = tB;
     if (!g.raw) ok = ok && encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.out, s.I, R, 32, 32);
@@ -650,7 +654,7 @@ static cudaError_t launch_q(const QArgs& g, cudaStream_t st) {
     p.K = s.I;
     p.n_tiles = (s.H + QBN - 1) / QBN;  // H is a multiple of 64: the last tile may be half full
     ok = encode_2d(&tA, bf, 2, g.a, s.I, R, 64, BM) &&
-         encode_3d(&tB, bf, 2, g.b, s.H, s.I, s.E, 64, 64);
+         encode_b_blocked(&tB, g.b, s.I, s.H, s.E, 1, 64, PAIR ? 1 : 2, 1);
     tOut = tB;
     if (!g.raw) ok = ok && encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.out, s.H, R, 64, 32);
   }

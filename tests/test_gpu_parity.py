@@ -119,9 +119,10 @@ SMALL = [
 ]
 
 
-@pytest.fixture(params=[1, 2], ids=["single_cta", "cta_pairs"])
+@pytest.fixture(params=[1, 2, 3], ids=["single_cta", "cta_pairs", "mcast_fc1"])
 def pairing(request):
-    """Force one grouped-GEMM tiling (single CTAs or CTA pairs) for the test."""
+    """Force one grouped-GEMM tiling (single CTAs, CTA pairs, or fc1 on
+    multicast 2-CTA clusters) for the test."""
     ensure_built()
     B.mc2_set_tile_pairing(request.param)
     yield request.param
@@ -161,6 +162,26 @@ def test_fc2_alone_on_oracle_h():
                         b.unpermute_dst, d["probs"], b.ws, b.out, b.dev_status)
     torch.cuda.synchronize()
     _tol(to_np(b.out), ref["out"], "out from oracle h")
+
+
+@pytest.mark.parametrize("name", ["uniform", "skew"])
+def test_tilings_equal_bitwise_full_size(name):
+    """Every fc1 tiling accumulates each output in the same K order: the
+    full-size h and out are identical bit for bit across single CTAs, CTA
+    pairs and multicast clusters."""
+    wl = WORKLOADS[name]
+    res = []
+    for mode in (1, 2, 3):
+        B.mc2_set_tile_pairing(mode)
+        try:
+            _, _, b = run_gpu(wl, seed=5)
+        finally:
+            B.mc2_set_tile_pairing(0)
+        assert int(b.dev_status.item()) == 0
+        res.append(b)
+    for b in res[1:]:
+        assert torch.equal(res[0].h.view(torch.int16), b.h.view(torch.int16))
+        assert torch.equal(res[0].out.view(torch.int16), b.out.view(torch.int16))
 
 
 def test_determinism_bitwise(pairing):
