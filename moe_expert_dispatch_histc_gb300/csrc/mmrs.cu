@@ -148,9 +148,26 @@ struct FParams {
   const float* xs;       // x1_scale [W, m]
   const float* ws;       // x2_scale [W, n]
   int32_t* dev_status;
-  int W, m, n, K, n_tiles, total, nchunk;
+  int W, m, n, K, n_tiles, m_tiles, total, nchunk;
   uint64_t wait_limit_ns;
 };
+
+// Output tile order: groups of MMRS_GROUP_M row blocks, and within a group
+// the row block varies fastest.  The clusters running at the same time then
+// cover a near-square block of output tiles, so the x1 row blocks and x2
+// column blocks they stream (for every rank) are shared by many of them,
+// and consecutive waves reuse the same row blocks from L2.
+constexpr int MMRS_GROUP_M = 8;
+
+__device__ __forceinline__ void mmrs_tile(int tile, int m_tiles, int n_tiles, int& mt, int& nt) {
+  const int per_group = MMRS_GROUP_M * n_tiles;
+  const int g = tile / per_group;
+  const int first = g * MMRS_GROUP_M;
+  const int gm = min(MMRS_GROUP_M, m_tiles - first);
+  const int local = tile - g * per_group;
+  mt = first + local % gm;
+  nt = local / gm;
+}
 
 template <int GW>
 __device__ __forceinline__ void tmem_ld_group(uint32_t taddr, uint32_t (&v)[GW]) {
@@ -244,7 +261,8 @@ __global__ void __launch_bounds__(FCfg<NB>::kThreads, 1)
     int n_arm = 0;
     bool ok = true;
     for (int tile = cluster; tile < total && ok; tile += nclusters) {
-      const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+      int mt, nt;
+      mmrs_tile(tile, p.m_tiles, p.n_tiles, mt, nt);
       const int row0 = mt * 256 + static_cast<int>(rank) * 128;     // row within a rank's x1
       const int col0 = nt * NB + static_cast<int>(rank) * (NB / 2);  // this CTA's half of B
       for (int r = 0; r < p.W && ok; ++r) {
@@ -345,7 +363,8 @@ __global__ void __launch_bounds__(FCfg<NB>::kThreads, 1)
     uint32_t aph = 0;
     bool ok = true;
     for (int tile = cluster; tile < total && ok; tile += nclusters) {
-      const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+      int mt, nt;
+      mmrs_tile(tile, p.m_tiles, p.n_tiles, mt, nt);
       const int grow0 = mt * 256 + static_cast<int>(rank) * 128 + q * 32;
       const int grow = grow0 + lane;
       const bool valid = grow < p.m;
@@ -438,7 +457,8 @@ cudaError_t launch_fused(const CUtensorMap& tA, const CUtensorMap& tB, const CUt
                          FParams p, cudaStream_t st) {
   using C = FCfg<NB>;
   p.n_tiles = (p.n + NB - 1) / NB;
-  p.total = ((p.m + 255) / 256) * p.n_tiles;
+  p.m_tiles = (p.m + 255) / 256;
+  p.total = p.m_tiles * p.n_tiles;
   // Persistent grid: as many pairs as can be resident at once (a pair needs
   // two SMs of one GPC, so this can be fewer than SMs / 2).
   static std::once_flag once;
