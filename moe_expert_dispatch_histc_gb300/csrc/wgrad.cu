@@ -9,9 +9,10 @@
 //  dw1: A = the permuted x rows, B = dG).  The token rows are the reduction
 // axis, so both operands are MN-major: a k-block is 64 consecutive rows of A
 // and of B, loaded as 128-byte-swizzled [64 rows][64 columns] blocks through
-// TMA.  The last k-block of an expert reaches into the next expert's rows;
-// the MMA warp zeroes those rows of the B stage before the MMAs read it, so
-// they add nothing.  One CTA per 128 x 256 output tile, the expert's rows in
+// TMA.  The last k-block of an expert reaches into the next expert's rows:
+// only its 16-row MMA steps with rows of the expert are issued, and the A
+// rows past the expert's end inside the last step are zeroed first (zeroing
+// the whole tail of B instead cost a quarter of the kernel's time).  One CTA per 128 x 256 output tile, the expert's rows in
 // order, so each tile is written once (no split over K, no atomics).
 //
 // Warp roles: warp 0 TMA producer, warp 1 MMA issuer (all 32 lanes zero the
@@ -152,16 +153,20 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
         if (lane == 0) ok = mbar_wait(&full[s], ph, ctl);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
+        // The block's rows past r1 belong to the next expert.  Only the
+        // 16-row MMA steps holding rows of expert e are issued, and inside
+        // the last of them the A rows past r1 (both 64-column blocks, at most
+        // 15 rows) are zeroed so they add nothing.
         const int rv = r1 - k0;  // rows of this block that belong to expert e
+        int nk = WG_BK / 16;
         if (rv < WG_BK) {
-          // zero the other experts' rows of B: 4 blocks x (64 - rv) rows x 128 B
-          uint8_t* b = sB + s * WG_B_STAGE;
-          const int nchunks = 4 * (WG_BK - rv) * 8;
-          for (int c = lane; c < nchunks; c += 32) {
-            const int blk = c / ((WG_BK - rv) * 8);
-            const int rem = c - blk * (WG_BK - rv) * 8;
-            const int row = rv + rem / 8;
-            *reinterpret_cast<uint4*>(b + blk * 8192 + row * 128 + (rem & 7) * 16) =
+          nk = (rv + 15) / 16;
+          const int nz = nk * 16 - rv;  // rows [rv, nk * 16) of A
+          uint8_t* a = sA + s * WG_A_STAGE;
+          for (int c = lane; c < 2 * nz * 8; c += 32) {
+            const int blk = c / (nz * 8);
+            const int rem = c - blk * nz * 8;
+            *reinterpret_cast<uint4*>(a + blk * 8192 + (rv + rem / 8) * 128 + (rem & 7) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
@@ -171,8 +176,7 @@ __global__ void __launch_bounds__(WG_THREADS, 1)
         if (lane == 0) {
           const uint32_t a_base = smem_u32(sA + s * WG_A_STAGE);
           const uint32_t b_base = smem_u32(sB + s * WG_B_STAGE);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
+          for (int kk = 0; kk < nk; ++kk) {
             const uint64_t adesc = smem_desc_sw128(a_base + kk * 2048, 8192, 1024);
             const uint64_t bdesc = smem_desc_sw128(b_base + kk * 2048, 8192, 1024);
             umma<0>(d_tmem, adesc, bdesc, IDESC, (k0 != r0 || kk != 0) ? 1u : 0u);
