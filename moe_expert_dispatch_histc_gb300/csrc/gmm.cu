@@ -594,10 +594,10 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
         for (int gi = 0; gi < NGROUPS; ++gi) {
           const int col0 = n * (!kIsFc2<MODE> ? BN / 2 : BN) + gi * GROUP_COLS;
           if (col0 >= p.out_cols) break;
-          // the previous store out of this warp's staging buffer has read it
-          if (lane == 0) bulk_wait_read_all();
-          __syncwarp();
           if constexpr (MODE == MODE_FC1_PRE) {
+            // the previous store out of this warp's staging buffer has read it
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
             // gate then up columns of G [R, 2I], bf16, as they leave the MMA
 #pragma unroll 1
             for (int part = 0; part < 2; ++part) {
@@ -654,6 +654,10 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
                 pk[i] = pack_bf16x2(silu_f(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]),
                                     silu_f(__uint_as_float(g[2 * i + 1])) *
                                         __uint_as_float(u[2 * i + 1]));
+              if (half == 0) {  // the previous store out of the staging buffer has read it
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+              }
 #pragma unroll
               for (int v = 0; v < 4; ++v) {
                 const int ch = half * 4 + v;
@@ -669,6 +673,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
             const float inv = pack_y16(a, b2, pk);
             if (lane < wrows)
               p.yscale[static_cast<int64_t>(grow0 + lane) * (p.out_cols / 64) + col0 / 64] = inv;
+            if (lane == 0) bulk_wait_read_all();  // the previous store has read the staging buffer
+            __syncwarp();
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               *reinterpret_cast<uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4)) =
@@ -688,6 +694,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
               tmem_ld32(tbase + gi * 32, v32);
               tmem_ld_wait();
             }
+            if (lane == 0) bulk_wait_read_all();  // the previous store has read the staging buffer
+            __syncwarp();
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               *reinterpret_cast<uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4)) =
@@ -1085,8 +1093,6 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
         for (int gi = 0; gi < NGROUPS; ++gi) {
           const int col0 = n * (!kIsFc2<MODE> ? BN / 2 : BN) + gi * GROUP_COLS;
           if (col0 >= p.out_cols) break;
-          if (lane == 0) bulk_wait_read_all();
-          __syncwarp();
           if (!kIsFc2<MODE> && ES == 2) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -1101,6 +1107,10 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
                 pk[i] = pack_bf16x2(silu_f(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]),
                                     silu_f(__uint_as_float(g[2 * i + 1])) *
                                         __uint_as_float(u[2 * i + 1]));
+              if (half == 0) {  // the previous store out of the staging buffer has read it
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+              }
 #pragma unroll
               for (int v = 0; v < 4; ++v) {
                 const int ch = half * 4 + v;
@@ -1116,6 +1126,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
             const float inv = pack_y16(a, b2, pk);
             if (lane < wrows)
               p.yscale[static_cast<int64_t>(grow0 + lane) * (p.out_cols / 64) + col0 / 64] = inv;
+            if (lane == 0) bulk_wait_read_all();  // the previous store has read the staging buffer
+            __syncwarp();
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               *reinterpret_cast<uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4)) =
@@ -1135,6 +1147,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
               tmem_ld32(tbase + gi * 32, v32);
               tmem_ld_wait();
             }
+            if (lane == 0) bulk_wait_read_all();  // the previous store has read the staging buffer
+            __syncwarp();
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               *reinterpret_cast<uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4)) =
