@@ -534,6 +534,403 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
   }
 }
 
+// ----------------------------------------------------------------------------
+// Wide int8 GEMM (the default single-CTA form): 128 x 256 tiles (fc1: 128
+// gate + 128 up columns), four 48 KB stages -- the bf16 block's 48 KB of
+// operands per 512 MMA cycles, where the 128 x 128 tiles above move 32 KB per
+// 256 cycles.  TMEM holds two 256-column accumulator slots, A and B: chunk 0
+// of K (k < 1024) accumulates in A, chunk 1 in B; with more chunks the
+// epilogue folds B into A as exact int32 (tcgen05.st; A then holds the running
+// int32 sum) and frees B for the next chunk.  The final sums are A + the last
+// chunk in B.  Both slots stay in use until the tile's epilogue ends, so the
+// epilogue does not overlap the next tile's MMAs.  The arithmetic after the
+// int32 sums is the 128 x 128 kernel's, so both give the same bits.
+// ----------------------------------------------------------------------------
+constexpr int QW_BN = 256;
+constexpr int QW_STAGES = 4;
+constexpr int QW_B_STAGE = 32768;          // 64 K rows x 256 columns x 2 B
+constexpr int QW_STAGE_BYTES = A_STAGE + QW_B_STAGE;
+constexpr size_t QW_SMEM_FIXED = 1024 + static_cast<size_t>(QW_STAGES) * QW_STAGE_BYTES +
+                                 4 * OUT_STAGE + 256;
+
+__device__ __forceinline__ int32_t f2i(uint32_t v) { return __float2int_rn(__uint_as_float(v)); }
+
+template <int MODE>
+__global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
+    gmm_qw_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmOut, const QParams p) {
+  constexpr int BK = 64;
+  constexpr int STAGES = QW_STAGES;
+  constexpr int B_STAGE = QW_B_STAGE;
+  constexpr int B_BLOCK = BK * 128;          // 64 K rows x 64 columns
+  constexpr int KK_B = 16 * 128;             // B bytes per UMMA K step
+  constexpr uint32_t IDESC = instr_desc(1, false, true, BM, QW_BN);
+  constexpr bool GATHER = MODE == MODE_FC1;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_STAGE;
+  uint8_t* sOut = sB + STAGES * B_STAGE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * OUT_STAGE);
+  uint64_t* empty = full + STAGES;
+  uint64_t* cdoneA = empty + STAGES;   // chunk 0 of a tile is in slot A
+  uint64_t* cdoneB = cdoneA + 1;       // a later chunk is in slot B
+  uint64_t* bfree = cdoneB + 1;        // slot B folded into A (epilogue -> MMA)
+  uint64_t* tfree = bfree + 1;         // both slots read (epilogue -> MMA)
+  uint64_t* mma_done = tfree + 1;
+  uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_sh = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
+  int32_t* prefix = reinterpret_cast<int32_t*>(tmem_base_sh + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+  const int nchunk = p.nchunk;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], GATHER ? 1 + 32 * QRoles<MODE>::kGatherWarps : 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(cdoneA, 1);
+    mbar_init(cdoneB, 1);
+    mbar_init(bfree, 4);   // lane 0 of each epilogue warp
+    mbar_init(tfree, 4);
+    mbar_init(mma_done, 1);
+    *abort_sh = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    if (!GATHER) tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (!p.raw) tma_prefetch_desc(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_base_sh, TMEM_COLS);
+    tmem_relinquish();
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+  if (warp == 2) {  // per-expert tile prefix: ceil(rows_e / BM) * n_tiles
+    int run = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      int t = 0;
+      if (e < E) {
+        const int rows = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+        t = ((rows + BM - 1) / BM) * p.n_tiles;
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += y;
+      }
+      if (e < E) prefix[e + 1] = run + t;
+      run += __shfl_sync(0xffffffffu, t, 31);
+    }
+    if (lane == 0) prefix[0] = 0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_base_sh;
+  const int total = prefix[E];
+  WaitCtl ctl{abort_sh, p.wait_limit_ns, p.dev_status};
+  const int kblocks = p.K / BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int s = 0;
+    uint32_t ph = 0;
+    int n_arm = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int e, n, row0, rows;
+      decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, ctl);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) {
+          const int k0 = kb * BK;
+          uint8_t* b_dst = sB + s * B_STAGE;
+          mbar_arrive_expect_tx(&full[s], GATHER ? B_STAGE : QW_STAGE_BYTES);
+          if (!GATHER) tma_load_2d(sA + s * A_STAGE, &tmA, &full[s], k0, row0);
+          // B in one blocked box: fc1 gate blocks 2n, 2n+1 then the same up
+          // blocks ([half][block][k row][128 B]); fc2 blocks 4n .. 4n+3
+          if (MODE == MODE_FC1) tma_load_5d(b_dst, &tmB, &full[s], 0, k0, 2 * n, 0, e);
+          else tma_load_4d(b_dst, &tmB, &full[s], 0, k0, 4 * n, e);
+        }
+        __syncwarp();
+        ++n_arm;
+        if (++s == STAGES) { s = 0; ph ^= 1; }
+      }
+    }
+    if (lane == 0) {  // every armed stage has landed before the CTA can exit (bounded)
+      volatile int never = 0;
+      WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
+      for (int st = 0; st < STAGES && st < n_arm; ++st) {
+        const int last = st + STAGES * ((n_arm - 1 - st) / STAGES);
+        mbar_wait(&full[st], (last / STAGES) & 1, drain);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int s = 0;
+    uint32_t ph = 0, tph = 0, bph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      if (lane == 0) ok = mbar_wait(tfree, tph ^ 1, ctl);  // the previous tile's slots are read
+      tph ^= 1;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      for (int kb = 0; kb < kblocks; ++kb) {
+        const int c = kb / QCHUNK_KB;
+        const bool first = (kb % QCHUNK_KB) == 0;
+        if (first && c >= 2) {  // slot B must have been folded into A first
+          if (lane == 0) ok = mbar_wait(bfree, bph, ctl);
+          bph ^= 1;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const uint32_t d = tmem_base + (c == 0 ? 0u : static_cast<uint32_t>(QW_BN));
+        if (lane == 0) {
+          ok = mbar_wait(&full[s], ph, ctl);
+          if (GATHER && ok) fence_proxy_async_smem();  // gathered rows -> async proxy
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a_base = smem_u32(sA + s * A_STAGE);
+          const uint32_t b_base = smem_u32(sB + s * B_STAGE);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bdesc = smem_desc_sw128(b_base + kk * KK_B, B_BLOCK, 1024);
+            umma<0>(d, adesc, bdesc, IDESC, (first && kk == 0) ? 0u : 1u);
+          }
+          umma_commit(&empty[s]);
+          if ((kb % QCHUNK_KB) == QCHUNK_KB - 1 || kb == kblocks - 1)
+            umma_commit(c == 0 ? cdoneA : cdoneB);  // the chunk is complete
+        }
+        __syncwarp();
+        if (++s == STAGES) { s = 0; ph ^= 1; }
+      }
+    }
+    if (lane == 0) {
+      umma_commit(mma_done);
+      volatile int never = 0;
+      WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
+      mbar_wait(mma_done, 0, drain);
+    }
+    __syncwarp();
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ fc1 row gather
+    const int t = threadIdx.x - 6 * 32;
+    const int chunk = t & 7, rsub = t >> 3;
+    const char* xg = static_cast<const char*>(p.a_ptr);
+    const int64_t row_bytes = static_cast<int64_t>(p.K) * 2;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int e, n, row0, rows;
+      decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
+      const int tok0 = __ldg(p.permute_src + row0) / p.k;  // tail rows repeat a valid row
+      const char* src[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = rsub + 16 * i;
+        const int tok = r < rows ? __ldg(p.permute_src + row0 + r) / p.k : tok0;
+        src[i] = xg + tok * row_bytes + chunk * 16;
+      }
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, ctl);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const uint32_t a_dst = smem_u32(sA + s * A_STAGE);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = rsub + 16 * i;
+          cp_async16(a_dst + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + kb * 128);
+        }
+        cp_async_mbar_arrive_noinc(&full[s]);
+        if (++s == STAGES) { s = 0; ph ^= 1; }
+      }
+    }
+    cp_async_wait<0>();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    uint8_t* stage = sOut + q * OUT_STAGE;
+    const uint32_t row_off = static_cast<uint32_t>(lane) * 128;
+    uint32_t pa = 0, pb = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, n, row0, rows;
+      decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(cdoneA, pa, ctl);
+      pa ^= 1;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tA = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      const uint32_t tB = tA + QW_BN;
+      const int wrows = min(32, rows - q * 32);
+      const int grow0 = row0 + q * 32;
+      const int grow = grow0 + lane;
+      const bool valid = lane < wrows;
+      bool a_int = false;  // slot A holds int32 sums (after a fold) instead of fp32
+      for (int c = 1; c < nchunk && ok; ++c) {
+        if (lane == 0) ok = mbar_wait(cdoneB, pb, ctl);
+        pb ^= 1;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+        if (c == nchunk - 1) break;  // the last chunk stays in B for the final sums
+        if (wrows > 0) {            // fold B into A, 32 columns at a time
+#pragma unroll 1
+          for (int g = 0; g < QW_BN / 32; ++g) {
+            uint32_t va[32], vb[32];
+            tmem_ld32(tA + g * 32, va);
+            tmem_ld32(tB + g * 32, vb);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              va[i] = static_cast<uint32_t>((a_int ? static_cast<int32_t>(va[i]) : f2i(va[i])) +
+                                            f2i(vb[i]));
+            tmem_st32(tA + g * 32, va);
+          }
+          tmem_st_wait();
+        }
+        a_int = true;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bfree);
+      }
+      if (!ok) break;
+      // exact int32 sums of 32 columns starting at TMEM column col
+      auto sums32 = [&](int col, int32_t (&out)[32]) {
+        uint32_t va[32];
+        tmem_ld32(tA + col, va);
+        if (nchunk > 1) {
+          uint32_t vb[32];
+          tmem_ld32(tB + col, vb);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            out[i] = (a_int ? static_cast<int32_t>(va[i]) : f2i(va[i])) + f2i(vb[i]);
+        } else {
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) out[i] = f2i(va[i]);
+        }
+      };
+      if (wrows > 0) {
+        float rs = 0.f;
+        if (valid && !p.raw)
+          rs = MODE == MODE_FC1 ? __ldg(p.a_scale + __ldg(p.permute_src + grow) / p.k)
+                                : __ldg(p.a_scale + grow);
+        const float* cs = p.b_scale + static_cast<int64_t>(e) *
+                                          (MODE == MODE_FC1 ? 2 * p.I : p.H);
+        // fc1: four groups of 32 gate columns (+ the matching up columns);
+        // fc2: four groups of 64 columns (s0: the first 32, s1: the next 32)
+        constexpr int GW = MODE == MODE_FC1 ? 32 : 64;
+#pragma unroll 1
+        for (int gi = 0; gi < 4; ++gi) {
+          const int col0 = n * (MODE == MODE_FC1 ? 128 : QW_BN) + gi * GW;
+          if (col0 >= (MODE == MODE_FC1 ? p.I : p.H)) break;
+          int32_t s0[32], s1[32];
+          if (MODE == MODE_FC1) {
+            sums32(gi * 32, s0);        // gate
+            sums32(128 + gi * 32, s1);  // up
+          } else {
+            sums32(gi * 64, s0);
+            sums32(gi * 64 + 32, s1);
+          }
+          if (p.raw) {  // test mode: the int32 accumulators themselves
+            if (valid) {
+              int32_t* o = static_cast<int32_t*>(p.out);
+              int4* d0;
+              int4* d1;
+              if (MODE == MODE_FC1) {
+                d0 = reinterpret_cast<int4*>(o + static_cast<int64_t>(grow) * 2 * p.I + col0);
+                d1 = reinterpret_cast<int4*>(o + static_cast<int64_t>(grow) * 2 * p.I + p.I + col0);
+              } else {
+                d0 = reinterpret_cast<int4*>(o + static_cast<int64_t>(grow) * p.H + col0);
+                d1 = reinterpret_cast<int4*>(o + static_cast<int64_t>(grow) * p.H + col0 + 32);
+              }
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                d0[v] = make_int4(s0[4 * v], s0[4 * v + 1], s0[4 * v + 2], s0[4 * v + 3]);
+                d1[v] = make_int4(s1[4 * v], s1[4 * v + 1], s1[4 * v + 2], s1[4 * v + 3]);
+              }
+            }
+            continue;
+          }
+          // dequant: (row scale * column scale) * acc, in fp32
+          uint32_t pk[32];
+          if (MODE == MODE_FC1) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float g = (rs * __ldg(cs + col0 + i)) * static_cast<float>(s0[i]);
+              const float u = (rs * __ldg(cs + p.I + col0 + i)) * static_cast<float>(s1[i]);
+              pk[i] = __float_as_uint(silu_f(g) * u);
+            }
+          } else {  // y as fp16 with a power-of-two scale per 64 columns
+            uint32_t y0[32], y1[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              y0[i] = __float_as_uint((rs * __ldg(cs + col0 + i)) * static_cast<float>(s0[i]));
+              y1[i] = __float_as_uint((rs * __ldg(cs + col0 + 32 + i)) * static_cast<float>(s1[i]));
+            }
+            const float inv = pack_y16(y0, y1, pk);
+            if (valid) p.yscale[static_cast<int64_t>(grow) * (p.H / 64) + col0 / 64] = inv;
+          }
+          const int out_cols = MODE == MODE_FC1 ? p.I : p.H;
+          constexpr int ESZ = MODE == MODE_FC1 ? 4 : 2;   // h fp32, y fp16
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4)) =
+                make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          if (wrows == 32) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmOut, stage, col0, grow0);
+              bulk_commit();
+            }
+          } else if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(p.out) +
+                                                  (static_cast<int64_t>(grow) * out_cols + col0) * ESZ);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = *reinterpret_cast<const uint4*>(stage + row_off + ((v ^ (lane & 7)) << 4));
+          }
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tfree);  // both slots read (after tcgen05.wait::ld)
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
 // int8 -> bf16 (exact), 16 values per thread step, over one or two tensors
 // (one launch: segment 0 then segment 1 in one grid-stride range)
 __global__ void i8_to_bf16_kernel(const int8_t* __restrict__ src0, __nv_bfloat16* __restrict__ dst0,
@@ -701,22 +1098,77 @@ static cudaError_t launch_q(const QArgs& g, cudaStream_t st) {
                        st, 1, tA, tB, tOut, p);
 }
 
-// Single CTAs unless mc2_set_tile_pairing forces pairs (both give the same
-// bits: every output accumulates its chunks in the same K order).  Measured
-// on GB300 with the 8192-token int8 workload (about 512 rows per expert):
-// pairs 1.736 ms per block against 1.509 ms (fc1 1.190 vs 0.999 ms, fc2 +
-// combine 0.530 vs 0.495 ms): 256-row tiles pad more rows, and fc1's odd CTA
-// still relays its gathered stages.
-static bool use_pairs_q(const mc2_shape_t&) {
-  return tile_pairing_override() == 2 && num_sms() >= 2;
+template <int MODE>
+static cudaError_t launch_qw(const QArgs& g, cudaStream_t st) {
+  const mc2_shape_t& s = *g.s;
+  const int64_t R = static_cast<int64_t>(s.T) * s.k;
+  CUtensorMap tA, tB, tOut;
+  QParams p;
+  p.a_ptr = g.a;
+  p.offsets = g.offsets;
+  p.permute_src = g.permute_src;
+  p.a_scale = g.a_scale;
+  p.b_scale = g.b_scale;
+  p.out = g.out;
+  p.yscale = g.yscale;
+  p.dev_status = g.dev_status;
+  p.E = s.E;
+  p.k = s.k;
+  p.I = s.I;
+  p.H = s.H;
+  p.raw = g.raw ? 1 : 0;
+  p.wait_limit_ns = wait_limit_ns();
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  bool ok;
+  if (MODE == MODE_FC1) {
+    p.K = s.H;
+    p.n_tiles = (s.I + 127) / 128;  // I is a multiple of 64: the last tile may be half full
+    ok = encode_b_blocked(&tB, g.b, s.H, 2ull * s.I, s.E, 2, 64, 2, 2);
+    tA = tB;  // unused: fc1's A rows are gathered with cp.async
+    tOut = tB;
+    if (!g.raw) ok = ok && encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, g.out, s.I, R, 32, 32);
+  } else {
+    p.K = s.I;
+    p.n_tiles = (s.H + QW_BN - 1) / QW_BN;
+    ok = encode_2d(&tA, bf, 2, g.a, s.I, R, 64, BM) &&
+         encode_b_blocked(&tB, g.b, s.I, s.H, s.E, 1, 64, 4, 1);
+    tOut = tB;
+    if (!g.raw) ok = ok && encode_2d(&tOut, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.out, s.H, R, 64, 32);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  p.nchunk = (p.K / 64 + QCHUNK_KB - 1) / QCHUNK_KB;
+  if (p.nchunk > QMAX_CHUNKS) return cudaErrorInvalidValue;
+  const size_t smem = QW_SMEM_FIXED + (s.E + 1) * sizeof(int32_t);
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(gmm_qw_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(QW_SMEM_FIXED + 1025 * sizeof(int32_t)));
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int64_t tiles_upper = (R / BM + s.E) * static_cast<int64_t>(p.n_tiles);
+  const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_upper, 1)));
+  return launch_kernel(gmm_qw_kernel<MODE>, dim3(grid), dim3(QRoles<MODE>::kThreads), smem, st, 1,
+                       tA, tB, tOut, p);
 }
 
+// Tiling of the int8 GEMMs (every form gives the same bits: each output
+// accumulates its chunks in the same K order and is dequantised alike):
+// by default the wide single-CTA kernel (128 x 256 tiles); mc2_set_tile_pairing
+// 1 selects the 128 x 128 single-CTA kernel, 2 the 256 x 128 CTA pairs.
+// Measured on GB300 with the 8192-token int8 workload (about 512 rows per
+// expert), 128 x 128 against pairs: block 1.509 vs 1.736 ms (256-row tiles
+// pad more rows, and fc1's odd CTA relays its gathered stages).
 cudaError_t launch_gemm_q(const QArgs& g, cudaStream_t st) {
   if (static_cast<int64_t>(g.s->T) * g.s->k == 0) return cudaSuccess;
-  const bool pairs = use_pairs_q(*g.s);
-  const cudaError_t e =
-      g.mode == MODE_FC1 ? (pairs ? launch_q<MODE_FC1, true>(g, st) : launch_q<MODE_FC1, false>(g, st))
-                         : (pairs ? launch_q<MODE_FC2, true>(g, st) : launch_q<MODE_FC2, false>(g, st));
+  const int forced = tile_pairing_override();
+  cudaError_t e;
+  if (forced == 2 && num_sms() >= 2)
+    e = g.mode == MODE_FC1 ? launch_q<MODE_FC1, true>(g, st) : launch_q<MODE_FC2, true>(g, st);
+  else if (forced == 1)
+    e = g.mode == MODE_FC1 ? launch_q<MODE_FC1, false>(g, st) : launch_q<MODE_FC2, false>(g, st);
+  else
+    e = g.mode == MODE_FC1 ? launch_qw<MODE_FC1>(g, st) : launch_qw<MODE_FC2>(g, st);
   note_launches(1);
   return e;
 }

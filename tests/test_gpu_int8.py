@@ -32,9 +32,10 @@ def _run(wl, inp, out):
     return d, b
 
 
-@pytest.fixture(params=[1, 2], ids=["single_cta", "cta_pairs"])
+@pytest.fixture(params=[0, 1, 2], ids=["wide", "single_cta", "cta_pairs"])
 def pairing(request):
-    """Force one int8 GEMM tiling (single CTAs or CTA pairs) for the test."""
+    """Force one int8 GEMM tiling for the test: the default 128 x 256 tiles
+    (K chunks folded in TMEM), 128 x 128 tiles, or 256 x 128 CTA pairs."""
     ensure_built()
     B.mc2_set_tile_pairing(request.param)
     yield request.param
@@ -45,6 +46,8 @@ SMALL_I8 = [
     Workload("i8_small", 256, 256, 128, 8, 2, 2, "i8"),
     Workload("i8_chunk_edge", 128, 2112, 192, 4, 2, 2, "i8"),    # K = 33 k-blocks: chunks 16+16+1
     Workload("i8_k3072", 64, 3072, 1536, 4, 2, 2, "i8"),         # three full chunks, two in fc2
+    Workload("i8_k4096", 96, 4096, 320, 4, 2, 2, "i8"),          # four chunks (two folds); I % 128 = 64
+    Workload("i8_fc2_k3072", 64, 320, 3072, 4, 2, 2, "i8"),      # fc2 K = 3072; H % 256 = 64
 ]
 
 
@@ -59,9 +62,12 @@ def test_int8_fc1_accumulators_exact(wl, pairing):
     assert int(b.dev_status.item()) == 0
 
 
-def test_int8_worst_case_magnitudes_exact(pairing):
-    """All values +-127 at K = 3072: |acc| = 49.5M > 2^24, exact only by chunking."""
-    wl = Workload("i8_worst", 64, 3072, 128, 2, 1, 1, "i8")
+@pytest.mark.parametrize("K", [3072, 4096])
+def test_int8_worst_case_magnitudes_exact(pairing, K):
+    """All values +-127: |acc| = K * 127^2 (49.5M at K = 3072, 66.1M at
+    K = 4096) > 2^24, exact only by chunking (and, for the wide tiles, by
+    folding the chunks into int32 in TMEM)."""
+    wl = Workload("i8_worst", 64, K, 128, 2, 1, 1, "i8")
     inp = make_inputs(wl, 0)
     inp["x"] = np.full_like(inp["x"], 127)
     inp["x"][1::2] = -127
@@ -70,7 +76,7 @@ def test_int8_worst_case_magnitudes_exact(pairing):
     d, b = _run(wl, inp, out="i32")
     ref = orc.quant_block_forward(inp["x"], inp["xs"], inp["w1"], inp["w1s"], inp["w2"],
                                   inp["w2s"], inp["sel"], inp["probs"], wl.E, wl.W)
-    assert np.abs(ref["acc1"]).max() == 3072 * 127 * 127
+    assert np.abs(ref["acc1"]).max() == K * 127 * 127
     assert np.array_equal(to_np(b.h).astype(np.int64), ref["acc1"])
 
 
@@ -160,14 +166,17 @@ def test_int8_full_size_accumulators_full(pairing):
     assert int(b.dev_status.item()) == 0
 
 
-def test_int8_pairs_equal_single_bitwise():
-    """Both int8 GEMM tilings accumulate every output's K chunks in the same
-    order: h_q, its scales and the block output are identical bit for bit
-    (a workload with several tiles per CTA and per CTA pair)."""
-    wl = Workload("i8_mid", 2048, 1024, 512, 16, 4, 4, "i8")
+@pytest.mark.parametrize("wl", [Workload("i8_mid", 2048, 1024, 512, 16, 4, 4, "i8"),
+                                Workload("i8_mid3", 1024, 3072, 1536, 16, 4, 4, "i8")],
+                         ids=lambda w: w.name)
+def test_int8_tilings_equal_bitwise(wl):
+    """Every int8 GEMM tiling accumulates each output's K chunks exactly and
+    dequantises alike: h_q, its scales and the block output are identical
+    bit for bit (workloads with several tiles per CTA and per CTA pair; the
+    second folds a chunk in fc1)."""
     inp = make_inputs(wl, 4)
     res = []
-    for mode in (1, 2):
+    for mode in (0, 1, 2):
         B.mc2_set_tile_pairing(mode)
         try:
             d, b = _run(wl, inp, out="bf16")
@@ -175,5 +184,6 @@ def test_int8_pairs_equal_single_bitwise():
             assert int(b.dev_status.item()) == 0
         finally:
             B.mc2_set_tile_pairing(0)
-    for a, c in zip(res[0], res[1]):
-        assert np.array_equal(a.view(np.uint8), c.view(np.uint8))
+    for other in res[1:]:
+        for a, c in zip(res[0], other):
+            assert np.array_equal(a.view(np.uint8), c.view(np.uint8))
