@@ -538,13 +538,14 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
 // Wide int8 GEMM (the default single-CTA form): 128 x 256 tiles (fc1: 128
 // gate + 128 up columns), four 48 KB stages -- the bf16 block's 48 KB of
 // operands per 512 MMA cycles, where the 128 x 128 tiles above move 32 KB per
-// 256 cycles.  TMEM holds two 256-column accumulator slots, A and B: chunk 0
-// of K (k < 1024) accumulates in A, chunk 1 in B; with more chunks the
-// epilogue folds B into A as exact int32 (tcgen05.st; A then holds the running
-// int32 sum) and frees B for the next chunk.  The final sums are A + the last
-// chunk in B.  Both slots stay in use until the tile's epilogue ends, so the
-// epilogue does not overlap the next tile's MMAs.  The arithmetic after the
-// int32 sums is the 128 x 128 kernel's, so both give the same bits.
+// 256 cycles.  TMEM holds two 256-column accumulator slots.  Tile t of a CTA
+// has a first slot F = t mod 2 and a second slot S: chunk 0 of K (k < 1024)
+// accumulates in F, every later chunk in S, and the epilogue folds each of
+// them into F as exact int32 (tcgen05.st; F then holds the running int32
+// sum), releasing S at once.  The next tile's chunk 0 therefore accumulates in
+// S while the epilogue dequantises and stores the current tile from F.  The
+// arithmetic after the int32 sums is the 128 x 128 kernel's, so both give the
+// same bits.
 // ----------------------------------------------------------------------------
 constexpr int QW_BN = 256;
 constexpr int QW_STAGES = 4;
@@ -575,11 +576,9 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
   uint8_t* sOut = sB + STAGES * B_STAGE;
   uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 4 * OUT_STAGE);
   uint64_t* empty = full + STAGES;
-  uint64_t* cdoneA = empty + STAGES;   // chunk 0 of a tile is in slot A
-  uint64_t* cdoneB = cdoneA + 1;       // a later chunk is in slot B
-  uint64_t* bfree = cdoneB + 1;        // slot B folded into A (epilogue -> MMA)
-  uint64_t* tfree = bfree + 1;         // both slots read (epilogue -> MMA)
-  uint64_t* mma_done = tfree + 1;
+  uint64_t* done = empty + STAGES;     // [2]: a chunk is complete in the slot (MMA -> epilogue)
+  uint64_t* sfree = done + 2;          // [2]: the slot has been read (epilogue -> MMA)
+  uint64_t* mma_done = sfree + 2;
   uint32_t* tmem_base_sh = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_sh = reinterpret_cast<volatile int*>(tmem_base_sh + 1);
   int32_t* prefix = reinterpret_cast<int32_t*>(tmem_base_sh + 2);
@@ -593,10 +592,10 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
       mbar_init(&full[s], GATHER ? 1 + 32 * QRoles<MODE>::kGatherWarps : 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(cdoneA, 1);
-    mbar_init(cdoneB, 1);
-    mbar_init(bfree, 4);   // lane 0 of each epilogue warp
-    mbar_init(tfree, 4);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&done[j], 1);
+      mbar_init(&sfree[j], 4);  // lane 0 of each epilogue warp
+    }
     mbar_init(mma_done, 1);
     *abort_sh = 0;
     fence_barrier_init();
@@ -678,26 +677,29 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Each chunk starts a fresh accumulation in its slot once the epilogue
+    // has released the slot's previous contents (the first use of each slot
+    // passes at once: parity of the phase before the first).
     int s = 0;
-    uint32_t ph = 0, tph = 0, bph = 0;
+    uint32_t ph = 0;
+    uint32_t nwait = 0;  // bit j: parity of the waits on slot j so far
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      if (lane == 0) ok = mbar_wait(tfree, tph ^ 1, ctl);  // the previous tile's slots are read
-      tph ^= 1;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      tc_fence_after();
+    int lt = 0;  // tiles of this CTA so far
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++lt) {
+      const int F = lt & 1;
+      uint32_t d = 0;
       for (int kb = 0; kb < kblocks; ++kb) {
         const int c = kb / QCHUNK_KB;
         const bool first = (kb % QCHUNK_KB) == 0;
-        if (first && c >= 2) {  // slot B must have been folded into A first
-          if (lane == 0) ok = mbar_wait(bfree, bph, ctl);
-          bph ^= 1;
+        const int slot = c == 0 ? F : F ^ 1;
+        if (first) {
+          if (lane == 0) ok = mbar_wait(&sfree[slot], ((nwait >> slot) & 1u) ^ 1u, ctl);
+          nwait ^= 1u << slot;
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
           tc_fence_after();
+          d = tmem_base + static_cast<uint32_t>(slot * QW_BN);
         }
-        const uint32_t d = tmem_base + (c == 0 ? 0u : static_cast<uint32_t>(QW_BN));
         if (lane == 0) {
           ok = mbar_wait(&full[s], ph, ctl);
           if (GATHER && ok) fence_proxy_async_smem();  // gathered rows -> async proxy
@@ -716,7 +718,7 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
           }
           umma_commit(&empty[s]);
           if ((kb % QCHUNK_KB) == QCHUNK_KB - 1 || kb == kblocks - 1)
-            umma_commit(c == 0 ? cdoneA : cdoneB);  // the chunk is complete
+            umma_commit(&done[slot]);  // the chunk is complete
         }
         __syncwarp();
         if (++s == STAGES) { s = 0; ph ^= 1; }
@@ -769,67 +771,61 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
     const int q = warp & 3;
     uint8_t* stage = sOut + q * OUT_STAGE;
     const uint32_t row_off = static_cast<uint32_t>(lane) * 128;
-    uint32_t pa = 0, pb = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    uint32_t pd = 0;  // bit j: parity of the next completion of done[j]
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++lt) {
       int e, n, row0, rows;
       decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
+      const int F = lt & 1, S = F ^ 1;
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(cdoneA, pa, ctl);
-      pa ^= 1;
+      if (lane == 0) ok = mbar_wait(&done[F], (pd >> F) & 1u, ctl);
+      pd ^= 1u << F;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tA = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      const uint32_t tB = tA + QW_BN;
+      const uint32_t tF = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                          static_cast<uint32_t>(F * QW_BN);
+      const uint32_t tS = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                          static_cast<uint32_t>(S * QW_BN);
       const int wrows = min(32, rows - q * 32);
       const int grow0 = row0 + q * 32;
       const int grow = grow0 + lane;
       const bool valid = lane < wrows;
-      bool a_int = false;  // slot A holds int32 sums (after a fold) instead of fp32
-      for (int c = 1; c < nchunk && ok; ++c) {
-        if (lane == 0) ok = mbar_wait(cdoneB, pb, ctl);
-        pb ^= 1;
+      bool f_int = false;  // slot F holds int32 sums (after a fold) instead of fp32
+      for (int c = 1; c < nchunk; ++c) {  // fold each later chunk into F, then release S
+        if (lane == 0) ok = mbar_wait(&done[S], (pd >> S) & 1u, ctl);
+        pd ^= 1u << S;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
-        if (c == nchunk - 1) break;  // the last chunk stays in B for the final sums
-        if (wrows > 0) {            // fold B into A, 32 columns at a time
+        if (wrows > 0) {
 #pragma unroll 1
           for (int g = 0; g < QW_BN / 32; ++g) {
             uint32_t va[32], vb[32];
-            tmem_ld32(tA + g * 32, va);
-            tmem_ld32(tB + g * 32, vb);
+            tmem_ld32(tF + g * 32, va);
+            tmem_ld32(tS + g * 32, vb);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              va[i] = static_cast<uint32_t>((a_int ? static_cast<int32_t>(va[i]) : f2i(va[i])) +
+              va[i] = static_cast<uint32_t>((f_int ? static_cast<int32_t>(va[i]) : f2i(va[i])) +
                                             f2i(vb[i]));
-            tmem_st32(tA + g * 32, va);
+            tmem_st32(tF + g * 32, va);
           }
           tmem_st_wait();
         }
-        a_int = true;
+        f_int = true;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bfree);
+        if (lane == 0) mbar_arrive(&sfree[S]);
       }
       if (!ok) break;
-      // exact int32 sums of 32 columns starting at TMEM column col
+      // exact int32 sums of 32 columns starting at TMEM column col of slot F
       auto sums32 = [&](int col, int32_t (&out)[32]) {
         uint32_t va[32];
-        tmem_ld32(tA + col, va);
-        if (nchunk > 1) {
-          uint32_t vb[32];
-          tmem_ld32(tB + col, vb);
-          tmem_ld_wait();
+        tmem_ld32(tF + col, va);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            out[i] = (a_int ? static_cast<int32_t>(va[i]) : f2i(va[i])) + f2i(vb[i]);
-        } else {
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) out[i] = f2i(va[i]);
-        }
+        for (int i = 0; i < 32; ++i) out[i] = f_int ? static_cast<int32_t>(va[i]) : f2i(va[i]);
       };
       if (wrows > 0) {
         float rs = 0.f;
@@ -875,19 +871,31 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
           }
           // dequant: (row scale * column scale) * acc, in fp32
           uint32_t pk[32];
+          // column scales as float4 loads (16-byte aligned: the scale rows
+          // start at multiples of 64 columns and col0 is a multiple of 32)
+          const float4* c0 = reinterpret_cast<const float4*>(cs + col0);
+          const float4* c1 = reinterpret_cast<const float4*>(
+              cs + (MODE == MODE_FC1 ? p.I + col0 : col0 + 32));
+          float w0[32], w1[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 a4 = __ldg(c0 + i), b4 = __ldg(c1 + i);
+            w0[4 * i] = a4.x; w0[4 * i + 1] = a4.y; w0[4 * i + 2] = a4.z; w0[4 * i + 3] = a4.w;
+            w1[4 * i] = b4.x; w1[4 * i + 1] = b4.y; w1[4 * i + 2] = b4.z; w1[4 * i + 3] = b4.w;
+          }
           if (MODE == MODE_FC1) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float g = (rs * __ldg(cs + col0 + i)) * static_cast<float>(s0[i]);
-              const float u = (rs * __ldg(cs + p.I + col0 + i)) * static_cast<float>(s1[i]);
+              const float g = (rs * w0[i]) * static_cast<float>(s0[i]);
+              const float u = (rs * w1[i]) * static_cast<float>(s1[i]);
               pk[i] = __float_as_uint(silu_f(g) * u);
             }
           } else {  // y as fp16 with a power-of-two scale per 64 columns
             uint32_t y0[32], y1[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              y0[i] = __float_as_uint((rs * __ldg(cs + col0 + i)) * static_cast<float>(s0[i]));
-              y1[i] = __float_as_uint((rs * __ldg(cs + col0 + 32 + i)) * static_cast<float>(s1[i]));
+              y0[i] = __float_as_uint((rs * w0[i]) * static_cast<float>(s0[i]));
+              y1[i] = __float_as_uint((rs * w1[i]) * static_cast<float>(s1[i]));
             }
             const float inv = pack_y16(y0, y1, pk);
             if (valid) p.yscale[static_cast<int64_t>(grow) * (p.H / 64) + col0 / 64] = inv;
@@ -919,7 +927,7 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tfree);  // both slots read (after tcgen05.wait::ld)
+      if (lane == 0) mbar_arrive(&sfree[F]);  // slot F read (after tcgen05.wait::ld)
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
