@@ -359,6 +359,23 @@ def test_invalid_ids_are_flagged_and_skipped(pairing):
     _check_custom(wl, _custom(wl, sel, seed=6), expect_bad=True)
 
 
+def test_zero_routing_weights(pairing):
+    """Slots with probability 0 (and a token whose every weight is 0) add
+    nothing: out matches the oracle, and the all-zero token's row is 0."""
+    wl = Workload("zero_probs", 512, 256, 128, 8, 4, 2, "bf16")
+    inp = make_inputs(wl, 9)
+    probs = inp["probs"].copy()
+    probs[::3, 1] = 0.0
+    probs[7, :] = 0.0
+    inp["probs"] = np.ascontiguousarray(probs)
+    inp, d, b = run_gpu(wl, inputs=inp)
+    x, w1, w2 = (as_f64(inp[n], wl.act) for n in ("x", "w1", "w2"))
+    ref = orc.block_forward(x, w1, w2, inp["sel"], inp["probs"], wl.E, wl.W, h_dtype="bf16")
+    _tol(to_np(b.out), ref["out"], "out with zero weights")
+    assert float(b.out[7].float().abs().max()) == 0.0
+    assert int(b.dev_status.item()) == 0
+
+
 def test_empty_input():
     wl = Workload("empty", 0, 256, 128, 8, 2, 2, "bf16")
     inp, d, b = run_gpu(wl)
