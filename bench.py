@@ -178,10 +178,12 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": _config(wl, l2="n/a (CPU)"),
+        "config": _headline_config(wl),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
                          "kind": "oracle",
-                         "sample": f"{Ts} tokens of the {wl.name} workload per step"},
+                         "sample": f"{Ts} tokens of the {wl.name} workload per step (numpy "
+                                   f"oracle, float64 / int64, all experts; host memory, no L2 "
+                                   f"flush)"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -203,6 +205,14 @@ def job_tokens_per_s(tokens_per_rank: int, world: int, steps: int, max_ms: float
     """Whole-job throughput of weak-scaled replicas: every rank's tokens over
     the slowest rank's time."""
     return tokens_per_rank * world * steps / (max_ms / 1e3)
+
+
+def _headline_config(wl):
+    """The config of a workload's line as the cuda arm prints it (the reference
+    arm reports the same workload under the same config)."""
+    c = _config(wl, l2="flushed (256 MB write) between steps")
+    c["role"] = "headline" if wl.name == HEADLINE else "context (the headline line is last)"
+    return c
 
 
 def _config(wl, l2):
@@ -477,6 +487,7 @@ def run_cuda_workload(args, wl, headline):
         line["config"]["note"] = ("correctness only: 64 tokens, a few-microsecond block; its "
                                   "roofline fraction says nothing about the kernels")
     line["config"]["role"] = "headline" if headline else "context (the headline line is last)"
+    assert headline == (wl.name == HEADLINE)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp, budget_s=12.0 if headline else 6.0)
     print(json.dumps(line), flush=True)
