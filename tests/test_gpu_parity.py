@@ -117,6 +117,7 @@ SMALL = [
     Workload("many_experts", 256, 512, 256, 64, 8, 4, "bf16"),      # ~32 rows/expert
     Workload("k1", 200, 128, 64, 4, 1, 2, "bf16"),
     Workload("fp32_ragged", 96, 192, 64, 4, 2, 2, "f32"),
+    Workload("e1024", 2048, 128, 64, 1024, 2, 8, "bf16"),         # the largest E: 1025-entry prefix
 ]
 
 
