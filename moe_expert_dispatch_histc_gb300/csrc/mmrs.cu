@@ -157,8 +157,9 @@ struct FParams {
 // share the x1 row blocks and x2 column blocks they stream (for every rank)
 // and consecutive waves reuse row blocks from L2.  Measured on GB300 at W8
 // m4096 k1024 n4096 (16 row blocks): groups of 2 / 4 / 8 / 16 row blocks
-// 0.255 / 0.252 / 0.248 / 0.246 ms per call; plain row-major order 0.255.
-constexpr int MMRS_GROUP_M = 16;
+// 0.255 / 0.252 / 0.248 / 0.246 ms per call, plain row-major order 0.255;
+// the kernel's DRAM reads 280 MB with 8 against 328 MB with 16.
+constexpr int MMRS_GROUP_M = 8;
 
 __device__ __forceinline__ void mmrs_tile(int tile, int m_tiles, int n_tiles, int& mt, int& nt) {
   const int per_group = MMRS_GROUP_M * n_tiles;
