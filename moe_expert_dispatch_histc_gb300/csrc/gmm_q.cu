@@ -798,18 +798,23 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         tc_fence_after();
-        if (wrows > 0) {
+        if (wrows > 0) {  // 64 columns per round trip: four loads behind one wait
 #pragma unroll 1
-          for (int g = 0; g < QW_BN / 32; ++g) {
-            uint32_t va[32], vb[32];
-            tmem_ld32(tF + g * 32, va);
-            tmem_ld32(tS + g * 32, vb);
+          for (int g = 0; g < QW_BN / 64; ++g) {
+            uint32_t va[2][32], vb[2][32];
+            tmem_ld32(tF + g * 64, va[0]);
+            tmem_ld32(tF + g * 64 + 32, va[1]);
+            tmem_ld32(tS + g * 64, vb[0]);
+            tmem_ld32(tS + g * 64 + 32, vb[1]);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              va[i] = static_cast<uint32_t>((f_int ? static_cast<int32_t>(va[i]) : f2i(va[i])) +
-                                            f2i(vb[i]));
-            tmem_st32(tF + g * 32, va);
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                va[h][i] = static_cast<uint32_t>(
+                    (f_int ? static_cast<int32_t>(va[h][i]) : f2i(va[h][i])) + f2i(vb[h][i]));
+            tmem_st32(tF + g * 64, va[0]);
+            tmem_st32(tF + g * 64 + 32, va[1]);
           }
           tmem_st_wait();
         }
@@ -819,13 +824,18 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
         if (lane == 0) mbar_arrive(&sfree[S]);
       }
       if (!ok) break;
-      // exact int32 sums of 32 columns starting at TMEM column col of slot F
-      auto sums32 = [&](int col, int32_t (&out)[32]) {
-        uint32_t va[32];
-        tmem_ld32(tF + col, va);
+      // exact int32 sums of the 32 columns at TMEM columns c0 and c1 of slot F
+      // (two loads behind one wait)
+      auto sums2x32 = [&](int c0, int c1, int32_t (&o0)[32], int32_t (&o1)[32]) {
+        uint32_t va[32], vb[32];
+        tmem_ld32(tF + c0, va);
+        tmem_ld32(tF + c1, vb);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) out[i] = f_int ? static_cast<int32_t>(va[i]) : f2i(va[i]);
+        for (int i = 0; i < 32; ++i) {
+          o0[i] = f_int ? static_cast<int32_t>(va[i]) : f2i(va[i]);
+          o1[i] = f_int ? static_cast<int32_t>(vb[i]) : f2i(vb[i]);
+        }
       };
       if (wrows > 0) {
         float rs = 0.f;
@@ -842,13 +852,8 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
           const int col0 = n * (MODE == MODE_FC1 ? 128 : QW_BN) + gi * GW;
           if (col0 >= (MODE == MODE_FC1 ? p.I : p.H)) break;
           int32_t s0[32], s1[32];
-          if (MODE == MODE_FC1) {
-            sums32(gi * 32, s0);        // gate
-            sums32(128 + gi * 32, s1);  // up
-          } else {
-            sums32(gi * 64, s0);
-            sums32(gi * 64 + 32, s1);
-          }
+          if (MODE == MODE_FC1) sums2x32(gi * 32, 128 + gi * 32, s0, s1);  // gate, up
+          else sums2x32(gi * 64, gi * 64 + 32, s0, s1);
           if (p.raw) {  // test mode: the int32 accumulators themselves
             if (valid) {
               int32_t* o = static_cast<int32_t*>(p.out);
