@@ -83,6 +83,21 @@ def test_backward_parity(wl):
         _tol(got[name], ref[name], name)
 
 
+@pytest.mark.parametrize("mode", [1, 2], ids=["single_cta", "cta_pairs"])
+@pytest.mark.parametrize("wl", [BWD[1], BWD[3]], ids=lambda w: w.name)
+def test_backward_parity_under_each_tiling(wl, mode):
+    """The two dgrad GEMMs on single-CTA tiles and on CTA pairs, forced: both
+    within the tolerance."""
+    B.mc2_set_tile_pairing(mode)
+    try:
+        got, ref, status = run_backward(wl, seed=2)
+    finally:
+        B.mc2_set_tile_pairing(0)
+    assert status == 0
+    for name in ("dx", "dw1", "dw2", "dprobs"):
+        _tol(got[name], ref[name], name)
+
+
 def test_backward_invalid_ids_and_empty_experts():
     """Invalid slots get dprobs 0 and no gradient; experts without rows get zero
     weight gradients."""
