@@ -294,7 +294,7 @@ def run_cuda(args):
     from moe_expert_dispatch_histc_gb300.build import build
     build()
     B.lib()
-    B.mc2_set_tile_pairing({"auto": 0, "single": 1, "pairs": 2, "mcast": 3}[args.tiling])
+    B.mc2_set_tile_pairing({"auto": 0, "single": 1, "pairs": 2}[args.tiling])
     names = [args.workload] if args.workload else [*CONTEXT, HEADLINE]
     if args.path == "unfused":   # the non-fused baseline exists for bf16 workloads only
         names = [n for n in names if WORKLOADS[n].act == "bf16"]
@@ -745,9 +745,8 @@ def main():
                     help="unfused: the non-fused baseline (materialised permute, plain grouped "
                          "fc1), bf16 workloads only; twopass (--op mm_reduce_scatter): int32 "
                          "partials through memory, then a reduce kernel")
-    ap.add_argument("--tiling", default="auto", choices=["auto", "single", "pairs", "mcast"],
-                    help="grouped-GEMM tiling of the block (mc2_set_tile_pairing; mcast: fc1 "
-                         "on 2-CTA clusters sharing the weight tile by multicast): all give "
+    ap.add_argument("--tiling", default="auto", choices=["auto", "single", "pairs"],
+                    help="grouped-GEMM tiling of the block (mc2_set_tile_pairing): all give "
                          "the same bits")
     ap.add_argument("--recompute-g", action="store_true",
                     help="--op backward: recompute G instead of taking the training forward's")

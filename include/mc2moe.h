@@ -323,11 +323,10 @@ void mc2_set_wait_limit_ns(uint64_t limit_ns);
 
 /* Grouped-GEMM tiling for later calls of this thread: 0 = automatic
  * (bf16/tf32 fc2 on CTA pairs with 256x256 tiles when experts average >= 256
- * rows; everything else on one CTA per 128x256 tile, int8 GEMMs 128x128),
- * 1 = always single CTAs, 2 = always CTA pairs (int8 GEMMs: 256x128 tiles),
- * 3 = bf16 fc1 on 2-CTA clusters that run two 128-row tiles of the same
- * expert and weight columns and share the weight tile by multicast (fc2 as
- * in 0).  The choice does not change any result bit: every tiling
+ * rows; everything else on one CTA per 128x256 tile, the int8 GEMMs with
+ * their K chunks folded in TMEM), 1 = always single CTAs (int8 GEMMs:
+ * 128x128 tiles), 2 = always CTA pairs (int8 GEMMs: 256x128 tiles); other
+ * values mean 0.  The choice does not change any result bit: every tiling
  * accumulates each output in the same K order.  Host only. */
 void mc2_set_tile_pairing(int32_t mode);
 

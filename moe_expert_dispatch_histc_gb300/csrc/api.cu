@@ -403,7 +403,7 @@ mc2_status_t mc2_selftest_wait(uint64_t limit_ns, int32_t* dev_status, void* str
 
 void mc2_set_wait_limit_ns(uint64_t limit_ns) { tl_wait_limit_ns = limit_ns; }
 
-void mc2_set_tile_pairing(int32_t mode) { tl_tile_pairing = mode >= 1 && mode <= 3 ? mode : 0; }
+void mc2_set_tile_pairing(int32_t mode) { tl_tile_pairing = mode >= 1 && mode <= 2 ? mode : 0; }
 
 void mc2_set_launch_overlap(int32_t enabled) { tl_launch_overlap = enabled ? 1 : 0; }
 

@@ -293,15 +293,7 @@ __device__ __forceinline__ void bulk_wait_keep_n(int keep) {
   }
 }
 
-// MC: a cluster of two CTAs runs two m-tiles of the same (expert, n-tile)
-// (m = 2 * pair + rank), each with its own accumulator; each CTA loads one
-// half of the shared weight tile (fc1: gate or up) with a multicast copy that
-// lands in both CTAs, so a k-block moves 32 KB from L2 per SM instead of 48.
-// A stage is reused once both CTAs' MMAs have released it (each MMA commit
-// arrives on the stage's empty barrier in both CTAs).  An expert with an odd
-// number of m-tiles leaves rank 1 without rows in its last pair (it computes
-// padding and stores nothing).  bf16 fc1 with gathered rows only.
-template <int MODE, int ES, bool MC = false>
+template <int MODE, int ES>
 __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     gmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
@@ -333,29 +325,18 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
-  static_assert(!MC || (MODE == MODE_FC1 && ES == 2), "multicast pairs: bf16 fc1 only");
-  const uint32_t rank = MC ? cluster_ctarank() : 0u;
-  const int unit = MC ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int nunits = MC ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-  // this CTA's rows of tile `tile`: [row0, row0 + rows) (rows <= 0: padding
-  // of an MC pair); pair0 is a valid row of the tile
-  auto tile_at = [&](int tile, int& e, int& n, int& row0, int& rows, int& pair0) {
+  const int unit = static_cast<int>(blockIdx.x);
+  const int nunits = static_cast<int>(gridDim.x);
+  // this CTA's rows of tile `tile`: [row0, row0 + rows)
+  auto tile_at = [&](int tile, int& e, int& n, int& row0, int& rows) {
     decode_tile(tile, prefix, E, p.n_tiles, p.offsets, e, n, row0, rows);
-    pair0 = row0;
-    if constexpr (MC) {  // decode_tile counted m-pairs: row0 = off + pair * BM
-      const int off = __ldg(p.offsets + e);
-      const int mp = (row0 - off) / BM;
-      pair0 = off + 2 * mp * BM;
-      row0 = pair0 + static_cast<int>(rank) * BM;
-      rows = min(BM, __ldg(p.offsets + e + 1) - row0);
-    }
   };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       // fc1: the TMA arm of the B tile plus one arrival per gather thread
       mbar_init(&full[s], GATHER ? 1 + 32 * Roles<MODE>::kGatherWarps : 1);
-      mbar_init(&empty[s], MC ? 2 : 1);  // MC: the MMA commits of both CTAs
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -387,7 +368,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
       int t = 0;
       if (e < E) {
         const int rows = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
-        t = ((rows + (MC ? 2 : 1) * BM - 1) / ((MC ? 2 : 1) * BM)) * p.n_tiles;
+        t = ((rows + BM - 1) / BM) * p.n_tiles;
       }
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -400,8 +381,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     if (lane == 0) prefix[0] = 0;
   }
   tc_fence_before();
-  if constexpr (MC) cluster_sync();  // the peer's barriers exist before any multicast
-  else __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_base_sh;
   const int total = prefix[E];
@@ -415,11 +395,10 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     int n_arm = 0;
     bool ok = true;
     for (int tile = unit; tile < total && ok; tile += nunits) {
-      int e, n, row0, rows, pair0;
-      tile_at(tile, e, n, row0, rows, pair0);
+      int e, n, row0, rows;
+      tile_at(tile, e, n, row0, rows);
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (lane == 0)
-          ok = MC ? mbar_wait_cluster(&empty[s], ph ^ 1, ctl) : mbar_wait(&empty[s], ph ^ 1, ctl);
+        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, ctl);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
@@ -427,11 +406,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           uint8_t* b_dst = sB + s * B_STAGE;
           const int k0 = kb * BK;
           if (!GATHER) tma_load_2d(sA + s * A_STAGE, &tmA, &full[s], k0, row0);
-          if constexpr (MC) {
-            // this CTA's half (gate or up blocks) into both CTAs of the pair
-            tma_load_5d_mcast(b_dst + rank * (B_STAGE / 2), &tmB, &full[s], 0, k0, n * (NB / 2),
-                              static_cast<int>(rank), e, 0x3);
-          } else if constexpr (BKM) {
+          if constexpr (BKM) {
             // K-major B: N rows of 128 bytes of K; fc1 loads the gate rows
             // and the up rows of the same output columns as two boxes
             if (!kIsFc2<MODE>) {
@@ -454,15 +429,13 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
         if (++s == STAGES) { s = 0; ph ^= 1; }
       }
     }
-    // Let every armed stage land (and, MC, both MMA commits to it arrive)
-    // before the CTA can exit (bounded).
+    // Let every armed stage land before the CTA can exit (bounded).
     if (lane == 0) {
       volatile int never = 0;
       WaitCtl drain{&never, p.wait_limit_ns, p.dev_status};
       for (int st = 0; st < STAGES && st < n_arm; ++st) {
         const int last = st + STAGES * ((n_arm - 1 - st) / STAGES);
-        mbar_wait_cluster(&full[st], (last / STAGES) & 1, drain);
-        if (MC) mbar_wait_cluster(&empty[st], (last / STAGES) & 1, drain);
+        mbar_wait(&full[st], (last / STAGES) & 1, drain);
       }
     }
   } else if (warp == 1) {
@@ -496,8 +469,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
                                        : smem_desc_sw128(b_base + kk * KK_B, B_BLOCK, 1024);
             umma<TR::KIND>(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0);
           }
-          if constexpr (MC) umma_commit_mcast(&empty[s], 0x3);  // frees the stage in both CTAs
-          else umma_commit(&empty[s]);
+          umma_commit(&empty[s]);
         }
         __syncwarp();
         if (++s == STAGES) { s = 0; ph ^= 1; }
@@ -535,9 +507,9 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     uint32_t ph = 0;
     bool ok = true;
     for (int tile = unit; tile < total && ok; tile += nunits) {
-      int e, n, row0, rows, pair0;
-      tile_at(tile, e, n, row0, rows, pair0);
-      const int tok0 = __ldg(p.permute_src + pair0) / p.k;  // tail rows repeat a valid row
+      int e, n, row0, rows;
+      tile_at(tile, e, n, row0, rows);
+      const int tok0 = __ldg(p.permute_src + row0) / p.k;  // tail rows repeat a valid row
       const char* src[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -546,8 +518,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
         src[i] = xg + tok * row_bytes + chunk * 16;
       }
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (lane == 0)
-          ok = MC ? mbar_wait_cluster(&empty[s], ph ^ 1, ctl) : mbar_wait(&empty[s], ph ^ 1, ctl);
+        if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1, ctl);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         const uint32_t a_dst = smem_u32(sA + s * A_STAGE);
@@ -576,8 +547,8 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
     int pend_grow0 = 0, pend_wrows = 0, pend_n = 0, qs = 0;
     uint32_t qph = 0;
     for (int tile = unit; tile < total; tile += nunits) {
-      int e, n, row0, rows, pair0;
-      tile_at(tile, e, n, row0, rows, pair0);
+      int e, n, row0, rows;
+      tile_at(tile, e, n, row0, rows);
       int ngroups_tma = 0;
       bool ok = true;
       if (lane == 0) ok = mbar_wait(&tfull[acc], aph, ctl);
@@ -753,8 +724,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
   }
 
   tc_fence_before();
-  if constexpr (MC) cluster_sync();  // no multicast copy or commit still targets this CTA
-  else __syncthreads();
+  __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
@@ -1347,7 +1317,7 @@ int num_sms() {
   return n > 0 ? n : 1;
 }
 
-template <int MODE, int ES, bool MC = false>
+template <int MODE, int ES>
 static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
   const mc2_shape_t& s = *g.s;
   using TR = ElemTraits<ES>;
@@ -1378,10 +1348,8 @@ static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
     p.K = s.H;
     p.n_tiles = (s.I + BN / 2 - 1) / (BN / 2);
     p.out_cols = s.I;
-    // MC: each CTA's box is one half (gate or up) of the B stage
     ok = (TR::B_KMAJOR ? encode_3d(&tB, dt, ES, g.b, s.H, 2ull * s.I, s.E, TR::BK, BN / 2)
-                       : encode_b_blocked(&tB, g.b, s.H, 2ull * s.I, s.E, 2, TR::BK, NB1 / 2,
-                                          MC ? 1 : 2)) &&
+                       : encode_b_blocked(&tB, g.b, s.H, 2ull * s.I, s.E, 2, TR::BK, NB1 / 2, 2)) &&
          encode_2d(&tOut, dt, ES, g.out, MODE == MODE_FC1_PRE ? 2ull * s.I : s.I, R, 128 / ES, 32);
     if (MODE == MODE_FC1_ROWS)  // already permuted rows [R, H]: plain TMA tiles
       ok = ok && encode_2d(&tA, dt, ES, g.a, s.H, R, 128 / ES, BM);
@@ -1402,41 +1370,14 @@ static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(gmm_kernel<MODE, ES, MC>,
+    attr_err = cudaFuncSetAttribute(gmm_kernel<MODE, ES>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(fixed + 1025 * sizeof(int32_t)));
   });
   if (attr_err != cudaSuccess) return attr_err;
-  if constexpr (MC) {
-    // persistent grid: as many 2-CTA clusters as can be resident at once
-    static std::once_flag once_clusters;
-    static int max_clusters = 0;
-    std::call_once(once_clusters, [&] {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(num_sms() & ~1, 1, 1);
-      cfg.blockDim = dim3(Roles<MODE>::kThreads, 1, 1);
-      cfg.dynamicSmemBytes = fixed + 1025 * sizeof(int32_t);
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&max_clusters, gmm_kernel<MODE, ES, MC>, &cfg) !=
-          cudaSuccess)
-        max_clusters = 0;
-    });
-    if (max_clusters < 1) return cudaErrorInvalidConfiguration;
-    const int64_t jobs_upper = (R / (2 * BM) + s.E) * static_cast<int64_t>(p.n_tiles);
-    const int grid =
-        2 * static_cast<int>(std::min<int64_t>(max_clusters, std::max<int64_t>(jobs_upper, 1)));
-    return launch_kernel(gmm_kernel<MODE, ES, MC>, dim3(grid), dim3(Roles<MODE>::kThreads), smem,
-                         st, 2, tA, tB, tOut, p);
-  }
   const int64_t tiles_upper = (R / BM + s.E) * static_cast<int64_t>(p.n_tiles);
   const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_upper, 1)));
-  return launch_kernel(gmm_kernel<MODE, ES, MC>, dim3(grid), dim3(Roles<MODE>::kThreads), smem,
+  return launch_kernel(gmm_kernel<MODE, ES>, dim3(grid), dim3(Roles<MODE>::kThreads), smem,
                        st, 1, tA, tB, tOut, p);
 }
 
@@ -1542,11 +1483,6 @@ static bool use_pairs(const mc2_shape_t& s, int mode) {
          R >= 2 * BM * static_cast<int64_t>(s.E);
 }
 
-// fc1 on multicast CTA pairs (MC): only when forced (mc2_set_tile_pairing(3)).
-static bool use_mcast_fc1(const mc2_shape_t&) {
-  return tile_pairing_override() == 3 && num_sms() >= 2;
-}
-
 bool fused_combine_supported(const mc2_shape_t& s) {
   const int64_t items = static_cast<int64_t>(s.T) * ((s.H + BN - 1) / BN);
   return s.k >= 1 && s.k <= KMAX_FUSED && items < (int64_t(1) << 31);
@@ -1645,9 +1581,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
   cudaError_t e;
   const bool pairs = use_pairs(*g.s, g.mode);
   if (g.mode == MODE_FC1) {
-    if (use_mcast_fc1(*g.s) && g.a_elem_bytes == 2)
-      e = launch_one<MODE_FC1, 2, true>(g, st);
-    else if (pairs)
+    if (pairs)
       e = g.a_elem_bytes == 2 ? launch_pair<MODE_FC1, 2>(g, st) : launch_pair<MODE_FC1, 4>(g, st);
     else
       e = g.a_elem_bytes == 2 ? launch_one<MODE_FC1, 2>(g, st) : launch_one<MODE_FC1, 4>(g, st);

@@ -199,20 +199,6 @@ __device__ __forceinline__ void tma_load_5d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// Multicast form: one copy from this CTA lands at the same shared-memory
-// offset in every CTA of `cta_mask` (this GPU's memory only) and signals the
-// mbarrier at the same offset in each of them.
-__device__ __forceinline__ void tma_load_5d_mcast(void* dst, const CUtensorMap* m, uint64_t* bar,
-                                                  int32_t c0, int32_t c1, int32_t c2, int32_t c3,
-                                                  int32_t c4, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
-      "r"(c4), "h"(cta_mask)
-      : "memory");
-}
-
 // Shared -> global tile store through a tensor map (bulk async-group).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int32_t c0,
                                              int32_t c1) {
@@ -355,16 +341,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-
-// Arrive once on `bar` (same offset) in every CTA of `cta_mask` when every
-// tcgen05 op issued so far by this thread (single-CTA MMAs) is done.
-__device__ __forceinline__ void umma_commit_mcast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 

@@ -121,10 +121,9 @@ SMALL = [
 ]
 
 
-@pytest.fixture(params=[1, 2, 3], ids=["single_cta", "cta_pairs", "mcast_fc1"])
+@pytest.fixture(params=[1, 2], ids=["single_cta", "cta_pairs"])
 def pairing(request):
-    """Force one grouped-GEMM tiling (single CTAs, CTA pairs, or fc1 on
-    multicast 2-CTA clusters) for the test."""
+    """Force one grouped-GEMM tiling (single CTAs or CTA pairs) for the test."""
     ensure_built()
     B.mc2_set_tile_pairing(request.param)
     yield request.param
@@ -168,12 +167,12 @@ def test_fc2_alone_on_oracle_h():
 
 @pytest.mark.parametrize("name", ["uniform", "skew"])
 def test_tilings_equal_bitwise_full_size(name):
-    """Every fc1 tiling accumulates each output in the same K order: the
-    full-size h and out are identical bit for bit across single CTAs, CTA
-    pairs and multicast clusters."""
+    """Every tiling accumulates each output in the same K order: the
+    full-size h and out are identical bit for bit on single CTAs and on CTA
+    pairs."""
     wl = WORKLOADS[name]
     res = []
-    for mode in (1, 2, 3):
+    for mode in (1, 2):
         B.mc2_set_tile_pairing(mode)
         try:
             _, _, b = run_gpu(wl, seed=5)
