@@ -792,6 +792,11 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
       const int grow = grow0 + lane;
       const bool valid = lane < wrows;
       bool f_int = false;  // slot F holds int32 sums (after a fold) instead of fp32
+      // The dequant needs only fp32(sum), the round-to-nearest value of the
+      // exact int32 sum.  With two chunks, both exact fp32 integers below
+      // 2^24, one fp32 add gives it (no conversions in the fold or the
+      // dequant).  The raw int32 output and longer K fold in exact int32.
+      const bool fsum = !p.raw && nchunk <= 2;
       for (int c = 1; c < nchunk; ++c) {  // fold each later chunk into F, then release S
         if (lane == 0) ok = mbar_wait(&done[S], (pd >> S) & 1u, ctl);
         pd ^= 1u << S;
@@ -807,18 +812,26 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
             tmem_ld32(tS + g * 64, vb[0]);
             tmem_ld32(tS + g * 64 + 32, vb[1]);
             tmem_ld_wait();
+            if (fsum) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+              for (int h = 0; h < 2; ++h)
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                va[h][i] = static_cast<uint32_t>(
-                    (f_int ? static_cast<int32_t>(va[h][i]) : f2i(va[h][i])) + f2i(vb[h][i]));
+                for (int i = 0; i < 32; ++i)
+                  va[h][i] = __float_as_uint(__uint_as_float(va[h][i]) + __uint_as_float(vb[h][i]));
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  va[h][i] = static_cast<uint32_t>(
+                      (f_int ? static_cast<int32_t>(va[h][i]) : f2i(va[h][i])) + f2i(vb[h][i]));
+            }
             tmem_st32(tF + g * 64, va[0]);
             tmem_st32(tF + g * 64 + 32, va[1]);
           }
           tmem_st_wait();
         }
-        f_int = true;
+        f_int = !fsum;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sfree[S]);
@@ -837,6 +850,26 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
           o1[i] = f_int ? static_cast<int32_t>(vb[i]) : f2i(vb[i]);
         }
       };
+      // the same sums rounded to fp32 (what the dequant multiplies): int32
+      // slots are converted, fp32 slots already hold that value (a zero sum is
+      // +0, as the conversion of int 0 gives)
+      auto acc2x32 = [&](int c0, int c1, float (&o0)[32], float (&o1)[32]) {
+        uint32_t va[32], vb[32];
+        tmem_ld32(tF + c0, va);
+        tmem_ld32(tF + c1, vb);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (f_int) {
+            o0[i] = static_cast<float>(static_cast<int32_t>(va[i]));
+            o1[i] = static_cast<float>(static_cast<int32_t>(vb[i]));
+          } else {
+            const float x0 = __uint_as_float(va[i]), x1 = __uint_as_float(vb[i]);
+            o0[i] = x0 == 0.f ? 0.f : x0;
+            o1[i] = x1 == 0.f ? 0.f : x1;
+          }
+        }
+      };
       if (wrows > 0) {
         float rs = 0.f;
         if (valid && !p.raw)
@@ -851,10 +884,10 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
         for (int gi = 0; gi < 4; ++gi) {
           const int col0 = n * (MODE == MODE_FC1 ? 128 : QW_BN) + gi * GW;
           if (col0 >= (MODE == MODE_FC1 ? p.I : p.H)) break;
-          int32_t s0[32], s1[32];
-          if (MODE == MODE_FC1) sums2x32(gi * 32, 128 + gi * 32, s0, s1);  // gate, up
-          else sums2x32(gi * 64, gi * 64 + 32, s0, s1);
           if (p.raw) {  // test mode: the int32 accumulators themselves
+            int32_t s0[32], s1[32];
+            if (MODE == MODE_FC1) sums2x32(gi * 32, 128 + gi * 32, s0, s1);  // gate, up
+            else sums2x32(gi * 64, gi * 64 + 32, s0, s1);
             if (valid) {
               int32_t* o = static_cast<int32_t*>(p.out);
               int4* d0;
@@ -875,6 +908,9 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
             continue;
           }
           // dequant: (row scale * column scale) * acc, in fp32
+          float s0[32], s1[32];
+          if (MODE == MODE_FC1) acc2x32(gi * 32, 128 + gi * 32, s0, s1);  // gate, up
+          else acc2x32(gi * 64, gi * 64 + 32, s0, s1);
           uint32_t pk[32];
           // column scales as float4 loads (16-byte aligned: the scale rows
           // start at multiples of 64 columns and col0 is a multiple of 32)
@@ -891,16 +927,16 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
           if (MODE == MODE_FC1) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float g = (rs * w0[i]) * static_cast<float>(s0[i]);
-              const float u = (rs * w1[i]) * static_cast<float>(s1[i]);
+              const float g = (rs * w0[i]) * s0[i];
+              const float u = (rs * w1[i]) * s1[i];
               pk[i] = __float_as_uint(silu_f(g) * u);
             }
           } else {  // y as fp16 with a power-of-two scale per 64 columns
             uint32_t y0[32], y1[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              y0[i] = __float_as_uint((rs * w0[i]) * static_cast<float>(s0[i]));
-              y1[i] = __float_as_uint((rs * w1[i]) * static_cast<float>(s1[i]));
+              y0[i] = __float_as_uint((rs * w0[i]) * s0[i]);
+              y1[i] = __float_as_uint((rs * w1[i]) * s1[i]);
             }
             const float inv = pack_y16(y0, y1, pk);
             if (valid) p.yscale[static_cast<int64_t>(grow) * (p.H / 64) + col0 / 64] = inv;

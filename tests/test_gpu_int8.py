@@ -80,6 +80,40 @@ def test_int8_worst_case_magnitudes_exact(pairing, K):
     assert np.array_equal(to_np(b.h).astype(np.int64), ref["acc1"])
 
 
+@pytest.mark.parametrize("K", [2048, 3072, 4096])
+def test_int8_worst_case_dequant_tilings_bitwise(K):
+    """All values +-127 in long same-sign runs: most fc1 sums lie past 2^24
+    (up to 47M at K = 4096), where fp32(acc) rounds.  The wide tiles form
+    fp32(acc) with one fp32 add of the two chunks' exact sums at K = 2048 and
+    by converting the folded int32 sums beyond; the 128 x 128 tiles convert
+    the exact int32 sums.  h_q, its scales and the block output must agree bit
+    for bit, and the output stays within the tolerance of the oracle."""
+    wl = Workload("i8_worst_dq", 64, K, 128, 2, 1, 1, "i8")
+    inp = make_inputs(wl, 1)
+    inp["x"] = np.full_like(inp["x"], 127)
+    inp["x"][1::2] = -127
+    inp["x"][2::4, ::5] = -127
+    inp["w1"] = np.full_like(inp["w1"], 127)
+    inp["w1"][:, :, 1::3] = -127
+    inp["w1"][:, ::7, :] = -inp["w1"][:, ::7, :]
+    res = []
+    for mode in (0, 1):
+        B.mc2_set_tile_pairing(mode)
+        try:
+            d, b = _run(wl, inp, out="bf16")
+            res.append((to_np(b.h), to_np(b.h_scale), to_np(b.out)))
+            assert int(b.dev_status.item()) == 0
+        finally:
+            B.mc2_set_tile_pairing(0)
+    for a, c in zip(res[0], res[1]):
+        assert np.array_equal(a.view(np.uint8), c.view(np.uint8))
+    ref = orc.quant_block_forward(inp["x"], inp["xs"], inp["w1"], inp["w1s"], inp["w2"],
+                                  inp["w2s"], inp["sel"], inp["probs"], wl.E, wl.W)
+    assert (np.abs(ref["acc1"]) > 2 ** 24).mean() > 0.5  # most sums round in fp32
+    ok, a, m = orc.bf16_tolerance_ok(res[0][2], ref["out"])
+    assert ok, f"out: max {a:.3e}, mean {m:.3e}"
+
+
 @pytest.mark.parametrize("wl", SMALL_I8, ids=lambda w: w.name)
 def test_int8_block_parity(wl, pairing):
     inp = make_inputs(wl, 8)
