@@ -541,11 +541,12 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
 // 256 cycles.  TMEM holds two 256-column accumulator slots.  Tile t of a CTA
 // has a first slot F = t mod 2 and a second slot S: chunk 0 of K (k < 1024)
 // accumulates in F, every later chunk in S, and the epilogue folds each of
-// them into F as exact int32 (tcgen05.st; F then holds the running int32
-// sum), releasing S at once.  The next tile's chunk 0 therefore accumulates in
-// S while the epilogue dequantises and stores the current tile from F.  The
-// arithmetic after the int32 sums is the 128 x 128 kernel's, so both give the
-// same bits.
+// them into F (tcgen05.ld, add, tcgen05.st), releasing S at once.  The next
+// tile's chunk 0 therefore accumulates in S while the epilogue dequantises and
+// stores the current tile from F.  The folds keep the running sum as exact
+// fp32 integers while they stay below 2^24 and as int32 beyond; the last fold
+// rounds once to fp32, the value the 128 x 128 kernel's dequant takes from
+// its int32 sums, so both give the same bits.
 // ----------------------------------------------------------------------------
 constexpr int QW_BN = 256;
 constexpr int QW_STAGES = 4;
@@ -791,12 +792,15 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
       const int grow0 = row0 + q * 32;
       const int grow = grow0 + lane;
       const bool valid = lane < wrows;
-      bool f_int = false;  // slot F holds int32 sums (after a fold) instead of fp32
-      // The dequant needs only fp32(sum), the round-to-nearest value of the
-      // exact int32 sum.  With two chunks, both exact fp32 integers below
-      // 2^24, one fp32 add gives it (no conversions in the fold or the
-      // dequant).  The raw int32 output and longer K fold in exact int32.
-      const bool fsum = !p.raw && nchunk <= 2;
+      // Representation of slot F per 64-column group (bit g of gint, the same
+      // for the whole warp): fp32 or int32.  Every chunk sum is an exact fp32
+      // integer below 2^24.  The dequant needs only fp32(sum), the
+      // round-to-nearest value of the exact int32 sum.  A fold adds in fp32
+      // while that stays exact (every |sum| of the warp's group below 2^24,
+      // checked by a warp vote) and always at the last fold (one rounding of
+      // the exact sum, which is fp32(sum)); otherwise the group switches to
+      // exact int32.  The raw int32 output folds in int32 throughout.
+      uint32_t gint = 0;
       for (int c = 1; c < nchunk; ++c) {  // fold each later chunk into F, then release S
         if (lane == 0) ok = mbar_wait(&done[S], (pd >> S) & 1u, ctl);
         pd ^= 1u << S;
@@ -812,26 +816,46 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
             tmem_ld32(tS + g * 64, vb[0]);
             tmem_ld32(tS + g * 64 + 32, vb[1]);
             tmem_ld_wait();
-            if (fsum) {
+            bool to_int = p.raw || ((gint >> g) & 1u);
+            if (!to_int && c == nchunk - 1) {  // last fold: one rounding of the exact sum
 #pragma unroll
               for (int h = 0; h < 2; ++h)
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                   va[h][i] = __float_as_uint(__uint_as_float(va[h][i]) + __uint_as_float(vb[h][i]));
-            } else {
+            } else if (!to_int) {
+              bool exact = true;
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  const float x = __uint_as_float(va[h][i]) + __uint_as_float(vb[h][i]);
+                  exact = exact && fabsf(x) < 16777216.0f;
+                  va[h][i] = __float_as_uint(x);
+                }
+              if (!__all_sync(0xffffffffu, exact)) {
+                // rare: F's group is still unchanged in TMEM; fold it in int32
+                tmem_ld32(tF + g * 64, va[0]);
+                tmem_ld32(tF + g * 64 + 32, va[1]);
+                tmem_ld_wait();
+                to_int = true;
+              }
+            }
+            if (to_int) {
+              const bool fi = (gint >> g) & 1u;
 #pragma unroll
               for (int h = 0; h < 2; ++h)
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                   va[h][i] = static_cast<uint32_t>(
-                      (f_int ? static_cast<int32_t>(va[h][i]) : f2i(va[h][i])) + f2i(vb[h][i]));
+                      (fi ? static_cast<int32_t>(va[h][i]) : f2i(va[h][i])) + f2i(vb[h][i]));
+              gint |= 1u << g;
             }
             tmem_st32(tF + g * 64, va[0]);
             tmem_st32(tF + g * 64 + 32, va[1]);
           }
           tmem_st_wait();
         }
-        f_int = !fsum;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sfree[S]);
@@ -844,10 +868,11 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
         tmem_ld32(tF + c0, va);
         tmem_ld32(tF + c1, vb);
         tmem_ld_wait();
+        const bool i0 = (gint >> (c0 >> 6)) & 1u, i1 = (gint >> (c1 >> 6)) & 1u;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          o0[i] = f_int ? static_cast<int32_t>(va[i]) : f2i(va[i]);
-          o1[i] = f_int ? static_cast<int32_t>(vb[i]) : f2i(vb[i]);
+          o0[i] = i0 ? static_cast<int32_t>(va[i]) : f2i(va[i]);
+          o1[i] = i1 ? static_cast<int32_t>(vb[i]) : f2i(vb[i]);
         }
       };
       // the same sums rounded to fp32 (what the dequant multiplies): int32
@@ -858,16 +883,12 @@ __global__ void __launch_bounds__(QRoles<MODE>::kThreads, 1)
         tmem_ld32(tF + c0, va);
         tmem_ld32(tF + c1, vb);
         tmem_ld_wait();
+        const bool i0 = (gint >> (c0 >> 6)) & 1u, i1 = (gint >> (c1 >> 6)) & 1u;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          if (f_int) {
-            o0[i] = static_cast<float>(static_cast<int32_t>(va[i]));
-            o1[i] = static_cast<float>(static_cast<int32_t>(vb[i]));
-          } else {
-            const float x0 = __uint_as_float(va[i]), x1 = __uint_as_float(vb[i]);
-            o0[i] = x0 == 0.f ? 0.f : x0;
-            o1[i] = x1 == 0.f ? 0.f : x1;
-          }
+          const float x0 = __uint_as_float(va[i]), x1 = __uint_as_float(vb[i]);
+          o0[i] = i0 ? static_cast<float>(static_cast<int32_t>(va[i])) : (x0 == 0.f ? 0.f : x0);
+          o1[i] = i1 ? static_cast<float>(static_cast<int32_t>(vb[i])) : (x1 == 0.f ? 0.f : x1);
         }
       };
       if (wrows > 0) {
