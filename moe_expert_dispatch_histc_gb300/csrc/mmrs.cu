@@ -387,25 +387,46 @@ __global__ void __launch_bounds__(FCfg<NB>::kThreads, 1)
 #pragma unroll
         for (int g = 0; g < 128 / GW; ++g) {
           if (g * GW < ncols) {   // no scales exist past column n
-            int32_t si[GW];
-#pragma unroll
-            for (int i = 0; i < GW; ++i) si[i] = 0;
-#pragma unroll 1
-            for (int c = 0; c < nchunk; ++c) {   // exact int32 sum of the chunk sums
+            // fp32 of the rank's exact int32 sum.  Each chunk sum is an exact
+            // fp32 integer below 2^24: one chunk is that value itself, two
+            // give it with one fp32 add (a single rounding of the exact sum);
+            // more chunks are summed in int32 and converted.
+            float af[GW];
+            if (nchunk <= 2) {
               uint32_t v[GW];
-              tmem_ld_group<GW>(tbase + c * NB + g * GW, v);
+              tmem_ld_group<GW>(tbase + g * GW, v);
               tmem_ld_wait();
 #pragma unroll
-              for (int i = 0; i < GW; ++i) si[i] += __float2int_rn(__uint_as_float(v[i]));
+              for (int i = 0; i < GW; ++i) af[i] = __uint_as_float(v[i]);
+              if (nchunk == 2) {
+                tmem_ld_group<GW>(tbase + NB + g * GW, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < GW; ++i) af[i] += __uint_as_float(v[i]);
+              }
+            } else {
+              int32_t si[GW];
+#pragma unroll
+              for (int i = 0; i < GW; ++i) si[i] = 0;
+#pragma unroll 1
+              for (int c = 0; c < nchunk; ++c) {   // exact int32 sum of the chunk sums
+                uint32_t v[GW];
+                tmem_ld_group<GW>(tbase + c * NB + g * GW, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < GW; ++i) si[i] += __float2int_rn(__uint_as_float(v[i]));
+              }
+#pragma unroll
+              for (int i = 0; i < GW; ++i) af[i] = static_cast<float>(si[i]);
             }
 #pragma unroll
             for (int i = 0; i < GW; i += 4) {
               const float4 w4 = __ldg(reinterpret_cast<const float4*>(wr + g * GW + i));
               float* sp = sum + g * GW + i;
-              sp[0] = __fmaf_rn(xr * w4.x, static_cast<float>(si[i]), sp[0]);
-              sp[1] = __fmaf_rn(xr * w4.y, static_cast<float>(si[i + 1]), sp[1]);
-              sp[2] = __fmaf_rn(xr * w4.z, static_cast<float>(si[i + 2]), sp[2]);
-              sp[3] = __fmaf_rn(xr * w4.w, static_cast<float>(si[i + 3]), sp[3]);
+              sp[0] = __fmaf_rn(xr * w4.x, af[i], sp[0]);
+              sp[1] = __fmaf_rn(xr * w4.y, af[i + 1], sp[1]);
+              sp[2] = __fmaf_rn(xr * w4.z, af[i + 2], sp[2]);
+              sp[3] = __fmaf_rn(xr * w4.w, af[i + 3], sp[3]);
             }
           }
         }

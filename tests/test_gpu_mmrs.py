@@ -78,11 +78,14 @@ def test_mm_reduce_scatter_parity(W, m, k, n):
     _run(W, m, k, n, seed=W * 7 + k)
 
 
-def test_mm_reduce_scatter_worst_case_accumulators():
-    """k = 4096 with every product -127*127: |acc| = 66 M > 2^24 per rank, still
-    exact in int32 (four exact 1024-long chunks; the fused form then has one
-    accumulator set in TMEM instead of two)."""
-    _run(2, 128, 4096, 128, worst=True)
+@pytest.mark.parametrize("k", [2048, 4096])
+def test_mm_reduce_scatter_worst_case_accumulators(k):
+    """Every product -127*127: |acc| = k * 127^2 > 2^24 per rank (33 M at
+    k = 2048, 66 M at k = 4096), exact in int32 (1024-long exact chunks; at
+    k = 4096 the fused form has one accumulator set in TMEM instead of two).
+    With two chunks the fused form rounds their fp32 sum once, which must
+    equal the two-pass form's conversion of the exact int32 sum bit for bit."""
+    _run(2, 128, k, 128, worst=True)
 
 
 def test_mm_reduce_scatter_empty_and_rejected():
