@@ -1056,6 +1056,45 @@ __global__ void requant_rows_kernel(const float* __restrict__ h, const int32_t* 
   }
 }
 
+// The same with the row held in registers (NV float4 per lane, I <= 128 NV):
+// one read of h, every load of the row in flight before the max.
+template <int NV>
+__global__ void requant_rows_reg_kernel(const float* __restrict__ h,
+                                        const int32_t* __restrict__ offsets, int E, int I,
+                                        int8_t* __restrict__ hq, float* __restrict__ hs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  griddep_wait();
+  griddep_launch_dependents();
+  if (row >= __ldg(offsets + E)) return;
+  const int I4 = I / 4;
+  const float4* hr = reinterpret_cast<const float4*>(h + row * I);
+  float4 v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = lane + 32 * i;
+    v[i] = c < I4 ? __ldg(hr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i)
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float scale = m > 0.f ? __fdiv_rn(m, 127.0f) : 1.0f;
+  if (lane == 0) hs[row] = scale;
+  char4* qr = reinterpret_cast<char4*>(hq + row * I);
+  auto q = [&](float x) {
+    const float r = rintf(__fdiv_rn(x, scale));
+    return static_cast<signed char>(fminf(fmaxf(r, -127.f), 127.f));
+  };
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = lane + 32 * i;
+    if (c < I4) qr[c] = make_char4(q(v[i].x), q(v[i].y), q(v[i].z), q(v[i].w));
+  }
+}
+
 cudaError_t launch_i8_to_bf16_2(const int8_t* src0, void* dst0, size_t n0, const int8_t* src1,
                                 void* dst1, size_t n1, cudaStream_t st) {
   // every int8 tensor converted here has a multiple of 64 elements
@@ -1081,9 +1120,19 @@ cudaError_t launch_requant(const float* h, const int32_t* offsets, const mc2_sha
   const int64_t R = static_cast<int64_t>(s.T) * s.k;
   if (R == 0) return cudaSuccess;
   const int warps = 8;
-  const cudaError_t e = launch_kernel(
-      requant_rows_kernel, dim3(static_cast<unsigned>((R + warps - 1) / warps)), dim3(warps * 32), 0,
-      st, 1, h, offsets, static_cast<int>(s.E), static_cast<int>(s.I), hq, hs);
+  const dim3 grid(static_cast<unsigned>((R + warps - 1) / warps)), block(warps * 32);
+  const int E = static_cast<int>(s.E), I = static_cast<int>(s.I);
+  cudaError_t e;
+  if (I <= 512)
+    e = launch_kernel(requant_rows_reg_kernel<4>, grid, block, 0, st, 1, h, offsets, E, I, hq, hs);
+  else if (I <= 1024)
+    e = launch_kernel(requant_rows_reg_kernel<8>, grid, block, 0, st, 1, h, offsets, E, I, hq, hs);
+  else if (I <= 1536)
+    e = launch_kernel(requant_rows_reg_kernel<12>, grid, block, 0, st, 1, h, offsets, E, I, hq, hs);
+  else if (I <= 2048)
+    e = launch_kernel(requant_rows_reg_kernel<16>, grid, block, 0, st, 1, h, offsets, E, I, hq, hs);
+  else
+    e = launch_kernel(requant_rows_kernel, grid, block, 0, st, 1, h, offsets, E, I, hq, hs);
   note_launches(1);
   return e;
 }
