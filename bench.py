@@ -456,7 +456,7 @@ def run_cuda_workload(args, wl, headline):
         "segments_ms": {name: float(seg[:, i].mean()) for name, i in segi.items()},
         "roofline": {"kernel": ("gmm_kernel<fc1 rows> (fc1 + SwiGLU on materialised rows)"
                                 if unfused else
-                                "gmm_q_kernel<fc1> (permute gather + exact int8 fc1 + dequant + "
+                                "gmm_qw_kernel<fc1> (permute gather + exact int8 fc1 + dequant + "
                                 "SwiGLU), timed over its segment, which also holds the x copy to "
                                 "bf16 and the row requant" if wl.act == "i8" else
                                 "gmm_kernel<fc1, tf32> (permute gather + fc1 + SwiGLU)"
@@ -475,6 +475,13 @@ def run_cuda_workload(args, wl, headline):
         "gpu_launches": launches,
         "clocks": clk,
     }
+    # the counts step against HBM: ids read once; counts, offsets and both
+    # index maps written (a few microseconds: launch and barrier latency bound)
+    c_ms = line["segments_ms"]["counts"]
+    R = wl.T * wl.k
+    c_bytes = 4 * (R + 2 * wl.W * wl.E + wl.E + 1 + 2 * R)
+    line["counts"] = {"ms": c_ms, "bytes": c_bytes, "achieved_gbs": c_bytes / (c_ms / 1e3) / 1e9,
+                      "frac_of_hbm": c_bytes / (c_ms / 1e3) / 1e9 / hbm}
     if unfused:
         line["config"]["path"] = "unfused: materialised permute + plain grouped fc1"
     if args.tiling != "auto":
