@@ -685,3 +685,34 @@ def test_planted_mistakes_are_caught(monkeypatch, mutation):
         except (AssertionError, ValueError, IndexError):
             failures += 1
     assert failures > 0, f"no pin caught the planted mistake {mutation}"
+
+
+def test_backward_gradients_are_local_to_experts_and_tokens():
+    """The chain rule keeps the block's gradients local: an expert's dw1, dw2
+    depend only on the rows routed to it, a token's dx and dprobs only on its
+    own k slots.  The full oracle must equal reduced problems built from one
+    expert (its routed tokens as single-slot tokens) or one token (with its k
+    experts); the full-size GPU backward test relies on this."""
+    rng = np.random.default_rng(5)
+    T, H, I, E, k, W = 24, 16, 8, 6, 2, 2
+    x = rng.standard_normal((T, H))
+    w1 = rng.standard_normal((E, H, 2 * I)) * 0.3
+    w2 = rng.standard_normal((E, I, H)) * 0.3
+    sel = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    probs = rng.uniform(0.1, 1.0, (T, k))
+    dout = rng.standard_normal((T, H))
+    full = orc.block_backward(x, w1, w2, sel, probs, dout, E, W)
+    for e in range(E):
+        ts, js = np.nonzero(sel == e)
+        if len(ts) == 0:
+            assert not full["dw1"][e].any() and not full["dw2"][e].any()
+            continue
+        red = orc.block_backward(x[ts], w1[e:e + 1], w2[e:e + 1], np.zeros((len(ts), 1), np.int32),
+                                 probs[ts, js][:, None], dout[ts], 1, 1)
+        assert np.allclose(full["dw1"][e], red["dw1"][0], rtol=1e-12, atol=1e-12)
+        assert np.allclose(full["dw2"][e], red["dw2"][0], rtol=1e-12, atol=1e-12)
+    for t in range(T):
+        red = orc.block_backward(x[t:t + 1], w1[sel[t]], w2[sel[t]], np.arange(k, dtype=np.int32)[None],
+                                 probs[t:t + 1], dout[t:t + 1], k, 1)
+        assert np.allclose(full["dx"][t], red["dx"][0], rtol=1e-12, atol=1e-12)
+        assert np.allclose(full["dprobs"][t], red["dprobs"][0], rtol=1e-12, atol=1e-12)
