@@ -102,14 +102,16 @@ def test_mm_reduce_scatter_empty_and_rejected():
                                       check=False) == B.MC2_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("W,m,k,n", [(2, 8192, 512, 2048), (2, 4096, 3072, 2048)])
+@pytest.mark.parametrize("W,m,k,n", [(2, 8192, 512, 2048), (2, 4096, 3072, 2048),
+                                     (8, 4096, 1024, 4096)])
 def test_mm_reduce_scatter_many_tiles_per_cluster(W, m, k, n):
     """Shapes where every CTA pair of the fused kernel takes three or more
     output tiles (256-column tiles with two accumulator sets at k = 512;
-    128-column tiles with three K chunks at k = 3072), so accumulators and
-    barrier phases are reused across tiles.  The fused result must equal the
-    two-pass result bit for bit; sampled rows of both, and the two-pass int32
-    partials, against the oracle on those rows."""
+    128-column tiles with three K chunks at k = 3072; the benchmarked
+    W8 m4096 k1024 n4096), so accumulators and barrier phases are reused
+    across tiles.  The fused result must equal the two-pass result bit for
+    bit; sampled rows of both, and the two-pass int32 partials, against the
+    oracle on those rows."""
     ensure_built()
     rng = np.random.default_rng(k + n)
     x1 = rng.integers(-127, 128, (W, m, k)).astype(np.int8)
