@@ -124,6 +124,8 @@ mc2_status_t mc2_moe_counts(const mc2_shape_t* s, const int32_t* sel, int32_t* c
  *             rows p >= offsets[E] are not written.
  *   h_scale   [dev] fp32 [T*k] out (act I8 and out BF16 only, else NULL):
  *             per-row scale of the int8 h (max|h| / 127, 1 for an all-zero row)
+ * With T = 0 nothing is launched and x, w1, the scales, permute_src and h may
+ * be NULL (as in mc2_gmm_alltoallv).
  */
 mc2_status_t mc2_alltoallv_gmm(const mc2_shape_t* s, const void* x, const float* x_scale,
                                const void* w1, const float* w1_scale, const int32_t* offsets,

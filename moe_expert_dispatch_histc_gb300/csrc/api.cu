@@ -108,7 +108,9 @@ mc2_status_t do_fc1_i8(const mc2_shape_t* s, const void* x, const float* x_scale
                        void* ws, void* h, float* h_scale, int32_t* dev_status, cudaStream_t st, bool launch = true) {
   const bool raw = s->out == MC2_I32;
   if (!offsets || !ws) return MC2_ERR_INVALID_ARG;
-  if (raw ? (h_scale != nullptr) : (!x_scale || !w1_scale || !h_scale)) return MC2_ERR_INVALID_ARG;
+  // with T = 0 nothing is launched and the scales may be NULL (as the weights may)
+  if (raw ? (h_scale != nullptr) : (s->T > 0 && (!w1_scale || !x_scale || !h_scale)))
+    return MC2_ERR_INVALID_ARG;
   if (s->T > 0 && (!x || !permute_src || !h)) return MC2_ERR_INVALID_ARG;
   if (!aligned({x, x_scale, w1_scale, offsets, permute_src, h, h_scale}) || !aligned({ws}, 256))
     return MC2_ERR_INVALID_ARG;
@@ -144,7 +146,7 @@ mc2_status_t do_fc2_i8(const mc2_shape_t* s, const void* h, const float* h_scale
                        int32_t* dev_status, cudaStream_t st, bool launch = true) {
   const bool raw = s->out == MC2_I32;
   if (!offsets || !ws) return MC2_ERR_INVALID_ARG;
-  if (!raw && (!h_scale || !w2_scale)) return MC2_ERR_INVALID_ARG;
+  if (!raw && s->T > 0 && (!w2_scale || !h_scale)) return MC2_ERR_INVALID_ARG;
   if (s->T > 0 && (!h || !permute_src || !out || (!raw && (!unpermute_dst || !probs))))
     return MC2_ERR_INVALID_ARG;
   if (!aligned({h, h_scale, w2_scale, offsets, permute_src, unpermute_dst, probs, out}) ||

@@ -89,6 +89,24 @@ def test_null_pointers_are_rejected_before_any_launch():
     assert B.mc2_selftest_wait(1000, None, stream=0, check=False) == B.MC2_ERR_INVALID_ARG
 
 
+def test_int8_empty_batch_accepts_null_arrays_and_launches_nothing():
+    """T = 0: the per-token and per-row arrays are empty, so x, the scales,
+    permute_src and h may be NULL; the calls succeed without touching the
+    device (the stream argument is never used).  With tokens present the
+    scales are required."""
+    fake = 1 << 40
+    s = _shape(T=0, act="i8", out="bf16")
+    assert B.mc2_alltoallv_gmm(s, None, None, None, None, fake, None, fake, None, None,
+                               stream=0, check=False) == B.MC2_OK
+    assert B.mc2_gmm_alltoallv(s, None, None, None, None, fake, None, None, None, fake, None,
+                               stream=0, check=False) == B.MC2_OK
+    s = _shape(act="i8", out="bf16")
+    assert B.mc2_alltoallv_gmm(s, fake, None, fake, fake, fake, fake, fake, fake, fake,
+                               stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+    assert B.mc2_gmm_alltoallv(s, fake, None, fake, fake, fake, fake, fake, fake, fake, fake,
+                               stream=0, check=False) == B.MC2_ERR_INVALID_ARG
+
+
 def test_misaligned_pointers_are_rejected():
     s = _shape()
     fake = 1 << 40

@@ -114,25 +114,25 @@ def test_int8_worst_case_dequant_tilings_bitwise(K):
     assert ok, f"out: max {a:.3e}, mean {m:.3e}"
 
 
-@pytest.mark.parametrize("wl", SMALL_I8, ids=lambda w: w.name)
-def test_int8_block_parity(wl, pairing):
-    inp = make_inputs(wl, 8)
+def _check_block(wl, inp, expect_bad=False):
+    """The int8 block through its entry points against the oracle: scales to
+    fp32 rounding and codes to +-1 at ties, fc2 exactly on the GPU's own h_q,
+    the output within the block's tolerance; the device status word."""
     d, b = _run(wl, inp, out="bf16")
     hq = to_np(b.h)
     hs = to_np(b.h_scale)
     ref = orc.quant_block_forward(inp["x"], inp["xs"], inp["w1"], inp["w1s"], inp["w2"],
                                   inp["w2s"], inp["sel"], inp["probs"], wl.E, wl.W)
     n = int(ref["offsets"][-1])
+    assert np.array_equal(to_np(b.offsets), ref["offsets"])
     # re-quantisation: scales agree to fp32 rounding, codes to +-1 at ties
     assert np.allclose(hs[:n], ref["hs"], rtol=1e-5, atol=0)
     diff = np.abs(hq[:n].astype(int) - ref["hq"].astype(int))
     assert diff.max() <= 1 and (diff > 0).mean() < 1e-3
     # fc2 exactly on the GPU's own h_q
-    wl_raw = wl
-    shape_raw = blk.shape_of(wl_raw, "i32")
     acc2 = torch.empty((wl.R, wl.H), dtype=torch.int32, device="cuda")
-    B.mc2_gmm_alltoallv(shape_raw, b.h, None, d["w2"], None, b.offsets, b.permute_src, None, None,
-                        b.ws, acc2, b.dev_status)
+    B.mc2_gmm_alltoallv(blk.shape_of(wl, "i32"), b.h, None, d["w2"], None, b.offsets,
+                        b.permute_src, None, None, b.ws, acc2, b.dev_status)
     torch.cuda.synchronize()
     ref2 = orc.quant_block_forward(inp["x"], inp["xs"], inp["w1"], inp["w1s"], inp["w2"],
                                    inp["w2s"], inp["sel"], inp["probs"], wl.E, wl.W,
@@ -141,6 +141,52 @@ def test_int8_block_parity(wl, pairing):
     # the block output (bf16) within the block's tolerance of the float64 oracle
     ok, a, m = orc.bf16_tolerance_ok(to_np(b.out), ref["out"])
     assert ok, f"out: max {a:.3e}, mean {m:.3e}"
+    status = int(b.dev_status.item())
+    assert bool(status & B.MC2_DEV_BAD_EXPERT_ID) == expect_bad
+    assert not status & B.MC2_DEV_TIMEOUT
+    return ref
+
+
+@pytest.mark.parametrize("wl", SMALL_I8, ids=lambda w: w.name)
+def test_int8_block_parity(wl, pairing):
+    _check_block(wl, make_inputs(wl, 8))
+
+
+def _with_sel(wl, sel, seed):
+    inp = make_inputs(wl, seed)
+    inp["sel"] = np.ascontiguousarray(np.asarray(sel).astype(np.int32))
+    return inp
+
+
+def test_int8_all_tokens_to_one_expert(pairing):
+    """Every token on expert 5, the seven others empty: 512 rows make four row
+    tiles of one expert, K = 3072 runs in three exact chunks; fc1's int32
+    accumulators exact, the block within tolerance."""
+    wl = Workload("i8_one_expert", 512, 3072, 256, 8, 1, 2, "i8")
+    inp = _with_sel(wl, np.full((512, 1), 5), 3)
+    d, b = _run(wl, inp, out="i32")
+    ref = orc.quant_block_forward(inp["x"], inp["xs"], inp["w1"], inp["w1s"], inp["w2"],
+                                  inp["w2s"], inp["sel"], inp["probs"], wl.E, wl.W)
+    assert np.array_equal(to_np(b.h)[:512].astype(np.int64), ref["acc1"])
+    _check_block(wl, inp)
+
+
+def test_int8_most_experts_empty(pairing):
+    wl = Workload("i8_sparse", 300, 256, 128, 16, 2, 2, "i8")
+    _check_block(wl, _with_sel(wl, np.stack([np.full(300, 3), np.full(300, 12)], axis=1), 4))
+
+
+def test_int8_invalid_ids_are_flagged_and_skipped():
+    wl = Workload("i8_bad_ids", 64, 256, 128, 8, 2, 2, "i8")
+    sel = make_inputs(wl, 6)["sel"].copy()
+    sel[3, 0], sel[17, 1], sel[40, 0] = 8, -1, 1000
+    _check_block(wl, _with_sel(wl, sel, 6), expect_bad=True)
+
+
+def test_int8_empty_input():
+    wl = Workload("i8_empty", 0, 256, 128, 8, 2, 2, "i8")
+    d, b = _run(wl, make_inputs(wl, 0), out="bf16")
+    assert to_np(b.cnt).sum() == 0 and to_np(b.offsets).sum() == 0
     assert int(b.dev_status.item()) == 0
 
 
