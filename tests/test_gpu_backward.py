@@ -121,6 +121,16 @@ def test_backward_invalid_ids_and_empty_experts():
         _tol(got[name], ref[name], name)
 
 
+def test_backward_empty_batch():
+    """No tokens: every expert's weight gradients are written as zeros (the
+    outputs start uninitialised) and nothing is flagged."""
+    wl = Workload("bwd_empty", 0, 256, 128, 8, 2, 2, "bf16")
+    got, status, _, _ = gpu_backward(wl, seed=0)
+    assert status == 0
+    assert got["dw1"].shape == (8, 256, 256) and not got["dw1"].any()
+    assert got["dw2"].shape == (8, 128, 256) and not got["dw2"].any()
+
+
 def test_backward_with_kept_pre_activation_is_bitwise_the_recompute():
     wl = BWD[3]
     got_r, _, st_r = run_backward(wl, seed=4)
