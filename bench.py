@@ -454,6 +454,8 @@ def run_cuda_workload(args, wl, headline):
         "data": "synthetic", "config": _config(wl, l2="flushed (256 MB write) between steps"),
         "tflops": tflops, "tflops_frac_of_peak": tflops / peak,
         "segments_ms": {name: float(seg[:, i].mean()) for name, i in segi.items()},
+        "step_ms_median": float(np.median(seg.sum(axis=1))),
+        "segments_ms_median": {name: float(np.median(seg[:, i])) for name, i in segi.items()},
         "roofline": {"kernel": ("gmm_kernel<fc1 rows> (fc1 + SwiGLU on materialised rows)"
                                 if unfused else
                                 "gmm_qw_kernel<fc1> (permute gather + exact int8 fc1 + dequant + "
