@@ -8,7 +8,8 @@
  * unpermute.  Here the W expert-parallel ranks are logical: rank r owns tokens
  * [r*T/W, (r+1)*T/W) and experts [r*E/W, (r+1)*E/W) of one GPU, so the two
  * AllToAllv exchanges become a row gather folded into the fc1 operand load
- * and a scatter/sum folded into the fc2 epilogue.  The int8 variant uses the
+ * and an ordered per-token sum of the fc2 rows (a separate pass by default,
+ * inside the fc2 kernel when selected).  The int8 variant uses the
  * dequantisation of "torch_npu.npu_mm_reduce_scatter_base" (Ascend op-plugin
  * docs), section "Function description": (x1_scale * x2_scale) * (x1 @ x2),
  * with no bias.
@@ -286,7 +287,7 @@ mc2_status_t mc2_mm_reduce_scatter_i8(const mc2_mmrs_shape_t* s, const int8_t* x
  * and before any act=I8 mc2_alltoallv_gmm / mc2_gmm_alltoallv / mc2_moe_forward
  * that uses this workspace.  w1/w2 passed to those calls must be the same
  * tensors.  The int8 path requires H <= 4096 and I <= 4096 (K is summed in
- * exact chunks of 1024 in at most four TMEM accumulators).
+ * at most four exact chunks of 1024).
  */
 mc2_status_t mc2_prepack_weights(const mc2_shape_t* s, const void* w1, const void* w2, void* ws,
                                  void* stream);
