@@ -51,3 +51,22 @@ def run_gpu(wl, seed=0, inputs=None, segments=False, out=None):
         blk.run_block(wl, d, b, out=out)
     torch.cuda.synchronize()
     return inp, d, b
+
+
+def random_shapes(seed, n, act):
+    """n seeded random block shapes within the library's rules: W in {1, 2, 4},
+    E a multiple of W up to 16 W, k up to min(E, 8), T a multiple of W up to
+    150 W, H and I multiples of 64 (64..512, 64..384) -- ragged tiles in every
+    dimension and expert counts that are not powers of two."""
+    from moe_expert_dispatch_histc_gb300.workloads import Workload
+    rng = np.random.default_rng(seed)
+    shapes = []
+    for i in range(n):
+        W = int(rng.choice([1, 2, 4]))
+        E = W * int(rng.integers(1, 17))
+        k = int(rng.integers(1, min(E, 8) + 1))
+        T = W * int(rng.integers(1, 151))
+        H = 64 * int(rng.integers(1, 9))
+        I = 64 * int(rng.integers(1, 7))
+        shapes.append(Workload(f"rand{i}_T{T}_H{H}_I{I}_E{E}_k{k}_W{W}", T, H, I, E, k, W, act))
+    return shapes

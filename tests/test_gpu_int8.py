@@ -17,7 +17,7 @@ from moe_expert_dispatch_histc_gb300 import binding as B
 from moe_expert_dispatch_histc_gb300 import block as blk
 from moe_expert_dispatch_histc_gb300.workloads import WORKLOADS, Workload, make_inputs
 
-from gpu_util import ensure_built, to_np
+from gpu_util import ensure_built, random_shapes, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -150,6 +150,19 @@ def _check_block(wl, inp, expect_bad=False):
 @pytest.mark.parametrize("wl", SMALL_I8, ids=lambda w: w.name)
 def test_int8_block_parity(wl, pairing):
     _check_block(wl, make_inputs(wl, 8))
+
+
+@pytest.mark.parametrize("wl", random_shapes(202, 10, "i8"), ids=lambda w: w.name)
+def test_int8_random_shapes(wl, pairing):
+    """Seeded random shapes on every int8 tiling: fc1's int32 accumulators
+    bit-exact, then the whole block against the oracle."""
+    inp = make_inputs(wl, 5)
+    d, b = _run(wl, inp, out="i32")
+    ref = orc.quant_block_forward(inp["x"], inp["xs"], inp["w1"], inp["w1s"], inp["w2"],
+                                  inp["w2s"], inp["sel"], inp["probs"], wl.E, wl.W)
+    n = int(ref["offsets"][-1])
+    assert np.array_equal(to_np(b.h)[:n].astype(np.int64), ref["acc1"])
+    _check_block(wl, inp)
 
 
 def _with_sel(wl, sel, seed):

@@ -17,7 +17,7 @@ from moe_expert_dispatch_histc_gb300 import binding as B
 from moe_expert_dispatch_histc_gb300.workloads import (WORKLOADS, Workload, as_f64, make_inputs,
                                                        make_routing)
 
-from gpu_util import F64Experts, ensure_built, run_gpu, to_np
+from gpu_util import F64Experts, ensure_built, random_shapes, run_gpu, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -139,6 +139,23 @@ def test_block_parity_full(wl, pairing):
     nvalid = int(offsets[-1])
     _tol(to_np(b.h)[:nvalid], ref["h"], "h (fc1 + SwiGLU)")
     _tol(to_np(b.out), ref["out"], "out (fc2 + combine)")
+    assert int(b.dev_status.item()) == 0
+
+
+@pytest.mark.parametrize("wl", random_shapes(101, 10, "bf16") + random_shapes(102, 4, "f32"),
+                         ids=lambda w: w.name)
+def test_random_shapes_parity(wl, pairing):
+    """Seeded random shapes -- ragged tiles in every dimension, expert counts
+    that are not powers of two, top-k from 1 to 8, one to four logical ranks:
+    counts and indices bit-exact, h and out within the tolerance, on both
+    tilings."""
+    inp, d, b = run_gpu(wl, seed=3)
+    src, offsets = _counts_exact(wl, inp, b)
+    x, w1, w2 = (as_f64(inp[n], wl.act) for n in ("x", "w1", "w2"))
+    ref = orc.block_forward(x, w1, w2, inp["sel"], inp["probs"], wl.E, wl.W, h_dtype=H_DTYPE[wl.act])
+    nvalid = int(offsets[-1])
+    _tol(to_np(b.h)[:nvalid], ref["h"], f"{wl.name}: h")
+    _tol(to_np(b.out), ref["out"], f"{wl.name}: out")
     assert int(b.dev_status.item()) == 0
 
 
