@@ -16,7 +16,7 @@ from moe_expert_dispatch_histc_gb300.workloads import (WORKLOADS, Workload, as_f
                                                        bf16_bits_to_f32, f32_to_bf16_bits,
                                                        make_inputs)
 
-from gpu_util import ensure_built, to_np
+from gpu_util import ensure_built, random_shapes, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -103,6 +103,16 @@ def test_backward_parity_under_each_tiling(wl, mode):
     assert status == 0
     for name in ("dx", "dw1", "dw2", "dprobs"):
         _tol(got[name], ref[name], name)
+
+
+@pytest.mark.parametrize("wl", random_shapes(303, 6, "bf16"), ids=lambda w: w.name)
+def test_backward_random_shapes(wl):
+    """Seeded random shapes (ragged in every dimension, odd expert counts,
+    top-k 1 to 8): every gradient within the tolerance."""
+    got, ref, status = run_backward(wl, seed=7)
+    assert status == 0
+    for name in ("dx", "dw1", "dw2", "dprobs"):
+        _tol(got[name], ref[name], f"{wl.name}: {name}")
 
 
 def test_backward_invalid_ids_and_empty_experts():

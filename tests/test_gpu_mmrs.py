@@ -78,6 +78,24 @@ def test_mm_reduce_scatter_parity(W, m, k, n):
     _run(W, m, k, n, seed=W * 7 + k)
 
 
+def _random_mmrs_shapes(seed, n):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        W = int(rng.choice([1, 2, 3, 4, 8]))
+        out.append((W, W * int(rng.integers(1, 80)), 64 * int(rng.integers(1, 40)),
+                    64 * int(rng.integers(1, 10))))
+    return out
+
+
+@pytest.mark.parametrize("W,m,k,n", _random_mmrs_shapes(404, 8))
+def test_mm_reduce_scatter_random_shapes(W, m, k, n):
+    """Seeded random shapes (ragged row and column tiles, one to three K
+    chunks, odd rank counts): bitwise equal to the two-pass form, int32
+    partials exact, the result within the tolerance."""
+    _run(W, m, k, n, seed=m + k + n)
+
+
 @pytest.mark.parametrize("k", [2048, 4096])
 def test_mm_reduce_scatter_worst_case_accumulators(k):
     """Every product -127*127: |acc| = k * 127^2 > 2^24 per rank (33 M at
