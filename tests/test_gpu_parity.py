@@ -235,7 +235,8 @@ COMBINE_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("wl", COMBINE_SHAPES, ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", COMBINE_SHAPES + random_shapes(505, 6, "bf16"),
+                         ids=lambda w: w.name)
 def test_fused_combine_equals_separate_bitwise(wl, pairing):
     """The combine inside the fc2 kernel and the separate combine kernel sum
     the same products in the same slot order: bitwise the same output, also
