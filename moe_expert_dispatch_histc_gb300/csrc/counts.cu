@@ -441,11 +441,12 @@ static ClusterCountsPlan plan_cluster_counts(const mc2_shape_t& s, int ctas) {
 
 // Cluster size for R entries: ~2K entries per CTA (each warp walks its chunk
 // serially, so spreading over SMs shortens the pass), at most 16 CTAs, and no
-// more than the GPU can co-schedule (checked once per size).
+// more than the GPU can co-schedule (checked once per size and device).
 static int cluster_counts_ctas(int64_t R) {
-  static std::once_flag once;
-  static bool fits[kClusterCountsMaxCtas + 1] = {};
-  std::call_once(once, [] {
+  struct Fits { bool at[kClusterCountsMaxCtas + 1]; };
+  static PerDevice<Fits> setup;
+  const Fits fits = once_per_device(setup, [] {
+    Fits r = {};
     cudaFuncSetAttribute(counts_cluster, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaFuncSetAttribute(counts_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
     for (int c = 1; c <= kClusterCountsMaxCtas; c *= 2) {
@@ -461,14 +462,15 @@ static int cluster_counts_ctas(int64_t R) {
       cfg.attrs = &attr;
       cfg.numAttrs = 1;
       int n = 0;
-      fits[c] = cudaOccupancyMaxActiveClusters(&n, counts_cluster, &cfg) == cudaSuccess && n >= 1;
+      r.at[c] = cudaOccupancyMaxActiveClusters(&n, counts_cluster, &cfg) == cudaSuccess && n >= 1;
     }
     cudaGetLastError();  // clear anything the queries left
+    return r;
   });
   int c = 1;
   while (c < kClusterCountsMaxCtas && static_cast<int64_t>(c) * 2048 < R) c *= 2;
-  while (c > 1 && !fits[c]) c /= 2;
-  return fits[c] ? c : 0;
+  while (c > 1 && !fits.at[c]) c /= 2;
+  return fits.at[c] ? c : 0;
 }
 
 static cudaError_t launch_counts_cluster(const mc2_shape_t& s, const ClusterCountsPlan& pl,

@@ -1367,14 +1367,12 @@ static cudaError_t launch_one(const GemmArgs& g, cudaStream_t st) {
   if (!ok) return cudaErrorInvalidValue;
   constexpr size_t fixed = SMEM_BYTES_FIXED + kQueueBytes<MODE>;
   const size_t smem = fixed + (s.E + 1) * sizeof(int32_t);
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(gmm_kernel<MODE, ES>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(fixed + 1025 * sizeof(int32_t)));
+  static PerDevice<KernelSetup> setup;
+  const KernelSetup su = once_per_device(setup, [] {
+    return setup_kernel(gmm_kernel<MODE, ES>, fixed + 1025 * sizeof(int32_t),
+                        Roles<MODE>::kThreads, false);
   });
-  if (attr_err != cudaSuccess) return attr_err;
+  if (su.err != cudaSuccess) return su.err;
   const int64_t tiles_upper = (R / BM + s.E) * static_cast<int64_t>(p.n_tiles);
   const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_upper, 1)));
   return launch_kernel(gmm_kernel<MODE, ES>, dim3(grid), dim3(Roles<MODE>::kThreads), smem,
@@ -1431,36 +1429,16 @@ static cudaError_t launch_pair(const GemmArgs& g, cudaStream_t st) {
   if (!ok) return cudaErrorInvalidValue;
   constexpr size_t fixed = P_SMEM_BYTES_FIXED + kQueueBytes<MODE>;
   const size_t smem = fixed + (s.E + 1) * sizeof(int32_t);
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(gmm_pair_kernel<MODE, ES>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(fixed + 1025 * sizeof(int32_t)));
+  static PerDevice<KernelSetup> setup;
+  const KernelSetup su = once_per_device(setup, [] {
+    return setup_kernel(gmm_pair_kernel<MODE, ES>, fixed + 1025 * sizeof(int32_t),
+                        Roles<MODE>::kThreads, true);
   });
-  if (attr_err != cudaSuccess) return attr_err;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(Roles<MODE>::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  if (su.err != cudaSuccess) return su.err;
   // Persistent grid: exactly as many pairs as can be resident at once.  A
   // pair needs two SMs of one GPC, so this can be fewer than SMs / 2; any
   // cluster beyond it would run its whole tile list as a second wave.
-  static std::once_flag once_clusters;
-  static int max_clusters = 0;
-  std::call_once(once_clusters, [&] {
-    cfg.gridDim = dim3(num_sms() & ~1, 1, 1);
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, gmm_pair_kernel<MODE, ES>, &cfg) !=
-        cudaSuccess)
-      max_clusters = 0;
-  });
+  const int max_clusters = su.pair_clusters;
   if (max_clusters < 1) return cudaErrorInvalidConfiguration;
   const int64_t pair_tiles_upper = (R / (2 * BM) + s.E) * static_cast<int64_t>(p.n_tiles);
   const int grid = 2 * static_cast<int>(std::min<int64_t>(max_clusters,

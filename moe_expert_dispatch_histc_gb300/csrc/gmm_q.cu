@@ -1179,30 +1179,13 @@ static cudaError_t launch_q(const QArgs& g, cudaStream_t st) {
   if (p.nchunk > QMAX_CHUNKS) return cudaErrorInvalidValue;
   using G = QGeom<PAIR>;
   const size_t smem = G::kSmemFixed + (s.E + 1) * sizeof(int32_t);
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  static int max_clusters = 0;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(gmm_q_kernel<MODE, PAIR>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(G::kSmemFixed + 1025 * sizeof(int32_t)));
-    if (attr_err != cudaSuccess || !PAIR) return;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(num_sms() & ~1, 1, 1);
-    cfg.blockDim = dim3(QRoles<MODE>::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = G::kSmemFixed + 1025 * sizeof(int32_t);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, gmm_q_kernel<MODE, PAIR>, &cfg) !=
-        cudaSuccess)
-      max_clusters = 0;
+  static PerDevice<KernelSetup> setup;
+  const KernelSetup su = once_per_device(setup, [] {
+    return setup_kernel(gmm_q_kernel<MODE, PAIR>, G::kSmemFixed + 1025 * sizeof(int32_t),
+                        QRoles<MODE>::kThreads, PAIR);
   });
-  if (attr_err != cudaSuccess) return attr_err;
+  if (su.err != cudaSuccess) return su.err;
+  const int max_clusters = su.pair_clusters;
   if (PAIR) {  // persistent grid: as many pairs as can be resident at once
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
     const int64_t tiles_upper = (R / (2 * BM) + s.E) * static_cast<int64_t>(p.n_tiles);
@@ -1258,13 +1241,12 @@ static cudaError_t launch_qw(const QArgs& g, cudaStream_t st) {
   p.nchunk = (p.K / 64 + QCHUNK_KB - 1) / QCHUNK_KB;
   if (p.nchunk > QMAX_CHUNKS) return cudaErrorInvalidValue;
   const size_t smem = QW_SMEM_FIXED + (s.E + 1) * sizeof(int32_t);
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(gmm_qw_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(QW_SMEM_FIXED + 1025 * sizeof(int32_t)));
+  static PerDevice<KernelSetup> setup;
+  const KernelSetup su = once_per_device(setup, [] {
+    return setup_kernel(gmm_qw_kernel<MODE>, QW_SMEM_FIXED + 1025 * sizeof(int32_t),
+                        QRoles<MODE>::kThreads, false);
   });
-  if (attr_err != cudaSuccess) return attr_err;
+  if (su.err != cudaSuccess) return su.err;
   const int64_t tiles_upper = (R / BM + s.E) * static_cast<int64_t>(p.n_tiles);
   const int grid = static_cast<int>(std::min<int64_t>(num_sms(), std::max<int64_t>(tiles_upper, 1)));
   return launch_kernel(gmm_qw_kernel<MODE>, dim3(grid), dim3(QRoles<MODE>::kThreads), smem, st, 1,

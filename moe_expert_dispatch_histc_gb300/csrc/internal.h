@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <initializer_list>
+#include <mutex>
 
 #include <utility>
 
@@ -174,5 +175,58 @@ cudaError_t launch_transpose_round_tf32(const float* src, float* dst, int batch,
 cudaError_t launch_selftest_wait(uint64_t limit_ns, int32_t* dev_status, cudaStream_t st);
 
 int num_sms();
+
+// Host set-up that belongs to a device (kernel attributes, occupancy
+// results): f() runs once for each device that is current at a call, and
+// its result is kept per device, so a process that drives several GPUs sets
+// each one up.
+template <class T>
+struct PerDevice {
+  std::mutex m;
+  uint64_t done = 0;
+  T val[64] = {};
+};
+
+template <class T, class F>
+T once_per_device(PerDevice<T>& o, F&& f) {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return f();
+  std::lock_guard<std::mutex> lk(o.m);
+  if (!((o.done >> d) & 1u)) {
+    o.val[d] = f();
+    o.done |= uint64_t(1) << d;
+  }
+  return o.val[d];
+}
+
+// What a launcher needs to know once per device: whether the kernel accepted
+// its shared-memory size, and (for kernels launched as CTA pairs) how many
+// 2-CTA clusters of `threads` threads fit at once with `smem` bytes each.
+struct KernelSetup {
+  cudaError_t err;
+  int pair_clusters;
+};
+
+template <typename... KArgs>
+KernelSetup setup_kernel(void (*kernel)(KArgs...), size_t smem, int threads, bool pairs) {
+  KernelSetup r{cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem)),
+                0};
+  if (r.err != cudaSuccess || !pairs) return r;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms() & ~1), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaOccupancyMaxActiveClusters(&r.pair_clusters, kernel, &cfg) != cudaSuccess)
+    r.pair_clusters = 0;
+  return r;
+}
 
 }  // namespace mc2

@@ -484,30 +484,11 @@ cudaError_t launch_fused(const CUtensorMap& tA, const CUtensorMap& tB, const CUt
   p.total = p.m_tiles * p.n_tiles;
   // Persistent grid: as many pairs as can be resident at once (a pair needs
   // two SMs of one GPC, so this can be fewer than SMs / 2).
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  static int max_clusters = 0;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(mmrs_fused_kernel<NB>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(C::kSmem));
-    if (attr_err != cudaSuccess) return;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(num_sms() & ~1, 1, 1);
-    cfg.blockDim = dim3(C::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = C::kSmem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, mmrs_fused_kernel<NB>, &cfg) !=
-        cudaSuccess)
-      max_clusters = 0;
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  static PerDevice<KernelSetup> setup;
+  const KernelSetup su = once_per_device(
+      setup, [] { return setup_kernel(mmrs_fused_kernel<NB>, C::kSmem, C::kThreads, true); });
+  if (su.err != cudaSuccess) return su.err;
+  const int max_clusters = su.pair_clusters;
   if (max_clusters < 1) return cudaErrorInvalidConfiguration;
   const int grid = 2 * std::min(max_clusters, std::max(p.total, 1));
   return launch_kernel(mmrs_fused_kernel<NB>, dim3(grid), dim3(C::kThreads), C::kSmem, st, 2, tA,

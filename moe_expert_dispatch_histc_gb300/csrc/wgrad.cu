@@ -284,13 +284,10 @@ cudaError_t launch_wgrad(const void* a, const void* b, const int32_t* offsets, i
   p.mt = (M + WG_BM - 1) / WG_BM;
   p.nt = (N + WG_BN - 1) / WG_BN;
   p.wait_limit_ns = wait_limit_ns();
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(WG_SMEM));
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  static PerDevice<KernelSetup> setup;
+  const KernelSetup su =
+      once_per_device(setup, [] { return setup_kernel(wgrad_kernel, WG_SMEM, WG_THREADS, false); });
+  if (su.err != cudaSuccess) return su.err;
   const int64_t tiles = static_cast<int64_t>(E) * p.mt * p.nt;
   const int grid = static_cast<int>(std::min<int64_t>(num_sms(), tiles));
   const cudaError_t e = launch_kernel(wgrad_kernel, dim3(grid), dim3(WG_THREADS), WG_SMEM, st, 1,
