@@ -612,7 +612,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
             continue;
           }
           if (!kIsFc2<MODE> && ES == 2) {
-#pragma unroll
+#pragma unroll 1
             for (int half = 0; half < 2; ++half) {
               uint32_t g[32], u[32];
               const int c = gi * 64 + half * 32;
@@ -1064,7 +1064,7 @@ __global__ void __launch_bounds__(Roles<MODE>::kThreads, 1)
           const int col0 = n * (!kIsFc2<MODE> ? BN / 2 : BN) + gi * GROUP_COLS;
           if (col0 >= p.out_cols) break;
           if (!kIsFc2<MODE> && ES == 2) {
-#pragma unroll
+#pragma unroll 1
             for (int half = 0; half < 2; ++half) {
               uint32_t g[32], u[32];
               const int c = gi * 64 + half * 32;
