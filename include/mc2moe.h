@@ -359,6 +359,21 @@ void mc2_set_mmrs_path(int32_t mode);
  * the same order: the outputs are identical bit for bit.  Host only. */
 void mc2_set_combine_path(int32_t mode);
 
+/* Timing of a grouped-matmul kernel alone (a diagnostic hook).  While set,
+ * every later call of this thread that launches an fc1 or fc2 kernel
+ * (mc2_alltoallv_gmm, mc2_gmm_alltoallv, mc2_gmm_swiglu, mc2_moe_forward)
+ * records `before` on its stream right before that kernel's launch and
+ * `after` right after it, so the time between the two events is that
+ * kernel's.  A call with two such kernels (mc2_moe_forward) records both
+ * events twice; the second pair, around fc2, is what remains.  The bf16 fc1
+ * call launches only its kernel; the int8 calls also convert their
+ * activations to bf16 before it and re-quantise h or combine after it.
+ * The handles are cudaEvent_t created by the caller on the stream's device
+ * (the library does not own them); either may be NULL (that event is not
+ * recorded), and both NULL, the default, records nothing.  A failed record
+ * returns MC2_ERR_CUDA.  Results are identical either way.  Host only. */
+void mc2_set_gemm_events(void* before, void* after);
+
 /* Programmatic dependent launch between the kernels of later calls of this
  * thread: 1 (default) lets each kernel's set-up overlap the end of the
  * previous kernel on the stream (each kernel still waits for its

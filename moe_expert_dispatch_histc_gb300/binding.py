@@ -66,6 +66,7 @@ _SIGS = {
     "mc2_set_counts_path": (None, [ctypes.c_int32]),
     "mc2_set_mmrs_path": (None, [ctypes.c_int32]),
     "mc2_set_combine_path": (None, [ctypes.c_int32]),
+    "mc2_set_gemm_events": (None, [ctypes.c_void_p, ctypes.c_void_p]),
     "mc2_last_launch_count": (ctypes.c_int32, []),
     "mc2_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -289,6 +290,15 @@ def mc2_set_mmrs_path(mode: int) -> None:
 def mc2_set_combine_path(mode: int) -> None:
     """0: the weighted combine in its own kernel (default); 1: inside the fc2 kernel."""
     lib().mc2_set_combine_path(int(mode))
+
+
+def mc2_set_gemm_events(before, after) -> None:
+    """CUDA events recorded around the fc1 / fc2 kernel of later calls of this
+    thread (torch.cuda.Event objects, already recorded once so that they exist,
+    or None); mc2_set_gemm_events(None, None) stops it."""
+    def handle(ev):
+        return None if ev is None else ctypes.c_void_p(int(ev.cuda_event))
+    lib().mc2_set_gemm_events(handle(before), handle(after))
 
 
 def mc2_last_launch_count() -> int:

@@ -19,6 +19,21 @@ static thread_local int tl_counts_path = 0;
 static thread_local int tl_mmrs_path = 0;
 static thread_local int tl_combine_path = 0;
 static thread_local int tl_launches = 0;
+static thread_local cudaEvent_t tl_gemm_before = nullptr;  // mc2_set_gemm_events
+static thread_local cudaEvent_t tl_gemm_after = nullptr;
+
+// Launch a call's grouped-matmul kernel, with the timing events of
+// mc2_set_gemm_events recorded on its stream right before and after it.
+template <class F>
+static cudaError_t timed_gemm(cudaStream_t st, F&& launch) {
+  if (tl_gemm_before) {
+    const cudaError_t e = cudaEventRecord(tl_gemm_before, st);
+    if (e != cudaSuccess) return e;
+  }
+  const cudaError_t e = launch();
+  if (e != cudaSuccess || !tl_gemm_after) return e;
+  return cudaEventRecord(tl_gemm_after, st);
+}
 
 uint64_t wait_limit_ns() { return tl_wait_limit_ns ? tl_wait_limit_ns : 2000000000ull; }  // 2 s
 
@@ -133,7 +148,7 @@ mc2_status_t do_fc1_i8(const mc2_shape_t* s, const void* x, const float* x_scale
   q.dev_status = dev_status;
   q.mode = 0;
   q.raw = raw;
-  cudaError_t e = launch_gemm_q(q, st);
+  cudaError_t e = timed_gemm(st, [&] { return launch_gemm_q(q, st); });
   if (e == cudaSuccess && !raw)
     e = launch_requant(reinterpret_cast<const float*>(w + L.h_f32), offsets, *s,
                        static_cast<int8_t*>(h), h_scale, st);
@@ -172,7 +187,7 @@ mc2_status_t do_fc2_i8(const mc2_shape_t* s, const void* h, const float* h_scale
   q.dev_status = dev_status;
   q.mode = 1;
   q.raw = raw;
-  cudaError_t e = launch_gemm_q(q, st);
+  cudaError_t e = timed_gemm(st, [&] { return launch_gemm_q(q, st); });
   if (e == cudaSuccess && !raw)
     e = launch_combine(*s, w + L.y, reinterpret_cast<const float*>(w + L.yscale), probs, offsets,
                        unpermute_dst, out, MC2_BF16, st);
@@ -218,7 +233,7 @@ mc2_status_t do_fc1(const mc2_shape_t* s, const void* x, const float* x_scale, c
     g.b = w1;
     g.a_elem_bytes = 2;
   }
-  return cuda_status(launch_gemm(g, st));
+  return cuda_status(timed_gemm(st, [&] { return launch_gemm(g, st); }));
 }
 
 mc2_status_t do_fc2(const mc2_shape_t* s, const void* h, const float* h_scale, const void* w2,
@@ -273,9 +288,9 @@ mc2_status_t do_fc2(const mc2_shape_t* s, const void* h, const float* h_scale, c
     g.defer_items = reinterpret_cast<int32_t*>(w + L.defer + 16);
     g.comb_out = out;
     g.out_dtype = s->out;
-    return cuda_status(launch_gemm(g, st));
+    return cuda_status(timed_gemm(st, [&] { return launch_gemm(g, st); }));
   }
-  cudaError_t e = launch_gemm(g, st);
+  cudaError_t e = timed_gemm(st, [&] { return launch_gemm(g, st); });
   if (e == cudaSuccess)
     e = launch_combine(*s, y, yscale, probs, offsets, unpermute_dst, out, s->out, st);
   return cuda_status(e);
@@ -378,7 +393,8 @@ mc2_status_t mc2_gmm_swiglu(const mc2_shape_t* s, const void* xp, const void* w1
   g.dev_status = dev_status;
   g.mode = MODE_FC1_ROWS;
   g.a_elem_bytes = 2;
-  return cuda_status(launch_gemm(g, static_cast<cudaStream_t>(stream)));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return cuda_status(timed_gemm(st, [&] { return launch_gemm(g, st); }));
 }
 
 mc2_status_t mc2_prepack_weights(const mc2_shape_t* s, const void* w1, const void* w2, void* ws,
@@ -414,6 +430,11 @@ void mc2_set_counts_path(int32_t mode) { tl_counts_path = mode == 1 || mode == 2
 void mc2_set_mmrs_path(int32_t mode) { tl_mmrs_path = mode == 1 ? 1 : 0; }
 
 void mc2_set_combine_path(int32_t mode) { tl_combine_path = mode == 1 ? 1 : 0; }
+
+void mc2_set_gemm_events(void* before, void* after) {
+  tl_gemm_before = static_cast<cudaEvent_t>(before);
+  tl_gemm_after = static_cast<cudaEvent_t>(after);
+}
 
 int32_t mc2_last_launch_count(void) { return tl_launches; }
 

@@ -54,7 +54,8 @@ def test_cuda_arm_line():
     assert "impl" not in d and d["config"]["workload"] == "tiny"
     rf = d["roofline"]
     assert rf["bound"] in ("hbm", "tensor") and rf["unit"] in ("GB/s", "TFLOP/s")
-    assert rf["achieved"] > 0 and rf["peak"] > 0
+    assert rf["achieved"] > 0 and rf["peak"] > 0 and rf["kernel_ms"] > 0
+    assert rf["kernel_ms"] <= d["segments_ms"]["fc1_swiglu"] * 1.05
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
     assert rf["traffic"] is None or rf["traffic"] > 0
     e2e = d["e2e"]

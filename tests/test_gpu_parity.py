@@ -166,6 +166,45 @@ def test_segments_equal_single_call(wl):
     assert torch.equal(b1.out, b2.out) and torch.equal(b1.h, b2.h)
 
 
+@pytest.mark.parametrize("wl", [SMALL[1], Workload("i8_events", 512, 256, 128, 8, 2, 2, "i8")],
+                         ids=lambda w: w.name)
+def test_gemm_events_bracket_the_fc1_kernel(wl):
+    """mc2_set_gemm_events (how the benchmark times the fc1 kernel alone): the
+    two events land around the kernel, inside the fc1 call's own span, and
+    the results are bitwise those of a run without them."""
+    from moe_expert_dispatch_histc_gb300 import block as blk
+    ensure_built()
+    inp = make_inputs(wl, 6)
+    d = blk.inputs_to_device(inp, wl)
+    b = blk.alloc_buffers(wl)
+    blk.prepack(wl, d, b)
+    shape = blk.shape_of(wl)
+    st = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in ev[1:3]:  # a first record creates the CUDA events
+        e.record(st)
+    B.mc2_moe_counts(shape, d["sel"], b.cnt, b.recv, b.offsets, b.permute_src, b.unpermute_dst,
+                     b.ws, b.dev_status)
+    ev[0].record(st)
+    B.mc2_set_gemm_events(ev[1], ev[2])
+    try:
+        B.mc2_alltoallv_gmm(shape, d["x"], d["xs"], d["w1"], d["w1s"], b.offsets, b.permute_src,
+                            b.ws, b.h, b.h_scale, b.dev_status)
+    finally:
+        B.mc2_set_gemm_events(None, None)
+    ev[3].record(st)
+    B.mc2_gmm_alltoallv(shape, b.h, b.h_scale, d["w2"], d["w2s"], b.offsets, b.permute_src,
+                        b.unpermute_dst, d["probs"], b.ws, b.out, b.dev_status)
+    torch.cuda.synchronize()
+    kernel_ms, call_ms = ev[1].elapsed_time(ev[2]), ev[0].elapsed_time(ev[3])
+    assert 0 < kernel_ms <= call_ms
+    assert ev[0].elapsed_time(ev[1]) >= 0 and ev[2].elapsed_time(ev[3]) >= 0
+    _, _, b0 = run_gpu(wl, seed=6)
+    assert torch.equal(b0.h.view(torch.uint8), b.h.view(torch.uint8))
+    assert torch.equal(b0.out.view(torch.uint8), b.out.view(torch.uint8))
+    assert int(b.dev_status.item()) == 0
+
+
 def test_fc2_alone_on_oracle_h():
     """fc2 + combine fed the oracle's h: isolates the combine segment."""
     wl = SMALL[1]
