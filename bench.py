@@ -594,11 +594,13 @@ def run_backward(args):
     peaks, src = _peaks()
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (ms / 1e3) / 1e12
-    # end to end: x, ids, probs and dout in from pinned host memory; dx, dprobs,
-    # dw1, dw2 back, every step (counts included: the ids arrive with the step)
+    # end to end: x, ids, probs and dout in from pinned host memory, every step
+    # (counts included: the ids arrive with the step); the gradients that leave
+    # the block towards the layers before it, dx and dprobs, back to the host.
+    # dw1 and dw2 stay on the device, where an optimizer step consumes them.
     host = {n: d[n].cpu().pin_memory() for n in ("x", "sel", "probs")}
     h_dout = dout.cpu().pin_memory()
-    outs = [dx, dprobs, dw1, dw2]
+    outs = [dx, dprobs]
     h_outs = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
     e2e_steps = max(3, args.steps // 4)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -640,7 +642,8 @@ def run_backward(args):
                      "peak_source": f"{src} bf16_tflops (burst)", "traffic": None},
         "e2e": {"value": wl.T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo, "steps": e2e_steps,
-                "mode": "inputs and dout in, counts + backward, dx/dprobs/dw1/dw2 out, serially"},
+                "mode": "inputs and dout in, counts + backward, dx and dprobs out (dw1, dw2 "
+                        "stay on the device), serially"},
         "cpu_baseline": {"value": Ts / cpu_s, "unit": "tokens/s", "cores": os.cpu_count(),
                          "kind": "oracle",
                          "sample": f"first {Ts} of {wl.T} tokens, all experts (numpy float64 "
