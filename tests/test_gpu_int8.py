@@ -184,6 +184,12 @@ def test_int8_all_tokens_to_one_expert(pairing):
     _check_block(wl, inp)
 
 
+def test_int8_large_topk(pairing):
+    """Twelve slots per token (the combine's generic loop) on sixteen experts."""
+    wl = Workload("i8_k12", 96, 256, 128, 16, 12, 4, "i8")
+    _check_block(wl, make_inputs(wl, 9))
+
+
 def test_int8_most_experts_empty(pairing):
     wl = Workload("i8_sparse", 300, 256, 128, 16, 2, 2, "i8")
     _check_block(wl, _with_sel(wl, np.stack([np.full(300, 3), np.full(300, 12)], axis=1), 4))

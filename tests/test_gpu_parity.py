@@ -142,6 +142,29 @@ def test_block_parity_full(wl, pairing):
     assert int(b.dev_status.item()) == 0
 
 
+LARGE_K = [
+    Workload("k10", 128, 192, 64, 16, 10, 4, "bf16"),        # top-k past the combine's unrolled forms
+    Workload("k_eq_E12", 96, 128, 128, 12, 12, 3, "bf16"),   # every token on every expert
+    Workload("k40_f32", 64, 128, 64, 64, 40, 4, "f32"),      # 40 slots per token
+]
+
+
+@pytest.mark.parametrize("wl", LARGE_K, ids=lambda w: w.name)
+def test_large_topk_parity(wl, pairing):
+    """Top-k beyond 8 (the combine's generic loop, many slots per token in
+    the counts and the gather) and k = E: counts and indices bit-exact, h and
+    out within the tolerance, on both tilings."""
+    inp, d, b = run_gpu(wl, seed=11)
+    src, offsets = _counts_exact(wl, inp, b)
+    x, w1, w2 = (as_f64(inp[n], wl.act) for n in ("x", "w1", "w2"))
+    ref = orc.block_forward(x, w1, w2, inp["sel"], inp["probs"], wl.E, wl.W, h_dtype=H_DTYPE[wl.act])
+    nvalid = int(offsets[-1])
+    assert nvalid == wl.R
+    _tol(to_np(b.h)[:nvalid], ref["h"], f"{wl.name}: h")
+    _tol(to_np(b.out), ref["out"], f"{wl.name}: out")
+    assert int(b.dev_status.item()) == 0
+
+
 @pytest.mark.parametrize("wl", random_shapes(101, 10, "bf16") + random_shapes(102, 4, "f32"),
                          ids=lambda w: w.name)
 def test_random_shapes_parity(wl, pairing):
