@@ -142,6 +142,14 @@ def test_block_parity_full(wl, pairing):
     assert int(b.dev_status.item()) == 0
 
 
+# Degenerate forms of the method: one expert (the block is a dense SwiGLU
+# MLP), one expert per logical rank, one token per logical rank.
+DEGENERATE = [
+    Workload("single_expert", 256, 128, 64, 1, 1, 1, "bf16"),
+    Workload("one_expert_per_rank", 128, 128, 64, 4, 2, 4, "bf16"),
+    Workload("one_token_per_rank", 4, 128, 64, 8, 2, 4, "bf16"),
+]
+
 LARGE_K = [
     Workload("k10", 128, 192, 64, 16, 10, 4, "bf16"),        # top-k past the combine's unrolled forms
     Workload("k_eq_E12", 96, 128, 128, 12, 12, 3, "bf16"),   # every token on every expert
@@ -149,11 +157,11 @@ LARGE_K = [
 ]
 
 
-@pytest.mark.parametrize("wl", LARGE_K, ids=lambda w: w.name)
-def test_large_topk_parity(wl, pairing):
+@pytest.mark.parametrize("wl", LARGE_K + DEGENERATE, ids=lambda w: w.name)
+def test_large_topk_and_degenerate_parity(wl, pairing):
     """Top-k beyond 8 (the combine's generic loop, many slots per token in
-    the counts and the gather) and k = E: counts and indices bit-exact, h and
-    out within the tolerance, on both tilings."""
+    the counts and the gather), k = E, and the degenerate shapes: counts and
+    indices bit-exact, h and out within the tolerance, on both tilings."""
     inp, d, b = run_gpu(wl, seed=11)
     src, offsets = _counts_exact(wl, inp, b)
     x, w1, w2 = (as_f64(inp[n], wl.act) for n in ("x", "w1", "w2"))
