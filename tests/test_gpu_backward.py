@@ -115,6 +115,20 @@ def test_backward_random_shapes(wl):
         _tol(got[name], ref[name], f"{wl.name}: {name}")
 
 
+@pytest.mark.parametrize("wl", [
+    Workload("bwd_k10", 128, 192, 64, 16, 10, 4, "bf16"),           # top-k past 8
+    Workload("bwd_single_expert", 128, 128, 64, 1, 1, 1, "bf16"),   # a dense SwiGLU MLP
+    Workload("bwd_one_token_per_rank", 4, 128, 64, 8, 2, 4, "bf16"),
+], ids=lambda w: w.name)
+def test_backward_large_topk_and_degenerate(wl):
+    """Top-k beyond 8 (the dx sum's generic loop), one expert, one token per
+    logical rank: every gradient within the tolerance."""
+    got, ref, status = run_backward(wl, seed=8)
+    assert status == 0
+    for name in ("dx", "dw1", "dw2", "dprobs"):
+        _tol(got[name], ref[name], f"{wl.name}: {name}")
+
+
 def test_backward_invalid_ids_and_empty_experts():
     """Invalid slots get dprobs 0 and no gradient; experts without rows get zero
     weight gradients."""
