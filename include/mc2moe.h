@@ -365,7 +365,8 @@ void mc2_set_combine_path(int32_t mode);
  * records `before` on its stream right before that kernel's launch and
  * `after` right after it, so the time between the two events is that
  * kernel's.  A call with two such kernels (mc2_moe_forward) records both
- * events twice; the second pair, around fc2, is what remains.  The bf16 fc1
+ * events twice; the second pair, around fc2, is what remains.  A call that
+ * launches nothing (T = 0) records nothing.  The bf16 fc1
  * call launches only its kernel; the int8 calls also convert their
  * activations to bf16 before it and re-quantise h or combine after it.
  * The handles are cudaEvent_t created by the caller on the stream's device
