@@ -297,8 +297,14 @@ def mc2_set_gemm_events(before, after) -> None:
     thread (torch.cuda.Event objects, already recorded once so that they exist,
     or None); mc2_set_gemm_events(None, None) stops it."""
     def handle(ev):
-        return None if ev is None else ctypes.c_void_p(int(ev.cuda_event))
-    lib().mc2_set_gemm_events(handle(before), handle(after))
+        if ev is None:
+            return None
+        h = int(ev.cuda_event)
+        if h == 0:  # torch creates the CUDA event at its first record
+            raise ValueError("mc2_set_gemm_events: record the event once before passing it")
+        return ctypes.c_void_p(h)
+    hb, ha = handle(before), handle(after)
+    lib().mc2_set_gemm_events(hb, ha)
 
 
 def mc2_last_launch_count() -> int:

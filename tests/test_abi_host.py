@@ -197,6 +197,15 @@ def test_status_strings():
     assert B.status_str(B.MC2_OK) == "ok"
 
 
+def test_gemm_events_hook_rejects_events_that_do_not_exist_yet():
+    """torch creates a CUDA event at its first record; before that the
+    binding refuses it instead of passing a NULL handle.  None clears."""
+    import torch
+    with pytest.raises(ValueError):
+        B.mc2_set_gemm_events(torch.cuda.Event(enable_timing=True), None)
+    B.mc2_set_gemm_events(None, None)
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(B, "_lib", None)
     monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "missing.so"))
