@@ -1448,10 +1448,12 @@ static cudaError_t launch_pair(const GemmArgs& g, cudaStream_t st) {
 }
 
 // Automatic choice, from measurements on GB300 (4096- and 16384-token
-// workloads): CTA pairs win for fc2 when experts average >= 256 rows (fc2
-// 173 vs 185 us and 544 vs 593 us) and tie or lose for fc1 (205 vs 203 us,
-// 615 vs 600 us); with few rows per expert (decode-like batches) single CTAs
-// waste less tensor work on padding and are already bound by weight streaming.
+// workloads): CTA pairs win for fc2 when experts average >= 256 rows (fc2 +
+// combine 125 vs 135 us and 400 vs 430 us, although 256-row tiles pad a
+// fifth of the 4096-token rows against a ninth for 128-row tiles) and lose
+// for fc1 (206 vs 191 us, 617 vs 583 us); with few rows per expert
+// (decode-like batches) single CTAs waste less tensor work on padding and are
+// already bound by weight streaming.
 static bool use_pairs(const mc2_shape_t& s, int mode) {
   const int forced = tile_pairing_override();
   if (forced == 1) return false;
