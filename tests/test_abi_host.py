@@ -1,8 +1,6 @@
 """Host-side checks of the C ABI: the library loads, exports what the header
 declares, applies its argument rules and launches nothing on bad input.
 None of these calls reaches the GPU."""
-import ctypes
-
 import pytest
 
 from moe_expert_dispatch_histc_gb300 import binding as B

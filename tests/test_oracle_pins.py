@@ -16,7 +16,7 @@ import torch
 
 from oracle import mc2_oracle as orc
 from moe_expert_dispatch_histc_gb300.workloads import (
-    WORKLOADS, make_inputs, make_routing, as_f64)
+    WORKLOADS, make_inputs, as_f64)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 

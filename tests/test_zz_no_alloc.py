@@ -9,7 +9,6 @@ compare it with mc2_moe_counts on two calls in a row (different inputs, so
 the second call also shows that the first call's leftover scratch does not
 leak into the result).  The file is named to be collected last.
 """
-import numpy as np
 import pytest
 import torch
 
