@@ -19,16 +19,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-__device__ __forceinline__ uint32_t lane_id() {
-  uint32_t l;
-  asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
-  return l;
-}
-
-__device__ __forceinline__ bool elect_one() {  // lane 0 of a converged warp
-  return lane_id() == 0;
-}
-
 // ----------------------------------------------------------------------------
 // programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start while the previous kernel in the stream finishes;
@@ -257,21 +247,11 @@ __device__ __forceinline__ float ld_cg_f32(const float* p) {
   return v;
 }
 
-// Drop a 128-byte L2 line without writing it back: its contents become
-// undefined.  For intermediate data that no one reads again.
-__device__ __forceinline__ void discard_l2_line(const void* p) {
-  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
-}
-
 // ----------------------------------------------------------------------------
 // cp.async (16-byte, L2-cached) for row gathers the tensor maps cannot express
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
 // The mbarrier receives one (pre-counted) arrival once every cp.async this
@@ -424,12 +404,6 @@ __device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr)
   uint32_t v;
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
   return v;
-}
-
-// Arrive on an mbarrier of another CTA of the cluster (release, cluster scope).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
 }
 
 // Relaxed remote arrive: carries only the signal, no release fence.  Used to
