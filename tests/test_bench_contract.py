@@ -65,3 +65,23 @@ def test_cuda_arm_line():
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(clk)
     assert d["step_ms_median"] > 0 and set(d["segments_ms_median"]) == set(d["segments_ms"])
     assert d["counts"]["achieved_gbs"] > 0
+
+
+def test_traffic_lookup_follows_the_kernel_source(tmp_path, monkeypatch):
+    """roofline.traffic comes from a committed ncu figure only while the
+    kernel's source (comments and blank space aside) is the one it was
+    taken on; any other source gives null."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_text("// a comment\n__global__ void k() { int a = 1; }\n")
+    h = bench._src_hash(str(src))
+    (tmp_path / "traffic.json").write_text(json.dumps(
+        {"gmm_fc1:uniform": {"src_sha256_16": h, "dram_bytes_per_launch": 123}}))
+    monkeypatch.setattr(bench, "PROFILE_DIR", str(tmp_path))
+    assert bench._ncu_traffic("gmm_fc1", "uniform", str(src)) == 123
+    assert bench._ncu_traffic("gmm_fc1", "skew", str(src)) is None
+    src.write_text("/* another\n comment */\n\n    __global__ void k() { int a = 1; }  // end\n")
+    assert bench._ncu_traffic("gmm_fc1", "uniform", str(src)) == 123   # comments, blank space
+    src.write_text("__global__ void k() { int a = 2; }\n")
+    assert bench._ncu_traffic("gmm_fc1", "uniform", str(src)) is None  # the code changed
