@@ -13,17 +13,20 @@ checked to stay below 2**53, so they are exact (``exact_int_matmul``).
 Sources (page title, then section):
 
 [EP]  "NPU Training Operators - MC2" (shaojiemike.top), section "Execution
-      path" (执行路径): the ep_mc2_forward data flow --
-        1 hidden_states.view(-1, hidden_size)
-        2 num_local = torch.histc(selected_experts.view(-1), bins=E, min=0, max=E)
-        3 all_gather_into_tensor(num_global, num_local, group=ep_group)
-        4 send_counts = num_local
-        5 recv_counts = num_global[:, start_idx:end_idx].reshape(-1)
-        6 permute(hidden_states, selected_experts.to(int32), fused=True)
-        7 all2all_grouped_matmul(inputs, fc1_weight, ep_group, send_counts, recv_counts)
-        8 swiglu(intermediate_hidden_states, fused=True)
-        9 grouped_matmul_all2all(inputs, fc2_weight, ep_group, recv_counts, send_counts)
-       10 unpermute(hidden_states, unpermute_indices, probs=routing_weights, fused=True)
+      path" (执行路径): the data flow of ep_mc2_forward, which this file
+      enumerates in the page's order as
+        1 flatten the token rows to [T, H];
+        2 count each rank's (token, slot) pairs per expert with histc over E
+          bins on [0, E];
+        3 gather every rank's counts (all_gather over the EP group);
+        4 a rank sends its own counts;
+        5 it receives, from every source rank, the counts of its local
+          experts' column range;
+        6 permute the token rows by expert;
+        7 dispatch exchange fused with the fc1 grouped matmul;
+        8 SwiGLU;
+        9 fc2 grouped matmul fused with the combine exchange;
+       10 unpermute, weighting each row by its routing probability.
 [BG]  same page, "Background constraints" (背景约束): dispatch = AllToAllv then
       GroupedMatmul; combine = GroupedMatmul then AllToAllv.
 [MIG] same page, "Migration checks" (迁移检查): num_experts % ep_size == 0; a
